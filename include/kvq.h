@@ -1,0 +1,229 @@
+/*
+ * kvq.h -- C ABI of libkvq.so: a KIVI-style asymmetric quantized KV cache with a
+ * single-query GQA decode attention over it, for NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (sources named by page title and section):
+ *
+ *  - Quantizer: "54. KV Cache Quantization Strategies" (datawhale llm-algo-leetcode),
+ *    Step 2 and the Step 4 reference solution.  Key: per channel, absmax over the
+ *    tokens of a flushed group; Value: per token, absmax over head_dim;
+ *    scale = qmax / max(absmax, eps) (correctly rounded fp32 division);
+ *    code = clamp(round_half_even(x * scale), -qmax, qmax) with x * scale one fp32
+ *    multiply; restore = code / scale.
+ *  - Residual window: same page, Step 3 and ``append_and_partition``.  The newest
+ *    tokens stay in a high-precision window (the input dtype); only tokens that
+ *    overflow it are quantized; the quantized prefix is never rewritten.  This
+ *    library flushes whole groups: after an append leaves L tokens in the window,
+ *    F = floor((L - R) / G) groups of the oldest G tokens are quantized when
+ *    L >= R + G (F = 0 otherwise), each group with its own Key scales.  With G = 1
+ *    this is the page's rule flush = max(L - R, 0).  The held partition depends
+ *    only on a sequence's length T: quantized = G * floor((T - R) / G) when
+ *    T >= R + G, else 0; window = T - quantized, so R <= window < R + G once
+ *    anything is quantized.
+ *  - Decode attention: "KV Cache 与自回归视频生成" (jefxiong), section 3.1
+ *    (o_t = sum_j softmax_j(q_t . k_j / sqrt(d)) v_j over every held token, the
+ *    token appended in the same step included) and section 04 ``attn_step``
+ *    (query head h reads KV head h / g, g = n_q_heads / n_kv_heads).  The
+ *    quantized prefix is dequantized in registers; the split over the sequence
+ *    and the merge of partial softmax states follow section 05 (FlashDecoding).
+ *  - Byte ledger: "KV Cache 量化与压缩" (xuujii M005) sections 01 and 05.
+ *
+ * Conventions for every entry point:
+ *  - Status codes: KVQ_OK on success; any other value leaves the cache state
+ *    unchanged and sets a thread-local message readable with kvq_last_error().
+ *  - Memory: the caller owns all device memory (the cache arena, inputs and
+ *    outputs); the library allocates no device memory and keeps no pointer to
+ *    inputs or outputs after a call returns (the work is stream ordered).
+ *  - Streams: ``stream`` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  kvq_append and kvq_decode_attention* only enqueue work and never
+ *    synchronize; the caller orders calls on one cache (one stream, or events).
+ *  - Device pointers must be 16-byte aligned and the tensors contiguous.
+ *  - One cache holds one layer.  A multi-layer model creates one cache per layer.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_EINVAL = 1,       /* bad argument: config, pointer, range, alignment */
+  KVQ_ECAPACITY = 2,    /* an append would exceed a sequence's capacity */
+  KVQ_ENOMEM = 3,       /* the caller's arena is smaller than kvq_required_bytes */
+  KVQ_ECUDA = 4,        /* a CUDA call or kernel launch failed */
+  KVQ_EUNSUPPORTED = 5, /* valid but not implemented (e.g. head_dim, group size) */
+  KVQ_EDEVICE = 6       /* a kernel reported an error through the device status word */
+} kvq_status;
+
+typedef enum kvq_dtype {
+  KVQ_BF16 = 0, /* K/V/q inputs and the residual window are bfloat16 */
+  KVQ_FP32 = 1  /* ... float32 */
+} kvq_dtype;
+
+/* Cache configuration (one layer). */
+typedef struct kvq_config {
+  int32_t batch;        /* B: number of sequences, >= 1 */
+  int32_t n_kv_heads;   /* Hkv >= 1 */
+  int32_t n_q_heads;    /* Hq, a multiple of Hkv with g = Hq / Hkv <= 8 */
+  int32_t head_dim;     /* d: a multiple of 16, 16 <= d <= 256 */
+  int32_t residual_len; /* R > 0: tokens kept at input precision */
+  int32_t group;        /* G > 0, a multiple of 8: tokens quantized together */
+  int32_t qmax;         /* 1..7: signed 4-bit codes, two per byte;
+                           8..127: signed 8-bit codes */
+  int32_t dtype;        /* kvq_dtype of inputs and window */
+  float eps;            /* absmax floor for the scale, e.g. 1e-8f (> 0) */
+} kvq_config;
+
+/* Held-bytes ledger (whole cache, all sequences and KV heads). */
+typedef struct kvq_bytes_t {
+  int64_t code_bytes;   /* Key + Value codes: 4-bit packed or 8-bit */
+  int64_t n_scales;     /* Key: head_dim per flushed group; Value: one per token */
+  int64_t scale_bytes;  /* 4 * n_scales (scales are fp32) */
+  int64_t window_elems; /* Key + Value elements in the residual windows */
+  int64_t window_bytes; /* window_elems * sizeof(dtype) */
+  int64_t total;        /* code_bytes + scale_bytes + window_bytes */
+  int64_t allocated;    /* bytes of the arena the cache was created on (0 for kvq_ledger) */
+} kvq_bytes_t;
+
+/* Per-sequence bookkeeping, the counters of ``append_and_partition``. */
+typedef struct kvq_seq_info {
+  int64_t total;        /* tokens appended so far (T) */
+  int64_t quantized;    /* tokens in the quantized prefix (multiple of G) */
+  int64_t window;       /* tokens in the residual window (T - quantized) */
+  int64_t last_flushed; /* tokens quantized by the most recent append to this sequence */
+  int64_t n_groups;     /* quantized / G */
+  int64_t capacity;     /* capacity given at creation */
+} kvq_seq_info;
+
+/* Host view of one (sequence, KV head) unit, filled by kvq_export_unit.  Every
+ * pointer is a HOST buffer owned by the caller, sized from kvq_seq_info:
+ *   k_codes, v_codes: int8 [quantized][head_dim], logical (unpacked) codes
+ *   k_scales: float [quantized / G][head_dim];  v_scales: float [quantized]
+ *   window_k, window_v: float [window][head_dim], token order (oldest first)
+ * Any pointer may be NULL to skip that part. */
+typedef struct kvq_unit_view {
+  int8_t* k_codes;
+  int8_t* v_codes;
+  float* k_scales;
+  float* v_scales;
+  float* window_k;
+  float* window_v;
+} kvq_unit_view;
+
+/* Options of kvq_decode_attention_ex (zero-initialise for defaults). */
+typedef struct kvq_decode_opts {
+  int32_t kernel;      /* 0 = automatic; 1 = CUDA-core kernel (any supported
+                          shape); 2 = tensor-core kernel (bf16, head_dim 64/128,
+                          G a multiple of 32); KVQ_EUNSUPPORTED if not applicable */
+  int32_t chunk_pages; /* 0 = automatic; else quantized groups per split item */
+  void* split_start;   /* optional cudaEvent_t recorded just before the split kernel */
+  void* split_stop;    /* optional cudaEvent_t recorded just after it */
+} kvq_decode_opts;
+
+typedef struct kvq_cache kvq_cache; /* opaque host handle */
+
+/*
+ * Device-memory layout (documented so that pages can be inspected).
+ *
+ * Group page: one per (sequence, KV head, flushed group), written once by the
+ * flush and never again.  With bits = 4 (qmax <= 7) or 8, in order:
+ *   1. Key codes: G rows (token order) of head_dim*bits/8 bytes.  4-bit: byte i
+ *      holds channel 2i in bits 0-3 and channel 2i+1 in bits 4-7 (two's
+ *      complement nibbles); 8-bit: byte c is channel c.
+ *   2. Value codes in sub-tiles of 32 tokens (the last sub-tile holds G mod 32
+ *      tokens if G is not a multiple of 32).  A sub-tile of n tokens is head_dim
+ *      rows (channel order) of n*bits/8 bytes.  4-bit rows are little-endian
+ *      32-bit words; word w covers tokens 8w..8w+7 of the sub-tile and its
+ *      nibble j holds token 8w+2j for j < 4 and token 8w+2(j-4)+1 for j >= 4.
+ *      8-bit rows hold token i in byte i.
+ *   3. Key scales: head_dim fp32.   4. Value scales: G fp32.
+ *   Page size = 2*G*head_dim*bits/8 + 4*head_dim + 4*G bytes.
+ * Pages of one unit are contiguous and in token order.
+ * Residual window: per unit a ring of Rcap = G * (ceil(R / G) + 1) rows of
+ * head_dim elements (dtype) for Key and another for Value; token t of the
+ * sequence lives in row t mod Rcap.
+ */
+
+/* Bytes of device memory a cache with this configuration and these per-sequence
+ * capacities needs (capacity_per_seq: host array of ``batch`` token counts,
+ * each >= 1 and < 2^31).  Pure host function. */
+kvq_status kvq_required_bytes(const kvq_config* cfg, const int64_t* capacity_per_seq,
+                              size_t* out_bytes);
+
+/* Create a cache on caller-owned device memory of the current CUDA device
+ * (``device_mem``: 256-byte aligned, ``device_bytes`` >= kvq_required_bytes).
+ * All sequences start empty.  Writes a small layout table and clears the
+ * device status word with synchronous copies (set-up only).  *out receives the
+ * handle; destroy it with kvq_destroy.  The memory must outlive the handle. */
+kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
+                      size_t device_bytes, kvq_cache** out);
+
+/* Append ``n_tokens`` new tokens to each of the sequences
+ * [seq_begin, seq_begin + n_seqs) ("append_and_partition": cat with the window,
+ * then flush whole groups).  new_k, new_v: device [n_seqs][n_kv_heads]
+ * [n_tokens][head_dim] of the cache dtype (post-RoPE Keys).  Errors:
+ * KVQ_EINVAL (n_tokens <= 0, bad range, NULL or misaligned pointer),
+ * KVQ_ECAPACITY (total would exceed a capacity) -- both before any launch.
+ * For ragged prefills call once per sequence with n_seqs = 1. */
+kvq_status kvq_append(kvq_cache* cache, const void* new_k, const void* new_v, int64_t n_tokens,
+                      int32_t seq_begin, int32_t n_seqs, void* stream);
+
+/* Decode attention for every sequence: q device [batch][n_q_heads][head_dim] of
+ * the cache dtype; out device float [batch][n_q_heads][head_dim].  A sequence
+ * with no tokens yields zeros.  Uses the arena's split scratch region. */
+kvq_status kvq_decode_attention(kvq_cache* cache, const void* q, float* out, void* stream);
+
+/* Same as kvq_decode_attention with explicit options (kernel choice, split
+ * size, timing events); opts may be NULL. */
+kvq_status kvq_decode_attention_ex(kvq_cache* cache, const void* q, float* out, void* stream,
+                                   const kvq_decode_opts* opts);
+
+/* Held-bytes ledger of a live cache (host counters, no device access). */
+kvq_status kvq_bytes(const kvq_cache* cache, kvq_bytes_t* out);
+
+/* Ledger of a cache of this configuration holding tokens_per_seq[b] tokens per
+ * sequence (host array of ``batch`` counts); pure host function. */
+kvq_status kvq_ledger(const kvq_config* cfg, const int64_t* tokens_per_seq, kvq_bytes_t* out);
+
+/* Bookkeeping of sequence ``seq`` (host counters, no device access). */
+kvq_status kvq_seq_state(const kvq_cache* cache, int32_t seq, kvq_seq_info* out);
+
+/* Copy one unit's codes, scales and window to host buffers, decoded from the
+ * layout above (synchronizes ``stream``). */
+kvq_status kvq_export_unit(const kvq_cache* cache, int32_t seq, int32_t kv_head,
+                           const kvq_unit_view* view, void* stream);
+
+/* Copy the raw bytes of one unit's group pages (n_groups * page size bytes,
+ * token order) to the host buffer ``host_dst`` of ``dst_bytes`` bytes
+ * (synchronizes ``stream``). */
+kvq_status kvq_export_pages(const kvq_cache* cache, int32_t seq, int32_t kv_head, void* host_dst,
+                            size_t dst_bytes, void* stream);
+
+/* Read the device status word (synchronizes ``stream``).  0 means no kernel has
+ * reported an error; non-zero codes come from bounded waits that gave up.
+ * Returns KVQ_EDEVICE when the word is non-zero. */
+kvq_status kvq_device_status(const kvq_cache* cache, int32_t* out_word, void* stream);
+
+/* Size in bytes of one group page for this configuration (0 if invalid). */
+size_t kvq_page_bytes(const kvq_config* cfg);
+
+/* Kernel launches this library has enqueued in this process so far (all
+ * caches, all devices); a monotonically increasing counter for accounting. */
+uint64_t kvq_kernel_launches(void);
+
+/* Free the host handle (device memory stays the caller's).  NULL is ignored. */
+void kvq_destroy(kvq_cache* cache);
+
+/* Message of the last failed call on this thread ("" if none). */
+const char* kvq_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

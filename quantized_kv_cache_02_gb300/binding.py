@@ -1,0 +1,280 @@
+"""ctypes binding of libkvq.so (include/kvq.h): the same entry points under the
+same names, plus ``KVQCache``, a small owner object that allocates the arena
+with torch and passes torch's current CUDA stream.  Argument marshalling only:
+all work runs in the library's CUDA kernels.  Importing fails loudly when the
+library has not been built; there is no other implementation to fall back on.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+
+KVQ_OK, KVQ_EINVAL, KVQ_ECAPACITY, KVQ_ENOMEM, KVQ_ECUDA, KVQ_EUNSUPPORTED, KVQ_EDEVICE = range(7)
+KVQ_BF16, KVQ_FP32 = 0, 1
+STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ECAPACITY", 3: "KVQ_ENOMEM", 4: "KVQ_ECUDA",
+                5: "KVQ_EUNSUPPORTED", 6: "KVQ_EDEVICE"}
+
+# Every function include/kvq.h declares.
+EXPORTED = ("kvq_required_bytes", "kvq_create", "kvq_append", "kvq_decode_attention",
+            "kvq_decode_attention_ex", "kvq_bytes", "kvq_ledger", "kvq_seq_state", "kvq_export_unit",
+            "kvq_export_pages", "kvq_device_status", "kvq_page_bytes", "kvq_kernel_launches", "kvq_destroy",
+            "kvq_last_error")
+
+
+class kvq_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("residual_len", ctypes.c_int32), ("group", ctypes.c_int32),
+                ("qmax", ctypes.c_int32), ("dtype", ctypes.c_int32), ("eps", ctypes.c_float)]
+
+
+class kvq_bytes_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("code_bytes", "n_scales", "scale_bytes", "window_elems",
+                                              "window_bytes", "total", "allocated")]
+
+
+class kvq_seq_info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("total", "quantized", "window", "last_flushed", "n_groups",
+                                              "capacity")]
+
+
+class kvq_unit_view(ctypes.Structure):
+    _fields_ = [("k_codes", ctypes.c_void_p), ("v_codes", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p), ("window_k", ctypes.c_void_p), ("window_v", ctypes.c_void_p)]
+
+
+class kvq_decode_opts(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("chunk_pages", ctypes.c_int32), ("split_start", ctypes.c_void_p),
+                ("split_stop", ctypes.c_void_p)]
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libkvq.so and declare its signatures (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} not found: build it with __graft_entry__.build()")
+    lib = ctypes.CDLL(path)
+    P, V, I32, I64, SZ = ctypes.POINTER, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    sigs = {
+        "kvq_required_bytes": ([P(kvq_config), P(I64), P(SZ)], ctypes.c_int),
+        "kvq_create": ([P(kvq_config), P(I64), V, SZ, P(V)], ctypes.c_int),
+        "kvq_append": ([V, V, V, I64, I32, I32, V], ctypes.c_int),
+        "kvq_decode_attention": ([V, V, V, V], ctypes.c_int),
+        "kvq_decode_attention_ex": ([V, V, V, V, P(kvq_decode_opts)], ctypes.c_int),
+        "kvq_bytes": ([V, P(kvq_bytes_t)], ctypes.c_int),
+        "kvq_ledger": ([P(kvq_config), P(I64), P(kvq_bytes_t)], ctypes.c_int),
+        "kvq_seq_state": ([V, I32, P(kvq_seq_info)], ctypes.c_int),
+        "kvq_export_unit": ([V, I32, I32, P(kvq_unit_view), V], ctypes.c_int),
+        "kvq_export_pages": ([V, I32, I32, V, SZ, V], ctypes.c_int),
+        "kvq_device_status": ([V, P(I32), V], ctypes.c_int),
+        "kvq_page_bytes": ([P(kvq_config)], SZ),
+        "kvq_kernel_launches": ([], ctypes.c_uint64),
+        "kvq_destroy": ([V], None),
+        "kvq_last_error": ([], ctypes.c_char_p),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != KVQ_OK:
+        raise KVQError(status, load_library().kvq_last_error().decode())
+
+
+def make_config(batch, n_kv_heads, n_q_heads, head_dim, residual_len, group, qmax, dtype=KVQ_BF16, eps=1e-8):
+    return kvq_config(batch, n_kv_heads, n_q_heads, head_dim, residual_len, group, qmax, dtype, eps)
+
+
+def _i64_array(values):
+    values = [int(v) for v in values]
+    return (ctypes.c_int64 * len(values))(*values)
+
+
+# ---- thin wrappers with the C names --------------------------------------------
+
+def kvq_required_bytes(cfg: kvq_config, capacity) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().kvq_required_bytes(ctypes.byref(cfg), _i64_array(capacity), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_ledger(cfg: kvq_config, tokens) -> dict:
+    out = kvq_bytes_t()
+    _check(load_library().kvq_ledger(ctypes.byref(cfg), _i64_array(tokens), ctypes.byref(out)))
+    return {n: getattr(out, n) for n, _ in kvq_bytes_t._fields_}
+
+
+def kvq_page_bytes(cfg: kvq_config) -> int:
+    return load_library().kvq_page_bytes(ctypes.byref(cfg))
+
+
+def kvq_create(cfg: kvq_config, capacity, device_ptr: int, device_bytes: int) -> int:
+    handle = ctypes.c_void_p()
+    _check(load_library().kvq_create(ctypes.byref(cfg), _i64_array(capacity), ctypes.c_void_p(device_ptr),
+                                     device_bytes, ctypes.byref(handle)))
+    return handle.value
+
+
+def kvq_append(handle, new_k_ptr, new_v_ptr, n_tokens, seq_begin, n_seqs, stream) -> None:
+    _check(load_library().kvq_append(handle, new_k_ptr, new_v_ptr, n_tokens, seq_begin, n_seqs, stream))
+
+
+def kvq_decode_attention(handle, q_ptr, out_ptr, stream) -> None:
+    _check(load_library().kvq_decode_attention(handle, q_ptr, out_ptr, stream))
+
+
+def kvq_decode_attention_ex(handle, q_ptr, out_ptr, stream, kernel=0, chunk_pages=0, split_start=None,
+                            split_stop=None) -> None:
+    opts = kvq_decode_opts(kernel, chunk_pages, split_start, split_stop)
+    _check(load_library().kvq_decode_attention_ex(handle, q_ptr, out_ptr, stream, ctypes.byref(opts)))
+
+
+def kvq_bytes(handle) -> dict:
+    out = kvq_bytes_t()
+    _check(load_library().kvq_bytes(handle, ctypes.byref(out)))
+    return {n: getattr(out, n) for n, _ in kvq_bytes_t._fields_}
+
+
+def kvq_seq_state(handle, seq: int) -> dict:
+    out = kvq_seq_info()
+    _check(load_library().kvq_seq_state(handle, seq, ctypes.byref(out)))
+    return {n: getattr(out, n) for n, _ in kvq_seq_info._fields_}
+
+
+def kvq_export_unit(handle, seq, kv_head, view: kvq_unit_view, stream) -> None:
+    _check(load_library().kvq_export_unit(handle, seq, kv_head, ctypes.byref(view), stream))
+
+
+def kvq_export_pages(handle, seq, kv_head, dst_ptr, dst_bytes, stream) -> None:
+    _check(load_library().kvq_export_pages(handle, seq, kv_head, dst_ptr, dst_bytes, stream))
+
+
+def kvq_device_status(handle, stream) -> int:
+    word = ctypes.c_int32(0)
+    status = load_library().kvq_device_status(handle, ctypes.byref(word), stream)
+    if status not in (KVQ_OK, KVQ_EDEVICE):
+        _check(status)
+    return word.value
+
+
+def kvq_kernel_launches() -> int:
+    return load_library().kvq_kernel_launches()
+
+
+def kvq_destroy(handle) -> None:
+    if handle:
+        load_library().kvq_destroy(handle)
+
+
+# ---- owner object ------------------------------------------------------------
+
+class KVQCache:
+    """One layer's quantized cache on the current CUDA device.  The arena is a
+    torch uint8 tensor kept alive by this object; every call runs on torch's
+    current stream."""
+
+    def __init__(self, batch, n_kv_heads, n_q_heads, head_dim, residual_len, group, qmax, capacity,
+                 dtype="bf16", eps=1e-8, device=None):
+        import torch
+        self.torch = torch
+        self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.dtype = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.cfg = make_config(batch, n_kv_heads, n_q_heads, head_dim, residual_len, group, qmax,
+                               KVQ_BF16 if dtype == "bf16" else KVQ_FP32, eps)
+        if isinstance(capacity, int):
+            capacity = [capacity] * batch
+        self.capacity = list(capacity)
+        self.nbytes = kvq_required_bytes(self.cfg, self.capacity)
+        self.arena = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=self.device)
+        base = self.arena.data_ptr()
+        self._base = (base + 255) // 256 * 256
+        with torch.cuda.device(self.device):
+            self.handle = kvq_create(self.cfg, self.capacity, self._base, self.nbytes)
+
+    def _stream(self):
+        return self.torch.cuda.current_stream(self.device).cuda_stream
+
+    def _check_input(self, t, shape):
+        assert t.is_cuda and t.device == self.device, "input must live on the cache's device"
+        assert t.dtype == self.dtype and t.is_contiguous(), f"input must be contiguous {self.dtype}"
+        assert tuple(t.shape) == tuple(shape), f"expected shape {tuple(shape)}, got {tuple(t.shape)}"
+
+    def append(self, new_k, new_v, seq_begin=0):
+        """new_k, new_v: [n_seqs, n_kv_heads, n_tokens, head_dim] on the device."""
+        n_seqs, _, n, _ = new_k.shape
+        shape = (n_seqs, self.cfg.n_kv_heads, n, self.cfg.head_dim)
+        self._check_input(new_k, shape)
+        self._check_input(new_v, shape)
+        kvq_append(self.handle, new_k.data_ptr(), new_v.data_ptr(), n, seq_begin, n_seqs, self._stream())
+
+    def decode_attention(self, q, out=None, kernel=0, chunk_pages=0, split_start=None, split_stop=None):
+        """q: [batch, n_q_heads, head_dim]; returns float32 [batch, n_q_heads, head_dim]."""
+        shape = (self.cfg.batch, self.cfg.n_q_heads, self.cfg.head_dim)
+        self._check_input(q, shape)
+        if out is None:
+            out = self.torch.empty(shape, dtype=self.torch.float32, device=self.device)
+        if kernel == 0 and chunk_pages == 0 and split_start is None and split_stop is None:
+            kvq_decode_attention(self.handle, q.data_ptr(), out.data_ptr(), self._stream())
+        else:
+            kvq_decode_attention_ex(self.handle, q.data_ptr(), out.data_ptr(), self._stream(), kernel, chunk_pages,
+                                    split_start, split_stop)
+        return out
+
+    def bytes(self):
+        return kvq_bytes(self.handle)
+
+    def seq_state(self, seq):
+        return kvq_seq_state(self.handle, seq)
+
+    def export_unit(self, seq, kv_head):
+        """Host numpy copies of one unit: dict of k_codes, v_codes, k_scales,
+        v_scales, window_k, window_v (token order)."""
+        import numpy as np
+        st = self.seq_state(seq)
+        Q, W, D, G = st["quantized"], st["window"], self.cfg.head_dim, self.cfg.group
+        arrs = {"k_codes": np.zeros((Q, D), np.int8), "v_codes": np.zeros((Q, D), np.int8),
+                "k_scales": np.zeros((Q // G, D), np.float32), "v_scales": np.zeros((Q,), np.float32),
+                "window_k": np.zeros((W, D), np.float32), "window_v": np.zeros((W, D), np.float32)}
+        view = kvq_unit_view(*[a.ctypes.data for a in arrs.values()])
+        kvq_export_unit(self.handle, seq, kv_head, view, self._stream())
+        return arrs
+
+    def export_pages(self, seq, kv_head):
+        import numpy as np
+        st = self.seq_state(seq)
+        n = (st["quantized"] // self.cfg.group) * kvq_page_bytes(self.cfg)
+        buf = np.zeros(max(n, 1), np.uint8)
+        kvq_export_pages(self.handle, seq, kv_head, buf.ctypes.data, buf.nbytes, self._stream())
+        return buf[:n].tobytes()
+
+    def device_status(self):
+        return kvq_device_status(self.handle, self._stream())
+
+    def close(self):
+        if getattr(self, "handle", None):
+            kvq_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,201 @@
+// Append / flush / quantize / pack.
+//
+// One launch appends n tokens to each sequence of [seq_begin, seq_begin + n_seqs):
+//   * flush blocks (blockIdx.x < flush_blocks): one CTA per (group, sequence, KV
+//     head) quantizes the oldest G tokens of the held tail -- Key per channel
+//     (absmax over the group's tokens), Value per token (absmax over head_dim),
+//     scale = qmax / max(absmax, eps), code = clamp(rint(x * scale)) -- and writes
+//     the group page once ("54. KV Cache Quantization Strategies", Step 2 and
+//     the Step 4 reference solution; the grouped flush rule is in kvq.h);
+//   * window block (the last blockIdx.x): copies the new tokens that stay in the
+//     residual window into the per-unit ring (preallocated, written in place
+//     rather than concatenated, as "KV Cache 与自回归视频生成" section 05 argues).
+// Tokens being flushed come from the ring (old window) or straight from the
+// input (new tokens), so a long prefill never passes through the ring.
+// Bit exactness: absmax is exact, the division is __fdiv_rn, the product is a
+// separately rounded __fmul_rn, rintf rounds half to even; no fast-math.
+
+#include <cuda_bf16.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kAppendThreads = 256;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
+  float r = rintf(__fmul_rn(x, scale));
+  r = fminf(fmaxf(r, -qmax), qmax);
+  return (int)r;
+}
+
+// Stage the G x D tile of tokens [t_first, t_first + G) as fp32 in shared memory.
+template <typename T>
+__device__ void load_group(float* tile, const T* ring, const T* input, int64_t t_first, int64_t T0,
+                           int G, int D, int Rcap) {
+  const int n = G * D;
+  for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
+    const int tl = idx / D, c = idx - tl * D;
+    const int64_t t = t_first + tl;
+    const T v = t < T0 ? ring[(t % Rcap) * D + c] : input[(t - T0) * D + c];
+    tile[idx] = to_f32(v);
+  }
+}
+
+template <typename T, int BITS>
+__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
+  extern __shared__ float smem[];
+  const int i = blockIdx.y;
+  const int h = blockIdx.z;
+  const int b = p.seq_begin + i;
+  const int D = p.D, G = p.G, Rcap = p.Rcap;
+  const int64_t T0 = p.old[i].total;
+  const int64_t Q0 = p.old[i].quantized;
+  const int64_t n = p.n;
+  const int64_t F = flush_groups(T0 - Q0, n, p.R, G);
+  const int64_t Q1 = Q0 + F * G;
+  const int64_t T1 = T0 + n;
+  const int64_t unit = (int64_t)b * p.Hkv + h;
+  const T* in_k = reinterpret_cast<const T*>(p.new_k) + ((int64_t)i * p.Hkv + h) * n * D;
+  const T* in_v = reinterpret_cast<const T*>(p.new_v) + ((int64_t)i * p.Hkv + h) * n * D;
+  T* ring_k = reinterpret_cast<T*>(p.ring_k) + unit * Rcap * D;
+  T* ring_v = reinterpret_cast<T*>(p.ring_v) + unit * Rcap * D;
+
+  if ((int)blockIdx.x >= p.flush_blocks) {
+    // Window block: the new tokens that stay in the residual window.
+    const int64_t t_lo = Q1 > T0 ? Q1 : T0;
+    const int64_t count = (T1 - t_lo) * D;
+    for (int64_t idx = threadIdx.x; idx < count; idx += blockDim.x) {
+      const int64_t t = t_lo + idx / D;
+      const int c = (int)(idx % D);
+      const int64_t src = (t - T0) * D + c;
+      const int64_t dst = (t % Rcap) * D + c;
+      ring_k[dst] = in_k[src];
+      ring_v[dst] = in_v[src];
+    }
+    return;
+  }
+
+  const int64_t j = blockIdx.x;
+  if (j >= F) return;
+  const int64_t t_first = Q0 + j * G;
+  const PageGeom& geom = p.geom;
+  uint8_t* page = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride +
+                  (t_first / G) * geom.page_bytes;
+  float* tile = smem;
+  float* sK = tile + G * D;
+  float* sV = sK + D;
+  const float qmax = (float)p.qmax;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+
+  // ---- Key: per-channel absmax over the group's tokens --------------------
+  load_group<T>(tile, ring_k, in_k, t_first, T0, G, D, Rcap);
+  __syncthreads();
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float a = 0.f;
+    for (int t = 0; t < G; ++t) a = fmaxf(a, fabsf(tile[t * D + c]));
+    sK[c] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+  }
+  __syncthreads();
+  {
+    // rows of D*BITS/8 bytes, written as 32-bit words
+    constexpr int kPerWord = 32 / BITS;  // codes per 32-bit word
+    const int words_per_row = D / kPerWord;
+    uint32_t* kc = reinterpret_cast<uint32_t*>(page);
+    for (int idx = threadIdx.x; idx < G * words_per_row; idx += blockDim.x) {
+      const int t = idx / words_per_row, w = idx - t * words_per_row;
+      uint32_t word = 0;
+#pragma unroll
+      for (int k = 0; k < kPerWord; ++k) {
+        const int c = w * kPerWord + k;
+        const int code = quantize_one(tile[t * D + c], sK[c], qmax);
+        word |= ((uint32_t)code & ((1u << BITS) - 1u)) << (BITS * k);
+      }
+      kc[idx] = word;
+    }
+    float* ks = reinterpret_cast<float*>(page + geom.kscale_off);
+    for (int c = threadIdx.x; c < D; c += blockDim.x) ks[c] = sK[c];
+  }
+  __syncthreads();
+
+  // ---- Value: per-token absmax over head_dim -----------------------------
+  load_group<T>(tile, ring_v, in_v, t_first, T0, G, D, Rcap);
+  __syncthreads();
+  for (int t = warp; t < G; t += nwarps) {
+    float a = 0.f;
+    for (int c = lane; c < D; c += 32) a = fmaxf(a, fabsf(tile[t * D + c]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) sV[t] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+  }
+  __syncthreads();
+  {
+    uint8_t* vbase = page + geom.code_bytes;
+    const int n_sub = (G + 31) / 32;
+    for (int st = 0; st < n_sub; ++st) {
+      const int n_st = min(32, G - 32 * st);
+      uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
+      if (BITS == 4) {
+        const int nw = n_st / 8;  // words per channel row
+        for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
+          const int c = idx / nw, w = idx - c * nw;
+          uint32_t word = 0;
+#pragma unroll
+          for (int jn = 0; jn < 8; ++jn) {
+            const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
+            const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
+            word |= ((uint32_t)code & 0xFu) << (4 * jn);
+          }
+          vc[idx] = word;
+        }
+      } else {
+        const int nw = n_st / 4;
+        for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
+          const int c = idx / nw, w = idx - c * nw;
+          uint32_t word = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int tok = 32 * st + 4 * w + k;
+            const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
+            word |= ((uint32_t)code & 0xFFu) << (8 * k);
+          }
+          vc[idx] = word;
+        }
+      }
+    }
+    float* vs = reinterpret_cast<float*>(page + geom.vscale_off);
+    for (int t = threadIdx.x; t < G; t += blockDim.x) vs[t] = sV[t];
+  }
+}
+
+template <typename T, int BITS>
+cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
+  const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
+  const size_t smem = p.flush_blocks ? ((size_t)p.G * p.D + p.D + p.G) * sizeof(float) : 0;
+  append_kernel<T, BITS><<<grid, kAppendThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, int BITS>
+cudaError_t configure_t(size_t smem) {
+  return cudaFuncSetAttribute(append_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)smem);
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s) {
+  if (dtype == 0) return p.bits == 4 ? launch_t<__nv_bfloat16, 4>(p, s) : launch_t<__nv_bfloat16, 8>(p, s);
+  return p.bits == 4 ? launch_t<float, 4>(p, s) : launch_t<float, 8>(p, s);
+}
+
+cudaError_t configure_append(int dtype, int bits, size_t smem_bytes) {
+  if (dtype == 0) return bits == 4 ? configure_t<__nv_bfloat16, 4>(smem_bytes) : configure_t<__nv_bfloat16, 8>(smem_bytes);
+  return bits == 4 ? configure_t<float, 4>(smem_bytes) : configure_t<float, 8>(smem_bytes);
+}
+
+}  // namespace kvq

@@ -1,0 +1,600 @@
+// Host side of libkvq: the C ABI of include/kvq.h.
+//
+// Bookkeeping follows "54. KV Cache Quantization Strategies" (append_and_partition:
+// total / quantized / flushed counters, validation of the inputs) with the
+// grouped flush rule; the byte ledger follows "KV Cache 量化与压缩" sections 01/05.
+// Counters live on the host and travel to the kernels in the launch parameter
+// block, so no call synchronizes with the device.
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/kvq.h"
+#include "kvq_internal.h"
+
+using kvq::SeqCounters;
+
+struct kvq_cache {
+  kvq_config cfg;
+  int bits;
+  int esize;        // bytes per window / input element
+  int rcap;         // ring rows per unit
+  int g;            // query heads per KV head
+  kvq::PageGeom geom;
+  std::vector<int64_t> cap;         // per sequence
+  std::vector<int64_t> pages_cap;   // group pages per unit, per sequence
+  std::vector<int64_t> page_base;   // byte offset of (seq, head 0, page 0)
+  std::vector<int32_t> total, quantized, last_flushed;
+  int max_splits;
+  int min_chunk_pages;
+  int n_sm;
+  int device;
+  // arena
+  uint8_t* base;
+  size_t arena_bytes;
+  int32_t* status;
+  kvq::SeqLayout* layout;
+  uint8_t* pages;
+  void* ring_k;
+  void* ring_v;
+  float* partials;
+};
+
+namespace {
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_launches{0};
+
+kvq_status fail(kvq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int64_t kMinChunkTokens = 256;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+kvq_status check_config(const kvq_config* c) {
+  if (!c) return fail(KVQ_EINVAL, "config is NULL");
+  if (c->batch < 1) return fail(KVQ_EINVAL, "batch must be >= 1 (got %d)", c->batch);
+  if (c->n_kv_heads < 1) return fail(KVQ_EINVAL, "n_kv_heads must be >= 1");
+  if (c->n_q_heads < 1 || c->n_q_heads % c->n_kv_heads != 0)
+    return fail(KVQ_EINVAL, "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)", c->n_q_heads,
+                c->n_kv_heads);
+  if (c->n_q_heads / c->n_kv_heads > kvq::kMaxGqa)
+    return fail(KVQ_EUNSUPPORTED, "query heads per KV head must be <= %d", kvq::kMaxGqa);
+  if (c->head_dim < 16 || c->head_dim > 256 || c->head_dim % 16 != 0)
+    return fail(KVQ_EUNSUPPORTED, "head_dim must be a multiple of 16 in [16, 256] (got %d)", c->head_dim);
+  if (c->residual_len <= 0) return fail(KVQ_EINVAL, "residual_length must be positive");
+  if (c->group <= 0 || c->group % 8 != 0)
+    return fail(KVQ_EUNSUPPORTED, "group must be a positive multiple of 8 (got %d)", c->group);
+  if (c->qmax < 1 || c->qmax > 127) return fail(KVQ_EINVAL, "qmax must be in [1, 127] (got %d)", c->qmax);
+  if (c->dtype != KVQ_BF16 && c->dtype != KVQ_FP32) return fail(KVQ_EINVAL, "unknown dtype %d", c->dtype);
+  if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return fail(KVQ_EINVAL, "eps must be positive and finite");
+  const size_t flush_smem = ((size_t)c->group * c->head_dim + c->head_dim + c->group) * sizeof(float);
+  if (flush_smem > 200 * 1024)
+    return fail(KVQ_EUNSUPPORTED, "group * head_dim too large for one flush tile (%zu bytes)", flush_smem);
+  return KVQ_OK;
+}
+
+int bits_of(const kvq_config* c) { return c->qmax <= 7 ? 4 : 8; }
+int esize_of(const kvq_config* c) { return c->dtype == KVQ_BF16 ? 2 : 4; }
+int rcap_of(const kvq_config* c) {
+  return c->group * ((c->residual_len + c->group - 1) / c->group + 1);
+}
+
+struct ArenaPlan {
+  size_t status, layout, pages, ring_k, ring_v, partials, total;
+  std::vector<int64_t> pages_cap, page_base;
+  int max_splits, min_chunk_pages;
+};
+
+kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a) {
+  if (!cap) return fail(KVQ_EINVAL, "capacity_per_seq is NULL");
+  const kvq::PageGeom geom = kvq::make_geom(c->group, c->head_dim, bits_of(c));
+  a->pages_cap.assign(c->batch, 0);
+  a->page_base.assign(c->batch, 0);
+  int64_t pmax = 0, off = 0;
+  for (int b = 0; b < c->batch; ++b) {
+    if (cap[b] < 1 || cap[b] >= (int64_t(1) << 31))
+      return fail(KVQ_EINVAL, "capacity of sequence %d must be in [1, 2^31) (got %lld)", b, (long long)cap[b]);
+    a->pages_cap[b] = cap[b] / c->group;
+    a->page_base[b] = off;
+    off += (int64_t)c->n_kv_heads * a->pages_cap[b] * geom.page_bytes;
+    pmax = std::max(pmax, a->pages_cap[b]);
+  }
+  a->min_chunk_pages = (int)std::max<int64_t>(1, (kMinChunkTokens + c->group - 1) / c->group);
+  a->max_splits = (int)((pmax + a->min_chunk_pages - 1) / a->min_chunk_pages) + 1;
+  const int g = c->n_q_heads / c->n_kv_heads;
+  const size_t units = (size_t)c->batch * c->n_kv_heads;
+  size_t o = 0;
+  a->status = o;
+  o = align_up(o + sizeof(int32_t), kAlign);
+  a->layout = o;
+  o = align_up(o + (size_t)c->batch * sizeof(kvq::SeqLayout), kAlign);
+  a->pages = o;
+  o = align_up(o + (size_t)off, kAlign);
+  const size_t ring = units * rcap_of(c) * c->head_dim * esize_of(c);
+  a->ring_k = o;
+  o = align_up(o + ring, kAlign);
+  a->ring_v = o;
+  o = align_up(o + ring, kAlign);
+  a->partials = o;
+  o = align_up(o + units * a->max_splits * g * (c->head_dim + 2) * sizeof(float), kAlign);
+  a->total = o;
+  return KVQ_OK;
+}
+
+bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+void fill_counters(const kvq_cache* c, int seq_begin, int n, SeqCounters* out) {
+  for (int i = 0; i < n; ++i) {
+    out[i].total = c->total[seq_begin + i];
+    out[i].quantized = c->quantized[seq_begin + i];
+  }
+}
+
+// Split plan for the decode launch over sequences [s0, s0 + n).
+void plan_splits(const kvq_cache* c, int s0, int n, int requested, int* chunk, int* grid_splits) {
+  int64_t total_pages = 0, pmax = 0;
+  for (int i = s0; i < s0 + n; ++i) {
+    const int64_t P = c->quantized[i] / c->cfg.group;
+    total_pages += P * c->cfg.n_kv_heads;
+    pmax = std::max(pmax, P);
+  }
+  int64_t ch;
+  if (requested > 0) {
+    ch = requested;
+  } else {
+    const int64_t target = (int64_t)c->n_sm * 8;
+    ch = std::max<int64_t>(c->min_chunk_pages, (total_pages + target - 1) / target);
+  }
+  ch = std::max<int64_t>(ch, (pmax + c->max_splits - 2) / std::max(1, c->max_splits - 1));
+  ch = std::max<int64_t>(ch, 1);
+  *chunk = (int)ch;
+  *grid_splits = (int)((pmax + ch - 1) / ch);
+}
+
+void base_decode_params(const kvq_cache* c, kvq::DecodeParams* p) {
+  memset(p, 0, sizeof *p);
+  p->D = c->cfg.head_dim;
+  p->Hkv = c->cfg.n_kv_heads;
+  p->Hq = c->cfg.n_q_heads;
+  p->g = c->g;
+  p->G = c->cfg.group;
+  p->Rcap = c->rcap;
+  p->bits = c->bits;
+  p->eps = c->cfg.eps;
+  p->qk_scale = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
+  p->geom = c->geom;
+  p->pages = c->pages;
+  p->layout = c->layout;
+  p->ring_k = c->ring_k;
+  p->ring_v = c->ring_v;
+  p->partials = c->partials;
+  p->max_splits = c->max_splits;
+  p->status = c->status;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_last_error(void) { return g_err.c_str(); }
+
+uint64_t kvq_kernel_launches(void) { return g_launches.load(); }
+
+size_t kvq_page_bytes(const kvq_config* cfg) {
+  if (check_config(cfg) != KVQ_OK) return 0;
+  return (size_t)kvq::make_geom(cfg->group, cfg->head_dim, bits_of(cfg)).page_bytes;
+}
+
+kvq_status kvq_required_bytes(const kvq_config* cfg, const int64_t* capacity_per_seq, size_t* out_bytes) {
+  if (!out_bytes) return fail(KVQ_EINVAL, "out_bytes is NULL");
+  kvq_status st = check_config(cfg);
+  if (st != KVQ_OK) return st;
+  ArenaPlan a;
+  st = plan_arena(cfg, capacity_per_seq, &a);
+  if (st != KVQ_OK) return st;
+  *out_bytes = a.total;
+  return KVQ_OK;
+}
+
+kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
+                      size_t device_bytes, kvq_cache** out) {
+  if (!out) return fail(KVQ_EINVAL, "out is NULL");
+  *out = nullptr;
+  kvq_status st = check_config(cfg);
+  if (st != KVQ_OK) return st;
+  ArenaPlan a;
+  st = plan_arena(cfg, capacity_per_seq, &a);
+  if (st != KVQ_OK) return st;
+  if (!device_mem || ((uintptr_t)device_mem & (kAlign - 1)))
+    return fail(KVQ_EINVAL, "device_mem must be a 256-byte aligned device pointer");
+  if (device_bytes < a.total)
+    return fail(KVQ_ENOMEM, "arena of %zu bytes is smaller than the %zu bytes required", device_bytes, a.total);
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, device_mem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(KVQ_EINVAL, "device_mem is not device memory");
+
+  kvq_cache* c = new kvq_cache();
+  c->cfg = *cfg;
+  c->bits = bits_of(cfg);
+  c->esize = esize_of(cfg);
+  c->rcap = rcap_of(cfg);
+  c->g = cfg->n_q_heads / cfg->n_kv_heads;
+  c->geom = kvq::make_geom(cfg->group, cfg->head_dim, c->bits);
+  c->cap.assign(capacity_per_seq, capacity_per_seq + cfg->batch);
+  c->pages_cap = a.pages_cap;
+  c->page_base = a.page_base;
+  c->total.assign(cfg->batch, 0);
+  c->quantized.assign(cfg->batch, 0);
+  c->last_flushed.assign(cfg->batch, 0);
+  c->max_splits = a.max_splits;
+  c->min_chunk_pages = a.min_chunk_pages;
+  c->device = attr.device;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != attr.device) cudaSetDevice(attr.device);
+  e = cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, attr.device);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "cudaDeviceGetAttribute");
+  }
+  c->base = static_cast<uint8_t*>(device_mem);
+  c->arena_bytes = device_bytes;
+  c->status = reinterpret_cast<int32_t*>(c->base + a.status);
+  c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + a.layout);
+  c->pages = c->base + a.pages;
+  c->ring_k = c->base + a.ring_k;
+  c->ring_v = c->base + a.ring_v;
+  c->partials = reinterpret_cast<float*>(c->base + a.partials);
+
+  std::vector<kvq::SeqLayout> table(cfg->batch);
+  for (int b = 0; b < cfg->batch; ++b) {
+    table[b].page_base = a.page_base[b];
+    table[b].unit_stride = a.pages_cap[b] * c->geom.page_bytes;
+  }
+  e = cudaMemcpy(c->layout, table.data(), table.size() * sizeof(kvq::SeqLayout), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) {
+    const size_t smem = ((size_t)cfg->group * cfg->head_dim + cfg->head_dim + cfg->group) * sizeof(float);
+    e = kvq::configure_append(cfg->dtype, c->bits, smem);
+  }
+  if (cur != attr.device) cudaSetDevice(cur);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "kvq_create set-up");
+  }
+  *out = c;
+  return KVQ_OK;
+}
+
+void kvq_destroy(kvq_cache* cache) { delete cache; }
+
+kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens, int32_t seq_begin,
+                      int32_t n_seqs, void* stream) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (n_tokens <= 0) return fail(KVQ_EINVAL, "n_tokens must be positive (got %lld)", (long long)n_tokens);
+  if (n_seqs <= 0 || seq_begin < 0 || seq_begin + (int64_t)n_seqs > c->cfg.batch)
+    return fail(KVQ_EINVAL, "sequence range [%d, %d) is outside [0, %d)", seq_begin, seq_begin + n_seqs,
+                c->cfg.batch);
+  if (!aligned16(new_k) || !aligned16(new_v))
+    return fail(KVQ_EINVAL, "new_k / new_v must be non-NULL 16-byte aligned device pointers");
+  for (int b = seq_begin; b < seq_begin + n_seqs; ++b) {
+    if (c->total[b] + n_tokens > c->cap[b])
+      return fail(KVQ_ECAPACITY, "sequence %d: %lld + %lld tokens exceed its capacity %lld", b,
+                  (long long)c->total[b], (long long)n_tokens, (long long)c->cap[b]);
+  }
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t R = c->cfg.residual_len, G = c->cfg.group;
+  const int64_t per_seq_elems = (int64_t)c->cfg.n_kv_heads * n_tokens * c->cfg.head_dim;
+  for (int s0 = seq_begin; s0 < seq_begin + n_seqs; s0 += kvq::kMaxSeqsPerLaunch) {
+    const int n = std::min(kvq::kMaxSeqsPerLaunch, seq_begin + n_seqs - s0);
+    kvq::AppendParams p;
+    memset(&p, 0, sizeof p);
+    p.D = c->cfg.head_dim;
+    p.Hkv = c->cfg.n_kv_heads;
+    p.G = (int)G;
+    p.R = (int)R;
+    p.Rcap = c->rcap;
+    p.qmax = c->cfg.qmax;
+    p.bits = c->bits;
+    p.eps = c->cfg.eps;
+    p.geom = c->geom;
+    p.pages = c->pages;
+    p.layout = c->layout;
+    p.ring_k = c->ring_k;
+    p.ring_v = c->ring_v;
+    const int64_t in_off = (int64_t)(s0 - seq_begin) * per_seq_elems * c->esize;
+    p.new_k = static_cast<const uint8_t*>(new_k) + in_off;
+    p.new_v = static_cast<const uint8_t*>(new_v) + in_off;
+    p.n = n_tokens;
+    p.seq_begin = s0;
+    p.n_seqs = n;
+    fill_counters(c, s0, n, p.old);
+    int64_t fmax = 0;
+    bool overlap = false;
+    for (int i = 0; i < n; ++i) {
+      const int64_t w = p.old[i].total - p.old[i].quantized;
+      const int64_t F = kvq::flush_groups(w, n_tokens, R, G);
+      fmax = std::max(fmax, F);
+      // ring rows read by the flush and written by the window copy coincide only
+      // when the old window plus the new tokens exceed the ring
+      if (F > 0 && w + n_tokens > c->rcap) overlap = true;
+    }
+    cudaError_t e;
+    if (!overlap) {
+      p.flush_blocks = (int)fmax;
+      p.window_blocks = 1;
+      e = kvq::launch_append(p, c->cfg.dtype, s);
+      g_launches += 1;
+    } else {
+      p.flush_blocks = (int)fmax;
+      p.window_blocks = 0;
+      e = kvq::launch_append(p, c->cfg.dtype, s);
+      g_launches += 1;
+      if (e == cudaSuccess) {
+        p.flush_blocks = 0;
+        p.window_blocks = 1;
+        e = kvq::launch_append(p, c->cfg.dtype, s);
+        g_launches += 1;
+      }
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  }
+  for (int b = seq_begin; b < seq_begin + n_seqs; ++b) {
+    const int64_t w = c->total[b] - c->quantized[b];
+    const int64_t F = kvq::flush_groups(w, n_tokens, R, G);
+    c->quantized[b] += (int32_t)(F * G);
+    c->total[b] += (int32_t)n_tokens;
+    c->last_flushed[b] = (int32_t)(F * G);
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void* stream,
+                                   const kvq_decode_opts* opts) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
+  const int kernel = opts ? opts->kernel : 0;
+  if (kernel < 0 || kernel > 2) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
+  const bool mma_ok = c->cfg.dtype == KVQ_BF16 && (c->cfg.head_dim == 64 || c->cfg.head_dim == 128) &&
+                      c->cfg.group % 32 == 0;
+  if (kernel == 2 && !mma_ok)
+    return fail(KVQ_EUNSUPPORTED, "tensor-core kernel needs bf16, head_dim 64/128 and group %% 32 == 0");
+  const bool use_mma = kernel == 2 || (kernel == 0 && mma_ok);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (opts && opts->split_start) {
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opts->split_start), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  }
+  struct Batch {
+    int s0, n, chunk, grid;
+  };
+  std::vector<Batch> batches;
+  for (int s0 = 0; s0 < c->cfg.batch; s0 += kvq::kMaxSeqsPerLaunch) {
+    Batch bt;
+    bt.s0 = s0;
+    bt.n = std::min(kvq::kMaxSeqsPerLaunch, c->cfg.batch - s0);
+    plan_splits(c, bt.s0, bt.n, opts ? opts->chunk_pages : 0, &bt.chunk, &bt.grid);
+    kvq::DecodeParams p;
+    base_decode_params(c, &p);
+    p.q = q;
+    p.chunk_pages = bt.chunk;
+    p.grid_splits = bt.grid;
+    p.seq_begin = bt.s0;
+    p.n_seqs = bt.n;
+    fill_counters(c, bt.s0, bt.n, p.ctr);
+    cudaError_t e;
+    if (use_mma) {
+      int supported = 0;
+      e = kvq::launch_decode_mma(p, s, &supported);
+      if (e == cudaSuccess && !supported) return fail(KVQ_EUNSUPPORTED, "tensor-core kernel not applicable");
+    } else {
+      e = kvq::launch_decode_simt(p, c->cfg.dtype, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
+    g_launches += 1;
+    batches.push_back(bt);
+  }
+  if (opts && opts->split_stop) {
+    const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opts->split_stop), s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  }
+  for (const Batch& bt : batches) {
+    kvq::CombineParams cp;
+    memset(&cp, 0, sizeof cp);
+    cp.D = c->cfg.head_dim;
+    cp.Hkv = c->cfg.n_kv_heads;
+    cp.Hq = c->cfg.n_q_heads;
+    cp.g = c->g;
+    cp.G = c->cfg.group;
+    cp.max_splits = c->max_splits;
+    cp.chunk_pages = bt.chunk;
+    cp.partials = c->partials;
+    cp.out = out;
+    cp.seq_begin = bt.s0;
+    cp.n_seqs = bt.n;
+    fill_counters(c, bt.s0, bt.n, cp.ctr);
+    const cudaError_t e = kvq::launch_combine(cp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    g_launches += 1;
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(kvq_cache* c, const void* q, float* out, void* stream) {
+  return kvq_decode_attention_ex(c, q, out, stream, nullptr);
+}
+
+kvq_status kvq_ledger(const kvq_config* cfg, const int64_t* tokens_per_seq, kvq_bytes_t* out) {
+  if (!out || !tokens_per_seq) return fail(KVQ_EINVAL, "NULL argument");
+  const kvq_status st = check_config(cfg);
+  if (st != KVQ_OK) return st;
+  const int64_t R = cfg->residual_len, G = cfg->group, H = cfg->n_kv_heads, D = cfg->head_dim;
+  const int bits = bits_of(cfg);
+  kvq_bytes_t r;
+  memset(&r, 0, sizeof r);
+  for (int b = 0; b < cfg->batch; ++b) {
+    const int64_t T = tokens_per_seq[b];
+    if (T < 0) return fail(KVQ_EINVAL, "negative token count for sequence %d", b);
+    const int64_t Q = T >= R + G ? (T - R) / G * G : 0;
+    r.code_bytes += 2 * H * Q * D * bits / 8;
+    r.n_scales += H * ((Q / G) * D + Q);
+    r.window_elems += 2 * H * (T - Q) * D;
+  }
+  r.scale_bytes = 4 * r.n_scales;
+  r.window_bytes = r.window_elems * esize_of(cfg);
+  r.total = r.code_bytes + r.scale_bytes + r.window_bytes;
+  *out = r;
+  return KVQ_OK;
+}
+
+kvq_status kvq_bytes(const kvq_cache* c, kvq_bytes_t* out) {
+  if (!c || !out) return fail(KVQ_EINVAL, "NULL argument");
+  std::vector<int64_t> t(c->total.begin(), c->total.end());
+  const kvq_status st = kvq_ledger(&c->cfg, t.data(), out);
+  if (st == KVQ_OK) out->allocated = (int64_t)c->arena_bytes;
+  return st;
+}
+
+kvq_status kvq_seq_state(const kvq_cache* c, int32_t seq, kvq_seq_info* out) {
+  if (!c || !out) return fail(KVQ_EINVAL, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.batch) return fail(KVQ_EINVAL, "sequence %d out of range", seq);
+  out->total = c->total[seq];
+  out->quantized = c->quantized[seq];
+  out->window = c->total[seq] - c->quantized[seq];
+  out->last_flushed = c->last_flushed[seq];
+  out->n_groups = c->quantized[seq] / c->cfg.group;
+  out->capacity = c->cap[seq];
+  return KVQ_OK;
+}
+
+kvq_status kvq_export_pages(const kvq_cache* c, int32_t seq, int32_t kv_head, void* host_dst, size_t dst_bytes,
+                            void* stream) {
+  if (!c || !host_dst) return fail(KVQ_EINVAL, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.batch || kv_head < 0 || kv_head >= c->cfg.n_kv_heads)
+    return fail(KVQ_EINVAL, "unit (%d, %d) out of range", seq, kv_head);
+  const size_t bytes = (size_t)(c->quantized[seq] / c->cfg.group) * c->geom.page_bytes;
+  if (dst_bytes < bytes) return fail(KVQ_EINVAL, "host buffer of %zu bytes < %zu", dst_bytes, bytes);
+  if (bytes == 0) return KVQ_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint8_t* src = c->pages + c->page_base[seq] + (int64_t)kv_head * c->pages_cap[seq] * c->geom.page_bytes;
+  cudaError_t e = cudaMemcpyAsync(host_dst, src, bytes, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_export_pages");
+}
+
+kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, const kvq_unit_view* view,
+                           void* stream) {
+  if (!c || !view) return fail(KVQ_EINVAL, "NULL argument");
+  if (seq < 0 || seq >= c->cfg.batch || kv_head < 0 || kv_head >= c->cfg.n_kv_heads)
+    return fail(KVQ_EINVAL, "unit (%d, %d) out of range", seq, kv_head);
+  const int D = c->cfg.head_dim, G = c->cfg.group, bits = c->bits;
+  const int64_t Q = c->quantized[seq], T = c->total[seq], P = Q / G;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::vector<uint8_t> pages((size_t)P * c->geom.page_bytes);
+  kvq_status st = kvq_export_pages(c, seq, kv_head, pages.data(), pages.size(), stream);
+  if (st != KVQ_OK) return st;
+  // ring rows of the window, read whole and reordered on the host
+  const size_t ring_bytes = (size_t)c->rcap * D * c->esize;
+  std::vector<uint8_t> rk(ring_bytes), rv(ring_bytes);
+  const int64_t unit = (int64_t)seq * c->cfg.n_kv_heads + kv_head;
+  cudaError_t e = cudaMemcpyAsync(rk.data(), static_cast<const uint8_t*>(c->ring_k) + unit * ring_bytes, ring_bytes,
+                                  cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(rv.data(), static_cast<const uint8_t*>(c->ring_v) + unit * ring_bytes, ring_bytes,
+                        cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "kvq_export_unit");
+
+  auto sext = [bits](uint32_t v) -> int8_t {
+    return bits == 4 ? (int8_t)(((int)(v & 0xF) ^ 8) - 8) : (int8_t)(v & 0xFF);
+  };
+  for (int64_t pg = 0; pg < P; ++pg) {
+    const uint8_t* page = pages.data() + pg * c->geom.page_bytes;
+    const float* ks = reinterpret_cast<const float*>(page + c->geom.kscale_off);
+    const float* vs = reinterpret_cast<const float*>(page + c->geom.vscale_off);
+    for (int t = 0; t < G; ++t) {
+      const int64_t tok = pg * G + t;
+      for (int ch = 0; ch < D; ++ch) {
+        if (view->k_codes) {
+          const uint32_t byte = bits == 4 ? page[(size_t)t * (D / 2) + ch / 2] : page[(size_t)t * D + ch];
+          view->k_codes[tok * D + ch] = sext(bits == 4 ? (ch & 1 ? byte >> 4 : byte) : byte);
+        }
+        if (view->v_codes) {
+          const uint8_t* vb = page + c->geom.code_bytes;
+          const int st_i = t / 32, o = t % 32, n_st = std::min(32, G - 32 * st_i);
+          const uint8_t* sub = vb + (size_t)st_i * 32 * D * bits / 8;
+          uint32_t code;
+          if (bits == 4) {
+            uint32_t word;
+            memcpy(&word, sub + ((size_t)ch * (n_st / 8) + o / 8) * 4, 4);
+            const int k = o % 8, jn = k / 2 + 4 * (k % 2);
+            code = word >> (4 * jn);
+          } else {
+            code = sub[(size_t)ch * n_st + o];
+          }
+          view->v_codes[tok * D + ch] = sext(code);
+        }
+      }
+      if (view->v_scales) view->v_scales[tok] = vs[t];
+    }
+    if (view->k_scales) memcpy(view->k_scales + pg * D, ks, (size_t)D * sizeof(float));
+  }
+  for (int64_t t = Q; t < T; ++t) {
+    const size_t row = (size_t)(t % c->rcap) * D;
+    for (int ch = 0; ch < D; ++ch) {
+      float kf, vf;
+      if (c->esize == 2) {
+        uint16_t kb, vb;
+        memcpy(&kb, rk.data() + (row + ch) * 2, 2);
+        memcpy(&vb, rv.data() + (row + ch) * 2, 2);
+        const uint32_t k32 = (uint32_t)kb << 16, v32 = (uint32_t)vb << 16;
+        memcpy(&kf, &k32, 4);
+        memcpy(&vf, &v32, 4);
+      } else {
+        memcpy(&kf, rk.data() + (row + ch) * 4, 4);
+        memcpy(&vf, rv.data() + (row + ch) * 4, 4);
+      }
+      if (view->window_k) view->window_k[(t - Q) * D + ch] = kf;
+      if (view->window_v) view->window_v[(t - Q) * D + ch] = vf;
+    }
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_device_status(const kvq_cache* c, int32_t* out_word, void* stream) {
+  if (!c || !out_word) return fail(KVQ_EINVAL, "NULL argument");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t w = 0;
+  cudaError_t e = cudaMemcpyAsync(&w, c->status, sizeof w, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "kvq_device_status");
+  *out_word = w;
+  if (w != 0) return fail(KVQ_EDEVICE, "device status word is 0x%x", (unsigned)w);
+  return KVQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// Internal definitions shared by the host side of libkvq and its kernels:
+// launch parameter blocks, the group-page layout and small device helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// Sequences per kernel launch: their counters travel in the parameter block.
+constexpr int kMaxSeqsPerLaunch = 256;
+// Largest GQA group (query heads per KV head) the kernels handle.
+constexpr int kMaxGqa = 8;
+
+// Device status word codes (kvq_device_status).
+constexpr int32_t kStatusWaitTimeout = 0x101;  // a bounded mbarrier wait gave up
+
+// Counters of one sequence as they stand before a launch.
+struct SeqCounters {
+  int32_t total;      // tokens held
+  int32_t quantized;  // tokens in the quantized prefix (multiple of G)
+};
+
+// Static placement of one sequence's pages (device table written at create).
+struct SeqLayout {
+  int64_t page_base;    // byte offset of (seq, kv head 0, page 0) from the page region
+  int64_t unit_stride;  // bytes between consecutive kv heads of the sequence
+};
+
+// Geometry of a group page (see the layout comment in kvq.h).
+struct PageGeom {
+  int32_t G, D, bits;
+  int64_t code_bytes;   // bytes of one code block (Key or Value): G * D * bits / 8
+  int64_t kscale_off;   // offset of the Key scales
+  int64_t vscale_off;   // offset of the Value scales
+  int64_t page_bytes;
+};
+
+__host__ __device__ inline PageGeom make_geom(int G, int D, int bits) {
+  PageGeom g;
+  g.G = G;
+  g.D = D;
+  g.bits = bits;
+  g.code_bytes = (int64_t)G * D * bits / 8;
+  g.kscale_off = 2 * g.code_bytes;
+  g.vscale_off = g.kscale_off + 4 * (int64_t)D;
+  g.page_bytes = g.vscale_off + 4 * (int64_t)G;
+  return g;
+}
+
+// Number of groups flushed when an append of n tokens meets a window of w
+// tokens (residual window R, group G).
+__host__ __device__ inline int64_t flush_groups(int64_t w, int64_t n, int64_t R, int64_t G) {
+  const int64_t tail = w + n;
+  return tail < R + G ? 0 : (tail - R) / G;
+}
+
+struct AppendParams {
+  int32_t D, Hkv, G, R, Rcap, qmax, bits;
+  float eps;
+  PageGeom geom;
+  uint8_t* pages;              // page region
+  const SeqLayout* layout;     // [batch]
+  void* ring_k;                // [batch][Hkv][Rcap][D] (dtype)
+  void* ring_v;
+  const void* new_k;           // [n_seqs][Hkv][n][D]
+  const void* new_v;
+  int64_t n;                   // new tokens per sequence
+  int32_t seq_begin, n_seqs;
+  int32_t flush_blocks;        // grid.x slots for flush groups (0 if none in this launch)
+  int32_t window_blocks;       // grid.x slots for window writes (0 or 1)
+  SeqCounters old[kMaxSeqsPerLaunch];
+};
+
+struct DecodeParams {
+  int32_t D, Hkv, Hq, g, G, Rcap, bits;
+  float eps;
+  float qk_scale;              // log2(e) / sqrt(D): scores are kept in base 2
+  PageGeom geom;
+  const uint8_t* pages;
+  const SeqLayout* layout;
+  const void* ring_k;
+  const void* ring_v;
+  const void* q;               // [batch][Hq][D]
+  float* partials;             // [batch*Hkv][max_splits][g][D + 2]
+  int32_t max_splits;          // slots per unit; the window uses slot max_splits - 1
+  int32_t chunk_pages;         // pages per quantized split
+  int32_t grid_splits;         // quantized split columns in this launch (window column after)
+  int32_t seq_begin, n_seqs;
+  int32_t* status;
+  SeqCounters ctr[kMaxSeqsPerLaunch];
+};
+
+struct CombineParams {
+  int32_t D, Hkv, Hq, g, G, max_splits, chunk_pages;
+  const float* partials;
+  float* out;                  // [batch][Hq][D]
+  int32_t seq_begin, n_seqs;
+  SeqCounters ctr[kMaxSeqsPerLaunch];
+};
+
+// Launchers (defined in the kernel translation units). Return cudaGetLastError().
+cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s);
+cudaError_t configure_append(int dtype, int bits, size_t smem_bytes);
+cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported);
+size_t decode_mma_smem_bytes(const DecodeParams& p);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+
+}  // namespace kvq

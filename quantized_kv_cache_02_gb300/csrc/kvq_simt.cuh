@@ -1,0 +1,214 @@
+// CUDA-core decode attention over one split item (a run of quantized group
+// pages, or the residual window) of one (sequence, KV head) unit, for all g
+// query heads that read that KV head ("KV Cache 与自回归视频生成" section 04,
+// attn_step: head h reads KV head h / g).  Each warp keeps an online-softmax
+// state (running max m, sum l, unnormalised o) per head over its tokens; the
+// CTA merges its warps and writes one partial (o[D], m, l) per head, which the
+// combine kernel merges across splits (section 05, FlashDecoding).
+// Dequantization follows the page's restore: x = code / scale (fp32 division).
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kSimtThreads = 128;
+constexpr int kSimtWarps = kSimtThreads / 32;
+
+__device__ __forceinline__ float ld_f32(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_f32(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
+
+// Signed code of channel c of token tl (group-local) of a page.
+template <int BITS>
+__device__ __forceinline__ int key_code(const uint8_t* page, int tl, int c, int D) {
+  if (BITS == 4) {
+    const uint8_t byte = page[(int64_t)tl * (D / 2) + (c >> 1)];
+    const int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
+    return (nib ^ 8) - 8;
+  } else {
+    return (int)(int8_t)page[(int64_t)tl * D + c];
+  }
+}
+
+template <int BITS>
+__device__ __forceinline__ int value_code(const uint8_t* vbase, int G, int tl, int c, int D) {
+  const int st = tl >> 5, o = tl & 31;
+  const int n_st = min(32, G - 32 * st);
+  const uint8_t* sub = vbase + (int64_t)st * 32 * D * BITS / 8;
+  if (BITS == 4) {
+    const int w = o >> 3, k = o & 7;
+    const int jn = (k >> 1) + 4 * (k & 1);  // nibble that holds token offset k
+    const uint32_t word = reinterpret_cast<const uint32_t*>(sub)[c * (n_st / 8) + w];
+    const int nib = (word >> (4 * jn)) & 0xF;
+    return (nib ^ 8) - 8;
+  } else {
+    return (int)(int8_t)sub[c * n_st + o];
+  }
+}
+
+template <int CPL>
+struct SimtState {
+  float m[kMaxGqa], l[kMaxGqa], o[kMaxGqa][CPL];
+};
+
+template <int CPL>
+__device__ __forceinline__ void simt_token(SimtState<CPL>& s, const float (&qv)[kMaxGqa][CPL],
+                                           const float (&kv)[CPL], const float (&vv)[CPL], int g) {
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+    if (j >= g) break;
+    float part = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) part = fmaf(qv[j][k], kv[k], part);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
+    const float m_new = fmaxf(s.m[j], part);
+    const float corr = exp2f(s.m[j] - m_new);
+    const float pw = exp2f(part - m_new);
+    s.l[j] = fmaf(s.l[j], corr, pw);
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) s.o[j][k] = fmaf(s.o[j][k], corr, pw * vv[k]);
+    s.m[j] = m_new;
+  }
+}
+
+// Shared scratch of simt_item in floats (q, per-warp m and l, per-warp o).
+template <int CPL>
+__host__ __device__ constexpr int simt_scratch_floats() {
+  return kMaxGqa * CPL * 32 + 2 * kSimtWarps * kMaxGqa + kSimtWarps * kMaxGqa * CPL * 32;
+}
+
+// Whole split item on CUDA cores; writes the partial of slot ``slot``.
+// ``win`` selects the residual window (tokens [Q, T) from the ring) instead of
+// pages [pg0, pg1) of the quantized prefix.
+
+template <typename T, int BITS, int CPL>
+__device__ void simt_item(const DecodeParams& p, int i, int h, bool win, int pg0, int pg1, int slot,
+                          float* scratch) {
+  float (*qs)[CPL * 32] = reinterpret_cast<float (*)[CPL * 32]>(scratch);
+  float (*wm)[kMaxGqa] = reinterpret_cast<float (*)[kMaxGqa]>(scratch + kMaxGqa * CPL * 32);
+  float (*wl)[kMaxGqa] = wm + kSimtWarps;
+  float (*wo)[kMaxGqa][CPL * 32] =
+      reinterpret_cast<float (*)[kMaxGqa][CPL * 32]>(scratch + kMaxGqa * CPL * 32 + 2 * kSimtWarps * kMaxGqa);
+  const int D = p.D, g = p.g, G = p.G;
+  const int b = p.seq_begin + i;
+  const int64_t unit = (int64_t)b * p.Hkv + h;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const T* q = reinterpret_cast<const T*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g) * D;
+  for (int idx = threadIdx.x; idx < kMaxGqa * CPL * 32; idx += blockDim.x) {
+    const int j = idx / (CPL * 32), c = idx - j * (CPL * 32);
+    qs[j][c] = (j < g && c < D) ? ld_f32(q, (int64_t)j * D + c) * p.qk_scale : 0.f;
+  }
+  __syncthreads();
+  float qv[kMaxGqa][CPL];
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j)
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) qv[j][k] = qs[j][lane + 32 * k];
+
+  SimtState<CPL> s;
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j) {
+    s.m[j] = -INFINITY;
+    s.l[j] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) s.o[j][k] = 0.f;
+  }
+
+  float kv[CPL], vv[CPL];
+  if (win) {
+    const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+    const T* rk = reinterpret_cast<const T*>(p.ring_k) + unit * p.Rcap * D;
+    const T* rv = reinterpret_cast<const T*>(p.ring_v) + unit * p.Rcap * D;
+    for (int64_t t = Q0 + warp; t < T0; t += kSimtWarps) {
+      const int64_t row = (t % p.Rcap) * D;
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int c = lane + 32 * k;
+        kv[k] = c < D ? ld_f32(rk, row + c) : 0.f;
+        vv[k] = c < D ? ld_f32(rv, row + c) : 0.f;
+      }
+      simt_token<CPL>(s, qv, kv, vv, g);
+    }
+  } else {
+    const uint8_t* unit_pages = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride;
+    const int64_t ntok = (int64_t)(pg1 - pg0) * G;
+    for (int64_t tt = warp; tt < ntok; tt += kSimtWarps) {
+      const int pg = pg0 + (int)(tt / G), tl = (int)(tt % G);
+      const uint8_t* page = unit_pages + (int64_t)pg * p.geom.page_bytes;
+      const float* ks = reinterpret_cast<const float*>(page + p.geom.kscale_off);
+      const float vs = reinterpret_cast<const float*>(page + p.geom.vscale_off)[tl];
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int c = lane + 32 * k;
+        if (c < D) {
+          kv[k] = __fdiv_rn((float)key_code<BITS>(page, tl, c, D), fmaxf(ks[c], p.eps));
+          vv[k] = __fdiv_rn((float)value_code<BITS>(page + p.geom.code_bytes, G, tl, c, D), fmaxf(vs, p.eps));
+        } else {
+          kv[k] = 0.f;
+          vv[k] = 0.f;
+        }
+      }
+      simt_token<CPL>(s, qv, kv, vv, g);
+    }
+  }
+
+  // merge the warps of this CTA
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < kMaxGqa; ++j) {
+      wm[warp][j] = s.m[j];
+      wl[warp][j] = s.l[j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxGqa; ++j)
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) wo[warp][j][lane + 32 * k] = s.o[j][k];
+  __syncthreads();
+  float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * (D + 2);
+  for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
+    const int j = idx / D, c = idx - j * D;
+    float M = -INFINITY;
+    for (int w = 0; w < kSimtWarps; ++w) M = fmaxf(M, wm[w][j]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kSimtWarps; ++w) {
+        if (wm[w][j] == -INFINITY) continue;
+        const float f = exp2f(wm[w][j] - M);
+        L = fmaf(wl[w][j], f, L);
+        O = fmaf(wo[w][j][c], f, O);
+      }
+    }
+    part[(int64_t)j * (D + 2) + c] = O;
+    if (c == 0) {
+      part[(int64_t)j * (D + 2) + D] = M;
+      part[(int64_t)j * (D + 2) + D + 1] = L;
+    }
+  }
+}
+
+// Which split item CTA (x, unit) of a decode launch handles.  Returns false if
+// the CTA has nothing to do.
+__device__ __forceinline__ bool split_item(const DecodeParams& p, int x, int i, bool* win, int* pg0,
+                                           int* pg1, int* slot) {
+  const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+  const int P = Q0 / p.G;
+  const int nsplit = (P + p.chunk_pages - 1) / p.chunk_pages;
+  if (x == p.grid_splits) {
+    *win = true;
+    *slot = p.max_splits - 1;
+    *pg0 = *pg1 = 0;
+    return T0 > Q0;
+  }
+  if (x >= nsplit) return false;
+  *win = false;
+  *slot = x;
+  *pg0 = x * p.chunk_pages;
+  *pg1 = min(P, *pg0 + p.chunk_pages);
+  return true;
+}
+
+}  // namespace kvq
