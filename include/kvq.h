@@ -200,7 +200,8 @@ kvq_status kvq_export_unit(const kvq_cache* cache, int32_t seq, int32_t kv_head,
 
 /* Copy the raw bytes of one unit's group pages (n_groups * page size bytes,
  * token order) to the host buffer ``host_dst`` of ``dst_bytes`` bytes
- * (synchronizes ``stream``). */
+ * (synchronizes ``stream``).  With no flushed group it copies nothing and
+ * ``host_dst`` may be NULL. */
 kvq_status kvq_export_pages(const kvq_cache* cache, int32_t seq, int32_t kv_head, void* host_dst,
                             size_t dst_bytes, void* stream);
 

@@ -14,9 +14,10 @@
 // which is q.k/sqrt(d) and p.v over restored values k = code/sK, v = code/sV
 // ("KV Cache Quantization Strategies", restore; "KV Cache 与自回归视频生成"
 // 3.1 and attn_step) with both scales folded into the f16 MMA operand that
-// is not the code.  Codes are exact small integers in f16; the nibble to f16
-// conversion writes the biased nibble into the mantissa of 1024.0 and
-// subtracts 1032.0 (IEEE binary16: 0x6400 | u == 1024 + u for u < 1024).
+// is not the code (q/sK as an f16 hi + lo pair, p/sV as one f16).  Codes are
+// exact small integers in f16; the nibble to f16 conversion writes the biased
+// nibble into the mantissa of 1024.0 and subtracts 1032.0 (IEEE binary16:
+// 0x6400 | u == 1024 + u for u < 1024).
 // Matrix shapes: S = A(K codes: 16 tokens x 16 channels) * B(q: 16 x 8 heads),
 // O^T = A(V codes^T: 16 channels x 16 tokens) * B(P^T: 16 tokens x 8 heads);
 // P goes from the S accumulator layout to the B layout with movmatrix.trans.
@@ -190,8 +191,11 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
                                          const float (&qreg)[Shape<D, BITS>::kChan], int gid, int tig,
                                          WarpState<D, BITS>& st) {
   using S = Shape<D, BITS>;
-  // ---- B operand of S: q / sK per channel, f16 --------------------------
-  uint32_t bq[S::kSteps][2];
+  // ---- B operand of S: q / sK per channel as an f16 pair hi + lo ---------
+  // (hi = f16(x), lo = f16(x - hi)): two MMAs against the same code operand
+  // give the scores to ~2^-22 relative instead of f16's 2^-12, which matters
+  // because outlier channels make the softmax very peaked.
+  uint32_t bq[S::kSteps][2], bl[S::kSteps][2];
   {
     const float* ks = reinterpret_cast<const float*>(pg + geom.kscale_off) + tig * S::kChan;
     float qk[S::kChan];
@@ -205,8 +209,15 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
     }
 #pragma unroll
     for (int kk = 0; kk < S::kSteps; ++kk) {
-      bq[kk][0] = qlive ? pack_f16x2(qk[kslot_channel<BITS>(kk, 0)], qk[kslot_channel<BITS>(kk, 1)]) : 0u;
-      bq[kk][1] = qlive ? pack_f16x2(qk[kslot_channel<BITS>(kk, 2)], qk[kslot_channel<BITS>(kk, 3)]) : 0u;
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)], x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)];
+        const __half2 hi = __floats2half2_rn(x0, x1);
+        const float2 back = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
+        bq[kk][r] = qlive ? *reinterpret_cast<const uint32_t*>(&hi) : 0u;
+        bl[kk][r] = qlive ? *reinterpret_cast<const uint32_t*>(&lo) : 0u;
+      }
     }
   }
   const float* vscale = reinterpret_cast<const float*>(pg + geom.vscale_off);
@@ -235,7 +246,9 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
             nibbles_to_f16(wa[mb][i], ra);
             nibbles_to_f16(wb[mb][i], rb);
             mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bq[2 * i][0], bq[2 * i][1]);
+            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bl[2 * i][0], bl[2 * i][1]);
             mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bq[2 * i + 1][0], bq[2 * i + 1][1]);
+            mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bl[2 * i + 1][0], bl[2 * i + 1][1]);
           }
         }
       } else {
@@ -247,6 +260,7 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
             bytes_to_f16(wa[mb][kk], ra);
             bytes_to_f16(wb[mb][kk], rb);
             mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bq[kk][0], bq[kk][1]);
+            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bl[kk][0], bl[kk][1]);
           }
         }
       }

@@ -493,12 +493,13 @@ kvq_status kvq_seq_state(const kvq_cache* c, int32_t seq, kvq_seq_info* out) {
 
 kvq_status kvq_export_pages(const kvq_cache* c, int32_t seq, int32_t kv_head, void* host_dst, size_t dst_bytes,
                             void* stream) {
-  if (!c || !host_dst) return fail(KVQ_EINVAL, "NULL argument");
+  if (!c) return fail(KVQ_EINVAL, "NULL argument");
   if (seq < 0 || seq >= c->cfg.batch || kv_head < 0 || kv_head >= c->cfg.n_kv_heads)
     return fail(KVQ_EINVAL, "unit (%d, %d) out of range", seq, kv_head);
   const size_t bytes = (size_t)(c->quantized[seq] / c->cfg.group) * c->geom.page_bytes;
-  if (dst_bytes < bytes) return fail(KVQ_EINVAL, "host buffer of %zu bytes < %zu", dst_bytes, bytes);
   if (bytes == 0) return KVQ_OK;
+  if (!host_dst) return fail(KVQ_EINVAL, "host_dst is NULL");
+  if (dst_bytes < bytes) return fail(KVQ_EINVAL, "host buffer of %zu bytes < %zu", dst_bytes, bytes);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint8_t* src = c->pages + c->page_base[seq] + (int64_t)kv_head * c->pages_cap[seq] * c->geom.page_bytes;
   cudaError_t e = cudaMemcpyAsync(host_dst, src, bytes, cudaMemcpyDeviceToHost, s);
