@@ -183,6 +183,28 @@ kvq_status kvq_decode_attention(kvq_cache* cache, const void* q, float* out, voi
 kvq_status kvq_decode_attention_ex(kvq_cache* cache, const void* q, float* out, void* stream,
                                    const kvq_decode_opts* opts);
 
+/* No counterpart in the source pages: an addition for callers that cannot
+ * allocate device memory when they decode (a plugin whose host framework owns
+ * every device allocation, a deployment that reserves all memory once at
+ * start-up).  Computes exactly what kvq_decode_attention computes, but keeps the
+ * split partials -- the decode's only scratch -- in a fixed array inside the
+ * library instead of the arena's scratch region, and allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library call.
+ *  - The array holds 2^21 floats (8 MiB); every GPU that loads the library
+ *    holds it until the process exits.  A cache whose batch * n_kv_heads *
+ *    (n_q_heads / n_kv_heads) * (head_dim + 2) floats times 2 split columns
+ *    (1 without any flushed group) exceed it is rejected with KVQ_ECAPACITY
+ *    before any launch; otherwise the split count is lowered to fit.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's
+ *    contents; nothing in it needs to start at zero, since every partial a
+ *    call reads is written earlier in the same call.  Calls that overlap on the
+ *    GPU (other streams, other caches) race on it: serialize them.
+ * Arguments, layout, ownership and errors are those of kvq_decode_attention. */
+kvq_status kvq_decode_attention_noalloc(kvq_cache* cache, const void* q, float* out, void* stream);
+
 /* Held-bytes ledger of a live cache (host counters, no device access). */
 kvq_status kvq_bytes(const kvq_cache* cache, kvq_bytes_t* out);
 

@@ -22,7 +22,7 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ECAPACITY", 3: "KVQ_ENOMEM
 EXPORTED = ("kvq_required_bytes", "kvq_create", "kvq_append", "kvq_decode_attention",
             "kvq_decode_attention_ex", "kvq_bytes", "kvq_ledger", "kvq_seq_state", "kvq_export_unit",
             "kvq_export_pages", "kvq_device_status", "kvq_page_bytes", "kvq_kernel_launches", "kvq_destroy",
-            "kvq_last_error")
+            "kvq_last_error", "kvq_decode_attention_noalloc")
 
 
 class kvq_config(ctypes.Structure):
@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_device_status": ([V, P(I32), V], ctypes.c_int),
         "kvq_page_bytes": ([P(kvq_config)], SZ),
         "kvq_kernel_launches": ([], ctypes.c_uint64),
+        "kvq_decode_attention_noalloc": ([V, V, V, V], ctypes.c_int),
         "kvq_destroy": ([V], None),
         "kvq_last_error": ([], ctypes.c_char_p),
     }
@@ -145,6 +146,12 @@ def kvq_decode_attention_ex(handle, q_ptr, out_ptr, stream, kernel=0, chunk_page
                             split_stop=None) -> None:
     opts = kvq_decode_opts(kernel, chunk_pages, split_start, split_stop)
     _check(load_library().kvq_decode_attention_ex(handle, q_ptr, out_ptr, stream, ctypes.byref(opts)))
+
+
+def kvq_decode_attention_noalloc(handle, q_ptr, out_ptr, stream) -> None:
+    """Decode attention with the split scratch in the library's fixed device
+    array (for callers that cannot allocate device memory at call time)."""
+    _check(load_library().kvq_decode_attention_noalloc(handle, q_ptr, out_ptr, stream))
 
 
 def kvq_bytes(handle) -> dict:

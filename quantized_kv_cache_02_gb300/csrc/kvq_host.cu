@@ -10,6 +10,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -446,6 +447,123 @@ kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void
 
 kvq_status kvq_decode_attention(kvq_cache* c, const void* q, float* out, void* stream) {
   return kvq_decode_attention_ex(c, q, out, stream, nullptr);
+}
+
+}  // extern "C"
+
+// ---- decode attention with library-owned scratch -------------------------------
+//
+// Some callers cannot allocate device memory when they run the decode: a plugin
+// inside a host framework that owns every device allocation, or a deployment
+// that reserves all its memory once at start-up, has no cudaMalloc to call and
+// no spare buffer to hand over.  kvq_decode_attention_noalloc serves them: the
+// split partials, the only scratch the decode needs, go to the fixed array
+// below instead of the arena's scratch region.  The array is 8 MiB of device
+// memory that every GPU which loads this library holds until the process exits.
+
+constexpr size_t kNoAllocScratchFloats = size_t(2) << 20;  // 8 MiB of float
+static __device__ __align__(256) float kvq_noalloc_scratch[kNoAllocScratchFloats];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+float* g_noalloc_ptr[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of kvq_noalloc_scratch on ``device``, looked up once per
+// device with that device current (host code only sees a stand-in symbol).
+kvq_status noalloc_scratch(int device, float** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (device < 0 || device >= kNoAllocMaxDevices)
+    return fail(KVQ_EUNSUPPORTED, "device %d is beyond the %d devices the scratch table covers", device,
+                kNoAllocMaxDevices);
+  if (!g_noalloc_ptr[device]) {
+    int cur = 0;
+    cudaError_t e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != device && (e = cudaSetDevice(device)) != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, kvq_noalloc_scratch);
+    if (cur != device) cudaSetDevice(cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(kvq_noalloc_scratch)");
+    g_noalloc_ptr[device] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[device];
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attention_noalloc(kvq_cache* c, const void* q, float* out, void* stream) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
+  const int B = c->cfg.batch, H = c->cfg.n_kv_heads, D = c->cfg.head_dim;
+  // one split plan for every sequence, then as many split slots as the array holds
+  int64_t pmax = 0;
+  for (int b = 0; b < B; ++b) pmax = std::max<int64_t>(pmax, c->quantized[b] / c->cfg.group);
+  const size_t per_slot = (size_t)B * H * c->g * (D + 2);  // floats of one split column
+  const size_t min_slots = pmax > 0 ? 2 : 1;              // one quantized split plus the window
+  if (per_slot * min_slots > kNoAllocScratchFloats)
+    return fail(KVQ_ECAPACITY,
+                "decode needs %zu floats of split scratch, more than the %zu floats (8 MiB) the library reserves",
+                per_slot * min_slots, kNoAllocScratchFloats);
+  int chunk = 1, grid = 0;
+  plan_splits(c, 0, B, 0, &chunk, &grid);
+  const int64_t fit = (int64_t)(kNoAllocScratchFloats / per_slot);  // >= min_slots
+  if (grid + 1 > fit) {
+    chunk = (int)((pmax + (fit - 1) - 1) / (fit - 1));
+    grid = (int)((pmax + chunk - 1) / chunk);
+  }
+  const int slots = grid + 1;
+  float* scratch = nullptr;
+  kvq_status st = noalloc_scratch(c->device, &scratch);
+  if (st != KVQ_OK) return st;
+  const bool use_mma = c->cfg.dtype == KVQ_BF16 && (D == 64 || D == 128) && c->cfg.group % 32 == 0;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int s0 = 0; s0 < B; s0 += kvq::kMaxSeqsPerLaunch) {
+    const int n = std::min(kvq::kMaxSeqsPerLaunch, B - s0);
+    kvq::DecodeParams p;
+    base_decode_params(c, &p);
+    p.q = q;
+    p.partials = scratch;
+    p.max_splits = slots;
+    p.chunk_pages = chunk;
+    p.grid_splits = grid;
+    p.seq_begin = s0;
+    p.n_seqs = n;
+    fill_counters(c, s0, n, p.ctr);
+    cudaError_t e;
+    if (use_mma) {
+      int supported = 0;
+      e = kvq::launch_decode_mma(p, s, &supported);
+    } else {
+      e = kvq::launch_decode_simt(p, c->cfg.dtype, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
+    g_launches += 1;
+  }
+  for (int s0 = 0; s0 < B; s0 += kvq::kMaxSeqsPerLaunch) {
+    kvq::CombineParams cp;
+    memset(&cp, 0, sizeof cp);
+    cp.D = D;
+    cp.Hkv = H;
+    cp.Hq = c->cfg.n_q_heads;
+    cp.g = c->g;
+    cp.G = c->cfg.group;
+    cp.max_splits = slots;
+    cp.chunk_pages = chunk;
+    cp.partials = scratch;
+    cp.out = out;
+    cp.seq_begin = s0;
+    cp.n_seqs = std::min(kvq::kMaxSeqsPerLaunch, B - s0);
+    fill_counters(c, s0, cp.n_seqs, cp.ctr);
+    const cudaError_t e = kvq::launch_combine(cp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    g_launches += 1;
+  }
+  return KVQ_OK;
 }
 
 kvq_status kvq_ledger(const kvq_config* cfg, const int64_t* tokens_per_seq, kvq_bytes_t* out) {
