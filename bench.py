@@ -226,6 +226,9 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     dev_index = torch.cuda.current_device()
     w = dict(WORKLOAD)
+    if args.layers:
+        w["layers"] = args.layers
+        w["name"] = f"{w['name']}_layers{args.layers}"
     L, B, H, Hq, D = w["layers"], w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"]
     K, W = args.steps, args.warmup
     # each rank runs its own batch of sequences (weak scaling): seeds differ by rank
@@ -315,7 +318,7 @@ def run_ours(args):
     assert Qsim == counters()[0], "host byte model out of step with the cache counters"
 
     # ---- end to end through the C ABI with host buffers ----------------------
-    n_ring = 8
+    n_ring = min(8, steps_total)
     pin_k = [torch.empty(B, H, 1, D, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring * L)]
     pin_v = [torch.empty(B, H, 1, D, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring * L)]
     pin_q = [torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring * L)]
@@ -464,6 +467,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; 0 = all 32)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")

@@ -104,35 +104,70 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-__device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
+// ---- codes as f16 subnormals --------------------------------------------
+// A stored code is two's complement; adding the bias (8 for 4-bit, 128 for
+// 8-bit) makes it an unsigned u in [1, 2*bias).  A 16-bit half whose bits are
+// just u (exponent 0) is the binary16 subnormal u * 2^-24, exactly; u << 4 is
+// 16 * u * 2^-24.  So masking the biased word yields MMA operands without any
+// floating-point conversion; the 2^-24, the x16 of the second nibble position
+// (cancelled by a 1/16 on the matching B rows) and the bias are undone after
+// the MMA: S = 2^24 * S' - bias * sum(B),  O = 2^24 * O' - bias * sum(p').
+
+// 4-bit: word of eight nibbles -> r[j] = (nibble j, nibble j + 4) as f16x2;
+// r[1] and r[3] carry an extra factor 16.
+__device__ __forceinline__ void nibble_regs(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t t = w ^ 0x88888888u;
+  const uint32_t t2 = t >> 8;
+  r[0] = t & 0x000F000Fu;
+  r[1] = t & 0x00F000F0u;
+  r[2] = t2 & 0x000F000Fu;
+  r[3] = t2 & 0x00F000F0u;
 }
 
-// Eight signed nibbles of ``w`` -> four f16x2 registers; register j holds
-// nibble j (low half) and nibble j + 4 (high half).  The lop3 builds
-// 0x6400 | (nibble ^ 8) in each half: truth table 0x6A over
-// (a = shifted word, b = 0x000F000F, c = 0x64086408) keeps a where b & ~c,
-// inverts it where b & c (the nibble's top bit) and sets the bits of c
-// outside b.  Subtracting 1032.0 leaves the signed value exactly.
-__device__ __forceinline__ void nibbles_to_f16(uint32_t w, uint32_t (&r)[4]) {
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    uint32_t t;
-    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(t) : "r"(w >> (4 * j)), "r"(0x000F000Fu), "r"(0x64086408u));
-    r[j] = f16x2_sub(t, 0x64086408u);
-  }
-}
-
-// Four signed bytes of ``w`` -> two f16x2 registers: (byte0, byte1), (byte2, byte3).
-__device__ __forceinline__ void bytes_to_f16(uint32_t w, uint32_t (&r)[2]) {
+// 8-bit: word of four bytes -> r[0] = (byte 0, byte 2), r[1] = (byte 1, byte 3).
+__device__ __forceinline__ void byte_regs(uint32_t w, uint32_t (&r)[2]) {
   const uint32_t t = w ^ 0x80808080u;
-  uint32_t x0, x1;
-  asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(x0) : "r"(t), "r"(0x64646464u));
-  asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(x1) : "r"(t), "r"(0x64646464u));
-  r[0] = f16x2_sub(x0, 0x64806480u);
-  r[1] = f16x2_sub(x1, 0x64806480u);
+  r[0] = t & 0x00FF00FFu;
+  r[1] = (t >> 8) & 0x00FF00FFu;
+}
+
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+// 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 template <int N>
@@ -157,84 +192,127 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[N]) {
   }
 }
 
-template <int D, int BITS>
+// GP = query heads per KV head rounded up to 2, 4 or 8.  The MMA's 8 columns
+// hold GP heads of each of PB = 8 / GP pages, so one B operand (q / sK) and one
+// softmax update serve PB pages ("streams"); column n belongs to stream n / GP.
+template <int D, int BITS, int GP>
 struct Shape {
-  static constexpr int kSteps = D / 16;        // k-steps of the S MMA, m-tiles of the O MMA
+  static constexpr int PB = 8 / GP;
+  static constexpr int kSteps = D / 16;          // k-steps of the S MMA, m-tiles of the O MMA
   static constexpr int kRowBytes = D * BITS / 8;
   static constexpr int kWords = kRowBytes / 16;  // 32-bit words of a K row per thread
-  static constexpr int kChan = D / 4;          // channels of a K row per thread
+  static constexpr int kChan = D / 4;            // channels of a K row per thread
   static constexpr int kSubBytes = 32 * D * BITS / 8;
+  static constexpr int kChunks = D / 4;          // float4 chunks of a page's Key scales
+  static constexpr float kBias = BITS == 4 ? 8.f : 128.f;
 };
 
-// Channel (relative to the thread's slice) of element e (0..3) of k-step kk:
-// e = 0, 1 -> B register 0 (k-slots 2tig, 2tig+1); e = 2, 3 -> register 1.
+// Channel (in the thread's slice) of element e of k-step kk's B operand:
+// e = 0, 1 -> register 0 (k-slots 2tig, 2tig+1); e = 2, 3 -> register 1.
 template <int BITS>
-__device__ __forceinline__ int kslot_channel(int kk, int e) {
-  if (BITS == 4) {
-    const int base = 8 * (kk >> 1) + 2 * (kk & 1);
-    const int off[4] = {0, 4, 1, 5};
-    return base + off[e];
-  } else {
-    return 4 * kk + e;
-  }
+__device__ __forceinline__ constexpr int kslot_channel(int kk, int e) {
+  return BITS == 4 ? 8 * (kk >> 1) + 2 * (kk & 1) + (e == 0 ? 0 : e == 1 ? 4 : e == 2 ? 1 : 5)
+                   : 4 * kk + (e == 0 ? 0 : e == 1 ? 2 : e == 2 ? 1 : 3);
 }
 
-template <int D, int BITS>
+// Token row (inside a 32-token sub-tile) of S rows gid (r0) and gid + 8 (r1)
+// of m-block mb; these orders match how the conversions pair tokens.
+template <int BITS>
+__device__ __forceinline__ int token_row0(int gid, int mb) {
+  return BITS == 4 ? 8 * (gid >> 1) + 4 * mb + (gid & 1) : 8 * (gid >> 1) + 4 * mb + 2 * (gid & 1);
+}
+template <int BITS>
+__device__ __forceinline__ constexpr int token_row_gap() {
+  return BITS == 4 ? 2 : 1;
+}
+
+template <int D>
 struct WarpState {
-  float O[D / 16][4];
-  float m0, m1, l0, l1;
+  float O[D / 16][4];  // O'^T accumulators (biased codes, scaled by 2^-24)
+  float m0, m1;        // running max of the thread's two columns (base 2)
+  float l0, l1;        // running sum of p (partial over this thread's rows)
+  float q0, q1;        // running sum of p / sV (partial), for the bias
 };
 
-// One group page (G tokens) in shared memory.
-template <int D, int BITS>
-__device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom, int G, bool qlive,
-                                         const float (&qreg)[Shape<D, BITS>::kChan], int gid, int tig,
-                                         WarpState<D, BITS>& st) {
-  using S = Shape<D, BITS>;
-  // ---- B operand of S: q / sK per channel as an f16 pair hi + lo ---------
-  // (hi = f16(x), lo = f16(x - hi)): two MMAs against the same code operand
-  // give the scores to ~2^-22 relative instead of f16's 2^-12, which matters
-  // because outlier channels make the softmax very peaked.
-  uint32_t bq[S::kSteps][2], bl[S::kSteps][2];
+// A group of up to PB pages (already in shared memory) of one warp.
+template <int D, int BITS, int GP>
+__device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BITS, GP>::PB], int npages,
+                                          const PageGeom& geom, int G, const float (&qreg)[D / 4],
+                                          float* rsc, int lane, int gid, int tig, WarpState<D>& st) {
+  using S = Shape<D, BITS, GP>;
+  constexpr float kTwo24 = 16777216.f;
+  // ---- reciprocal Key scales, cooperatively, in a bank-friendly order -------
+  // chunk i (channels tig*kChan + 4i .. +3) of slice tig goes to float4 slot i*4 + tig
+#pragma unroll
+  for (int q = lane; q < S::PB * S::kChunks; q += 32) {
+    const int j = q / S::kChunks, cc = q - j * S::kChunks;
+    if (j < npages) {
+      const float4 s4 = reinterpret_cast<const float4*>(pg[j] + geom.kscale_off)[cc];
+      const float4 r4 = make_float4(fast_rcp(s4.x), fast_rcp(s4.y), fast_rcp(s4.z), fast_rcp(s4.w));
+      const int tg = cc / (S::kChan / 4), i = cc - tg * (S::kChan / 4);
+      reinterpret_cast<float4*>(rsc + j * D)[i * 4 + tg] = r4;
+    }
+  }
+  __syncwarp();
+  // ---- B operand of S: q / sK for (head gid % GP, page gid / GP), hi + lo ---
+  uint32_t bh[S::kSteps][2], bl[S::kSteps][2];
+  float beta0, beta1;
   {
-    const float* ks = reinterpret_cast<const float*>(pg + geom.kscale_off) + tig * S::kChan;
+    const int jb = min(gid / GP, npages - 1);
+    const float4* rj = reinterpret_cast<const float4*>(rsc + jb * D);
     float qk[S::kChan];
+    float beta = 0.f;
 #pragma unroll
     for (int i = 0; i < S::kChan / 4; ++i) {
-      const float4 s4 = reinterpret_cast<const float4*>(ks)[i];
-      qk[4 * i + 0] = __fdividef(qreg[4 * i + 0], s4.x);
-      qk[4 * i + 1] = __fdividef(qreg[4 * i + 1], s4.y);
-      qk[4 * i + 2] = __fdividef(qreg[4 * i + 2], s4.z);
-      qk[4 * i + 3] = __fdividef(qreg[4 * i + 3], s4.w);
+      const float4 r = rj[i * 4 + tig];
+      qk[4 * i + 0] = qreg[4 * i + 0] * r.x;
+      qk[4 * i + 1] = qreg[4 * i + 1] * r.y;
+      qk[4 * i + 2] = qreg[4 * i + 2] * r.z;
+      qk[4 * i + 3] = qreg[4 * i + 3] * r.w;
+      beta += (qk[4 * i + 0] + qk[4 * i + 1]) + (qk[4 * i + 2] + qk[4 * i + 3]);
     }
+    beta += __shfl_xor_sync(0xffffffffu, beta, 1);
+    beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+    beta0 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig));
+    beta1 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig + 1));
 #pragma unroll
     for (int kk = 0; kk < S::kSteps; ++kk) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)], x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)];
+        const float f = (BITS == 4 && r == 1) ? 0.0625f : 1.f;
+        const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)] * f, x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)] * f;
         const __half2 hi = __floats2half2_rn(x0, x1);
         const float2 back = __half22float2(hi);
         const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
-        bq[kk][r] = qlive ? *reinterpret_cast<const uint32_t*>(&hi) : 0u;
-        bl[kk][r] = qlive ? *reinterpret_cast<const uint32_t*>(&lo) : 0u;
+        bh[kk][r] = *reinterpret_cast<const uint32_t*>(&hi);
+        bl[kk][r] = *reinterpret_cast<const uint32_t*>(&lo);
       }
     }
   }
-  const float* vscale = reinterpret_cast<const float*>(pg + geom.vscale_off);
-  const int r_base = 8 * (gid >> 1) + (gid & 1);  // token row of m-block 0 inside a sub-tile
+  const int sj = (2 * tig) / GP;                  // this thread's stream (both columns)
+  const int vpage = min(sj, npages - 1);          // a valid page for its Value scales
+  const uint8_t* vpg = pg[0];
+#pragma unroll
+  for (int j = 1; j < S::PB; ++j)
+    if (j == vpage) vpg = pg[j];
+  constexpr int kGap = token_row_gap<BITS>();
 
   for (int sub = 0; sub < G / 32; ++sub) {
-    const uint8_t* kc = pg + sub * 32 * S::kRowBytes;
-    const uint8_t* vc = pg + geom.code_bytes + sub * S::kSubBytes;
-    // ---- S = K q for the two 16-token m-blocks --------------------------
-    float s[2][4];
-    {
+    // ---- scores of every page; keep each column's own page ------------------
+    float ss[2][4];
+#pragma unroll
+    for (int mb = 0; mb < 2; ++mb) ss[mb][0] = ss[mb][1] = ss[mb][2] = ss[mb][3] = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < S::PB; ++j) {
+      if (j >= npages) break;
+      const uint8_t* kc = pg[j] + sub * 32 * S::kRowBytes;
       uint32_t wa[2][S::kWords], wb[2][S::kWords];
+      float s[2][4];
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
-        const int r0 = r_base + 4 * mb;
+        const int r0 = token_row0<BITS>(gid, mb);
         lds_words<S::kWords>(kc + r0 * S::kRowBytes + tig * (S::kRowBytes / 4), wa[mb]);
-        lds_words<S::kWords>(kc + (r0 + 2) * S::kRowBytes + tig * (S::kRowBytes / 4), wb[mb]);
+        lds_words<S::kWords>(kc + (r0 + kGap) * S::kRowBytes + tig * (S::kRowBytes / 4), wb[mb]);
         s[mb][0] = s[mb][1] = s[mb][2] = s[mb][3] = 0.f;
       }
       if (BITS == 4) {
@@ -243,11 +321,11 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
 #pragma unroll
           for (int mb = 0; mb < 2; ++mb) {
             uint32_t ra[4], rb[4];
-            nibbles_to_f16(wa[mb][i], ra);
-            nibbles_to_f16(wb[mb][i], rb);
-            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bq[2 * i][0], bq[2 * i][1]);
+            nibble_regs(wa[mb][i], ra);
+            nibble_regs(wb[mb][i], rb);
+            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bh[2 * i][0], bh[2 * i][1]);
             mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bl[2 * i][0], bl[2 * i][1]);
-            mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bq[2 * i + 1][0], bq[2 * i + 1][1]);
+            mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bh[2 * i + 1][0], bh[2 * i + 1][1]);
             mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bl[2 * i + 1][0], bl[2 * i + 1][1]);
           }
         }
@@ -257,33 +335,43 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
 #pragma unroll
           for (int mb = 0; mb < 2; ++mb) {
             uint32_t ra[2], rb[2];
-            bytes_to_f16(wa[mb][kk], ra);
-            bytes_to_f16(wb[mb][kk], rb);
-            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bq[kk][0], bq[kk][1]);
+            byte_regs(wa[mb][kk], ra);
+            byte_regs(wb[mb][kk], rb);
+            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bh[kk][0], bh[kk][1]);
             mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bl[kk][0], bl[kk][1]);
           }
         }
       }
+      if (sj == j) {
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+          ss[mb][0] = fmaf(s[mb][0], kTwo24, -beta0);
+          ss[mb][1] = fmaf(s[mb][1], kTwo24, -beta1);
+          ss[mb][2] = fmaf(s[mb][2], kTwo24, -beta0);
+          ss[mb][3] = fmaf(s[mb][3], kTwo24, -beta1);
+        }
+      }
     }
-    // ---- online softmax (base 2) over the 32 tokens -----------------------
-    float mx0 = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-    float mx1 = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
+    // ---- online softmax (base 2) over the 32 tokens of each column ----------
+    float mx0 = fmaxf(fmaxf(ss[0][0], ss[0][2]), fmaxf(ss[1][0], ss[1][2]));
+    float mx1 = fmaxf(fmaxf(ss[0][1], ss[0][3]), fmaxf(ss[1][1], ss[1][3]));
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-    const float a0 = fast_exp2(st.m0 - mn0), a1 = fast_exp2(st.m1 - mn1);
+    const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float a0 = fast_exp2(st.m0 - ms0), a1 = fast_exp2(st.m1 - ms1);
     st.m0 = mn0;
     st.m1 = mn1;
     float pr[2][4];
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
-      pr[mb][0] = fast_exp2(s[mb][0] - mn0);
-      pr[mb][1] = fast_exp2(s[mb][1] - mn1);
-      pr[mb][2] = fast_exp2(s[mb][2] - mn0);
-      pr[mb][3] = fast_exp2(s[mb][3] - mn1);
+      pr[mb][0] = fast_exp2(ss[mb][0] - ms0);
+      pr[mb][1] = fast_exp2(ss[mb][1] - ms1);
+      pr[mb][2] = fast_exp2(ss[mb][2] - ms0);
+      pr[mb][3] = fast_exp2(ss[mb][3] - ms1);
     }
     st.l0 = fmaf(st.l0, a0, (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
     st.l1 = fmaf(st.l1, a1, (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
@@ -296,55 +384,206 @@ __device__ __forceinline__ void mma_page(const uint8_t* pg, const PageGeom& geom
         st.O[mt][3] *= a1;
       }
     }
-    // ---- B operand of O: p / sV per token, transposed to the B layout ------
-    uint32_t bp[2][2];
+    // ---- p / sV (Value scale of this thread's stream page) ------------------
+    const float* vscale = reinterpret_cast<const float*>(vpg + geom.vscale_off) + sub * 32;
+    uint32_t pk[2][2];
+    float psum0 = 0.f, psum1 = 0.f;
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
-      const int r0 = sub * 32 + r_base + 4 * mb;
-      const float v0 = vscale[r0], v1 = vscale[r0 + 2];
-      bp[mb][0] = transpose8x8(pack_f16x2(__fdividef(pr[mb][0], v0), __fdividef(pr[mb][1], v0)));
-      bp[mb][1] = transpose8x8(pack_f16x2(__fdividef(pr[mb][2], v1), __fdividef(pr[mb][3], v1)));
+      const int r0 = token_row0<BITS>(gid, mb);
+      const float i0 = fast_rcp(vscale[r0]), i1 = fast_rcp(vscale[r0 + kGap]);
+      const float p00 = pr[mb][0] * i0, p01 = pr[mb][1] * i0, p10 = pr[mb][2] * i1, p11 = pr[mb][3] * i1;
+      const float f = BITS == 4 ? 0.0625f : 1.f;  // rows fed by the x16 registers
+      pk[mb][0] = pack_f16x2(p00, p01);
+      pk[mb][1] = pack_f16x2(p10 * f, p11 * f);
+      // the bias correction must subtract exactly what the MMA adds: sum the
+      // f16-rounded values
+      const float2 r0v = __half22float2(*reinterpret_cast<const __half2*>(&pk[mb][0]));
+      const float2 r1v = __half22float2(*reinterpret_cast<const __half2*>(&pk[mb][1]));
+      psum0 += r0v.x + r1v.x * (1.f / f);
+      psum1 += r0v.y + r1v.y * (1.f / f);
     }
-    // ---- O^T += V^T P ------------------------------------------------------
+    st.q0 = fmaf(st.q0, a0, psum0);
+    st.q1 = fmaf(st.q1, a1, psum1);
+    // ---- O'^T += V'^T P' for every page, P' masked to the page's columns ------
 #pragma unroll
-    for (int mt = 0; mt < S::kSteps; ++mt) {
-      const int c_lo = 16 * mt + gid, c_hi = c_lo + 8;
-      if (BITS == 4) {
-        const uint32_t wl = *reinterpret_cast<const uint32_t*>(vc + c_lo * 16 + 4 * tig);
-        const uint32_t wh = *reinterpret_cast<const uint32_t*>(vc + c_hi * 16 + 4 * tig);
-        uint32_t rl[4], rh[4];
-        nibbles_to_f16(wl, rl);
-        nibbles_to_f16(wh, rh);
-        mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
-        mma16816(st.O[mt], rl[2], rh[2], rl[3], rh[3], bp[1][0], bp[1][1]);
-      } else {
-        const uint2 vl = *reinterpret_cast<const uint2*>(vc + c_lo * 32 + 8 * tig);
-        const uint2 vh = *reinterpret_cast<const uint2*>(vc + c_hi * 32 + 8 * tig);
-        uint32_t rl[2], rh[2];
-        bytes_to_f16(vl.x, rl);
-        bytes_to_f16(vh.x, rh);
-        mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
-        bytes_to_f16(vl.y, rl);
-        bytes_to_f16(vh.y, rh);
-        mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[1][0], bp[1][1]);
+    for (int j = 0; j < S::PB; ++j) {
+      if (j >= npages) break;
+      const bool mine = sj == j;
+      uint32_t bp[2][2];
+#pragma unroll
+      for (int mb = 0; mb < 2; ++mb) {
+        bp[mb][0] = transpose8x8(mine ? pk[mb][0] : 0u);
+        bp[mb][1] = transpose8x8(mine ? pk[mb][1] : 0u);
+      }
+      const uint8_t* vc = pg[j] + geom.code_bytes + sub * S::kSubBytes;
+#pragma unroll
+      for (int mt = 0; mt < S::kSteps; ++mt) {
+        const int c_lo = 16 * mt + gid, c_hi = c_lo + 8;
+        if (BITS == 4) {
+          const uint32_t wl = *reinterpret_cast<const uint32_t*>(vc + c_lo * 16 + 4 * tig);
+          const uint32_t wh = *reinterpret_cast<const uint32_t*>(vc + c_hi * 16 + 4 * tig);
+          uint32_t rl[4], rh[4];
+          nibble_regs(wl, rl);
+          nibble_regs(wh, rh);
+          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
+          mma16816(st.O[mt], rl[2], rh[2], rl[3], rh[3], bp[1][0], bp[1][1]);
+        } else {
+          const uint2 vl = *reinterpret_cast<const uint2*>(vc + c_lo * 32 + 8 * tig);
+          const uint2 vh = *reinterpret_cast<const uint2*>(vc + c_hi * 32 + 8 * tig);
+          uint32_t rl[2], rh[2];
+          byte_regs(vl.x, rl);
+          byte_regs(vh.x, rh);
+          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
+          byte_regs(vl.y, rl);
+          byte_regs(vh.y, rh);
+          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[1][0], bp[1][1]);
+        }
       }
     }
   }
 }
 
-template <int D, int BITS>
+// The residual window of a unit on the tensor cores.  Steps of 16 tokens:
+// the bf16 Key/Value rows are copied from the ring into a per-warp shared
+// buffer (16-byte chunks XOR-swizzled by row so ldmatrix is conflict free;
+// rows past the window are zero-filled), then S = K q with bf16 MMAs (q is
+// the bf16 input, so every product is exact), the same online softmax as the
+// pages, and O^T += V^T P with V^T read by ldmatrix.trans and P as a bf16
+// hi + lo pair.  Column n holds head (n % GP) % g; only n < g is kept.
+template <int D, int GP>
+__device__ __forceinline__ void window_mma(const DecodeParams& p, int i, int h, int lane, int warp, int gid,
+                                           int tig, uint8_t* wbuf, WarpState<D>& st) {
+  constexpr int kRow = D * 2;             // bytes of one bf16 row
+  constexpr int kChunks = kRow / 16;      // 16-byte chunks per row
+  const int b = p.seq_begin + i;
+  const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+  const int W = (int)(T0 - Q0);
+  const int64_t unit = (int64_t)b * p.Hkv + h;
+  const __nv_bfloat16* rk = reinterpret_cast<const __nv_bfloat16*>(p.ring_k) + unit * p.Rcap * D;
+  const __nv_bfloat16* rv = reinterpret_cast<const __nv_bfloat16*>(p.ring_v) + unit * p.Rcap * D;
+  uint32_t bq[D / 16][2];
+  {
+    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                             ((int64_t)b * p.Hq + (int64_t)h * p.g + (gid % GP) % p.g) * D;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      bq[kk][0] = *reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig);
+      bq[kk][1] = *reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig + 8);
+    }
+  }
+  uint8_t* kb = wbuf;
+  uint8_t* vb = wbuf + 16 * kRow;
+  const uint32_t kb_s = smem_addr(kb), vb_s = smem_addr(vb);
+  const int nsteps = (W + 15) / 16;
+  for (int stp = warp; stp < nsteps; stp += kMmaWarps) {
+    const int t0 = stp * 16;
+    for (int idx = lane; idx < 16 * kChunks; idx += 32) {
+      const int r = idx / kChunks, c = idx - r * kChunks;
+      const bool valid = t0 + r < W;
+      const int64_t row = (Q0 + t0 + (valid ? r : 0)) % p.Rcap;
+      const uint32_t off = r * kRow + ((c ^ (r & 7)) * 16);
+      cp_async16(kb_s + off, rk + row * D + c * 8, valid ? 16u : 0u);
+      cp_async16(vb_s + off, rv + row * D + c * 8, valid ? 16u : 0u);
+    }
+    cp_async_wait_all();
+    __syncwarp();
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    {
+      const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        uint32_t a[4];
+        ldmatrix_x4(a, kb_s + r * kRow + (((2 * kk + (lane >> 4)) ^ (r & 7)) * 16));
+        mma16816_bf16(s, a[0], a[1], a[2], a[3], bq[kk][0], bq[kk][1]);
+      }
+    }
+    const bool v0 = t0 + gid < W, v1 = t0 + gid + 8 < W;
+    s[0] = v0 ? s[0] * p.qk_scale : -INFINITY;
+    s[1] = v0 ? s[1] * p.qk_scale : -INFINITY;
+    s[2] = v1 ? s[2] * p.qk_scale : -INFINITY;
+    s[3] = v1 ? s[3] * p.qk_scale : -INFINITY;
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+    const float a0 = fast_exp2(st.m0 - mn0), a1 = fast_exp2(st.m1 - mn1);  // mn is finite: row 0 is valid
+    st.m0 = mn0;
+    st.m1 = mn1;
+    const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
+    const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
+    st.l0 = fmaf(st.l0, a0, p0 + p2);
+    st.l1 = fmaf(st.l1, a1, p1 + p3);
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.O[mt][0] *= a0;
+      st.O[mt][1] *= a1;
+      st.O[mt][2] *= a0;
+      st.O[mt][3] *= a1;
+    }
+    uint32_t bh[2], bl[2];
+    {
+      const uint32_t h0 = pack_bf16x2(p0, p1), h1 = pack_bf16x2(p2, p3);
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h0));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h1));
+      bh[0] = transpose8x8(h0);
+      bh[1] = transpose8x8(h1);
+      bl[0] = transpose8x8(pack_bf16x2(p0 - f0.x, p1 - f0.y));
+      bl[1] = transpose8x8(pack_bf16x2(p2 - f1.x, p3 - f1.y));
+    }
+    {
+      const int r = (lane & 7) + 8 * (lane >> 4);
+#pragma unroll
+      for (int mt = 0; mt < D / 16; ++mt) {
+        uint32_t a[4];
+        ldmatrix_x4_trans(a, vb_s + r * kRow + (((2 * mt + ((lane >> 3) & 1)) ^ (r & 7)) * 16));
+        mma16816_bf16(st.O[mt], a[0], a[1], a[2], a[3], bh[0], bh[1]);
+        mma16816_bf16(st.O[mt], a[0], a[1], a[2], a[3], bl[0], bl[1]);
+      }
+    }
+    __syncwarp();  // the buffer is refilled by the next step
+  }
+}
+
+// Merge the thread's (m, l, O) of its two columns with lane ^ off (same heads,
+// another stream of pages).
+template <int D>
+__device__ __forceinline__ void merge_streams(WarpState<D>& st, int off) {
+  const float m0o = __shfl_xor_sync(0xffffffffu, st.m0, off), m1o = __shfl_xor_sync(0xffffffffu, st.m1, off);
+  const float l0o = __shfl_xor_sync(0xffffffffu, st.l0, off), l1o = __shfl_xor_sync(0xffffffffu, st.l1, off);
+  const float M0 = fmaxf(st.m0, m0o), M1 = fmaxf(st.m1, m1o);
+  const float s0 = M0 == -INFINITY ? 0.f : M0, s1 = M1 == -INFINITY ? 0.f : M1;
+  const float fa0 = fast_exp2(st.m0 - s0), fb0 = fast_exp2(m0o - s0);
+  const float fa1 = fast_exp2(st.m1 - s1), fb1 = fast_exp2(m1o - s1);
+  st.l0 = st.l0 * fa0 + l0o * fb0;
+  st.l1 = st.l1 * fa1 + l1o * fb1;
+  st.m0 = M0;
+  st.m1 = M1;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    const float o0 = __shfl_xor_sync(0xffffffffu, st.O[mt][0], off);
+    const float o1 = __shfl_xor_sync(0xffffffffu, st.O[mt][1], off);
+    const float o2 = __shfl_xor_sync(0xffffffffu, st.O[mt][2], off);
+    const float o3 = __shfl_xor_sync(0xffffffffu, st.O[mt][3], off);
+    st.O[mt][0] = st.O[mt][0] * fa0 + o0 * fb0;
+    st.O[mt][1] = st.O[mt][1] * fa1 + o1 * fb1;
+    st.O[mt][2] = st.O[mt][2] * fa0 + o2 * fb0;
+    st.O[mt][3] = st.O[mt][3] * fa1 + o3 * fb1;
+  }
+}
+
+template <int D, int BITS, int GP>
 __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeParams p, int slots) {
-  using S = Shape<D, BITS>;
+  using S = Shape<D, BITS, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int u = blockIdx.y;
   const int i = u / p.Hkv, h = u - i * p.Hkv;
   bool win;
   int pg0, pg1, slot;
   if (!split_item(p, blockIdx.x, i, &win, &pg0, &pg1, &slot)) return;
-  if (win) {
-    simt_item<__nv_bfloat16, BITS, D / 32>(p, i, h, true, 0, 0, slot, reinterpret_cast<float*>(smem));
-    return;
-  }
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
@@ -353,18 +592,45 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
   const PageGeom geom = p.geom;
   const uint32_t page_bytes = (uint32_t)geom.page_bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  uint8_t* buf = smem + ((kMmaWarps * slots * 8 + 127) / 128) * 128;
+  float* scratch = reinterpret_cast<float*>(smem + 128 * ((kMmaWarps * slots * 8 + 127) / 128));
+  float* my_rsc = scratch + warp * S::PB * D;
+  uint8_t* buf = reinterpret_cast<uint8_t*>(scratch + kMmaWarps * S::PB * D);
   uint8_t* my_buf = buf + (size_t)warp * slots * page_bytes;
   const uint32_t my_bar = smem_addr(bars + warp * slots);
 
-  // this thread's query slice (head gid, channels tig*D/4 ...), pre-scaled
-  const bool qlive = gid < g;
+  WarpState<D> st;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
+  st.m0 = st.m1 = -INFINITY;
+  st.l0 = st.l1 = st.q0 = st.q1 = 0.f;
+  bool ok = true;
+
+  if (win) {
+    window_mma<D, GP>(p, i, h, lane, warp, gid, tig, buf + (size_t)warp * 32 * D * 2, st);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+      st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+    }
+  } else {
+  // query slice of head (gid % GP) -- a real head of this KV head even for the
+  // padding columns, so every value stays finite -- channels tig*D/4 .., pre-scaled
   float qreg[S::kChan];
   {
-    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                             ((int64_t)b * p.Hq + (int64_t)h * g + (qlive ? gid : 0)) * D + tig * S::kChan;
+    const int hq = (gid % GP) % g;
+    const __nv_bfloat16* q =
+        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g + hq) * D + tig * S::kChan;
 #pragma unroll
-    for (int c = 0; c < S::kChan; ++c) qreg[c] = qlive ? __bfloat162float(q[c]) * p.qk_scale : 0.f;
+    for (int c = 0; c < S::kChan; c += 8) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(q + c);
+      const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(v[e]);
+        qreg[c + 2 * e] = f.x * p.qk_scale;
+        qreg[c + 2 * e + 1] = f.y * p.qk_scale;
+      }
+    }
   }
 
   const uint8_t* unit_pages = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride;
@@ -382,28 +648,28 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
   }
   __syncwarp();
 
-  WarpState<D, BITS> st;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
-  st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = 0.f;
-
   int k = 0;
-  bool ok = true;
-  for (; k < my_n; ++k) {
-    const int s = k % slots;
-    if (!mbar_wait(my_bar + 8 * s, (uint32_t)((k / slots) & 1))) {
-      ok = false;
-      break;
-    }
-    mma_page<D, BITS>(my_buf + (size_t)s * page_bytes, geom, p.G, qlive, qreg, gid, tig, st);
+  for (; k < my_n; k += S::PB) {
+    const int np = min(S::PB, my_n - k);
+    const uint8_t* pgs[S::PB];
+#pragma unroll
+    for (int j = 0; j < S::PB; ++j) pgs[j] = my_buf + (size_t)((k + min(j, np - 1)) % slots) * page_bytes;
+    for (int j = 0; j < np && ok; ++j)
+      ok = mbar_wait(my_bar + 8 * ((k + j) % slots), (uint32_t)(((k + j) / slots) & 1));
+    if (!ok) break;
+    mma_group<D, BITS, GP>(pgs, np, geom, p.G, qreg, my_rsc, lane, gid, tig, st);
     __syncwarp();
-    if (lane == 0 && k + slots < my_n) {
+    if (lane == 0) {
       fence_proxy_async();
-      mbar_expect_tx(my_bar + 8 * s, page_bytes);
-      bulk_load(smem_addr(my_buf + (size_t)s * page_bytes),
-                unit_pages + (int64_t)(pg0 + warp + (k + slots) * kMmaWarps) * page_bytes, page_bytes,
-                my_bar + 8 * s);
+      for (int j = 0; j < np; ++j) {
+        const int kk = k + j;
+        if (kk + slots < my_n) {
+          mbar_expect_tx(my_bar + 8 * (kk % slots), page_bytes);
+          bulk_load(smem_addr(my_buf + (size_t)(kk % slots) * page_bytes),
+                    unit_pages + (int64_t)(pg0 + warp + (kk + slots) * kMmaWarps) * page_bytes, page_bytes,
+                    my_bar + 8 * (kk % slots));
+        }
+      }
     }
   }
   if (!ok) {
@@ -412,31 +678,52 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
     for (int kk = k; kk < issued; ++kk) mbar_wait(my_bar + 8 * (kk % slots), (uint32_t)((kk / slots) & 1));
     if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
     st.m0 = st.m1 = -INFINITY;
-    st.l0 = st.l1 = 0.f;
+    st.l0 = st.l1 = st.q0 = st.q1 = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
   }
+  // sums over the thread's rows -> over the warp's rows; undo the code bias
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
+    st.q0 += __shfl_xor_sync(0xffffffffu, st.q0, off);
+    st.q1 += __shfl_xor_sync(0xffffffffu, st.q1, off);
   }
+  {
+    constexpr float kTwo24 = 16777216.f;
+    const float c0 = S::kBias * st.q0, c1 = S::kBias * st.q1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.O[mt][0] = fmaf(st.O[mt][0], kTwo24, -c0);
+      st.O[mt][1] = fmaf(st.O[mt][1], kTwo24, -c1);
+      st.O[mt][2] = fmaf(st.O[mt][2], kTwo24, -c0);
+      st.O[mt][3] = fmaf(st.O[mt][3], kTwo24, -c1);
+    }
+  }
+  // fold the page streams onto stream 0 (columns 0 .. GP-1)
+#pragma unroll
+  for (int off = GP / 2; off < 4; off <<= 1) merge_streams<D>(st, off);
+  }  // page path
   __syncthreads();  // every warp is done with its slots: reuse them for the merge
 
   float* mrg = reinterpret_cast<float*>(buf);  // [kMmaWarps][kMaxGqa][D + 2]
-  const int hd0 = 2 * tig, hd1 = 2 * tig + 1;
+  const int hd0 = 2 * tig, hd1 = 2 * tig + 1;  // heads of the stream-0 columns
   float* mw = mrg + (size_t)warp * kMaxGqa * (D + 2);
+  const bool stream0 = 2 * tig < GP;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     const int c_lo = 16 * mt + gid;
-    if (hd0 < g) {
-      mw[hd0 * (D + 2) + c_lo] = ok ? st.O[mt][0] : 0.f;
-      mw[hd0 * (D + 2) + c_lo + 8] = ok ? st.O[mt][2] : 0.f;
+    if (stream0 && hd0 < g) {
+      mw[hd0 * (D + 2) + c_lo] = st.O[mt][0];
+      mw[hd0 * (D + 2) + c_lo + 8] = st.O[mt][2];
     }
-    if (hd1 < g) {
-      mw[hd1 * (D + 2) + c_lo] = ok ? st.O[mt][1] : 0.f;
-      mw[hd1 * (D + 2) + c_lo + 8] = ok ? st.O[mt][3] : 0.f;
+    if (stream0 && hd1 < g) {
+      mw[hd1 * (D + 2) + c_lo] = st.O[mt][1];
+      mw[hd1 * (D + 2) + c_lo + 8] = st.O[mt][3];
     }
   }
-  if (gid == 0) {
+  if (gid == 0 && stream0) {
     if (hd0 < g) {
       mw[hd0 * (D + 2) + D] = st.m0;
       mw[hd0 * (D + 2) + D + 1] = st.l0;
@@ -473,37 +760,57 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
   }
 }
 
-int mma_slots(int64_t page_bytes) {
-  int slots = (int)(80 * 1024 / (kMmaWarps * page_bytes));
-  if (slots < 2) slots = 2;
-  if (slots > 6) slots = 6;
+int gqa_pad(int g) { return g <= 2 ? 2 : g <= 4 ? 4 : 8; }
+
+// Shared-memory page slots per warp: about 60 KB of pages per CTA, at least
+// one group (8 / padded g pages) and at most 8.
+int mma_slots(int64_t page_bytes, int g) {
+  const int pb = 8 / gqa_pad(g);
+  int slots = (int)(60 * 1024 / (kMmaWarps * page_bytes));
+  if (slots < pb) slots = pb;
+  if (slots > 8) slots = 8;
   return slots;
 }
 
+constexpr size_t kMaxSmem = 227 * 1024;
+
 template <int D>
 size_t smem_for(const DecodeParams& p) {
-  const int slots = mma_slots(p.geom.page_bytes);
+  const int slots = mma_slots(p.geom.page_bytes, p.g);
   size_t pages = (size_t)kMmaWarps * slots * p.geom.page_bytes;
   const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
-  const size_t simt = (size_t)simt_scratch_floats<D / 32>() * sizeof(float);
+  const size_t window = (size_t)kMmaWarps * 32 * D * 2;  // per warp 16 K rows + 16 V rows of bf16
   if (pages < merge) pages = merge;
-  if (pages < simt) pages = simt;
-  return ((kMmaWarps * slots * 8 + 127) / 128) * 128 + pages;
+  if (pages < window) pages = window;
+  const size_t scratch = (size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D * sizeof(float);
+  return 128 * ((kMmaWarps * slots * 8 + 127) / 128) + scratch + pages;
+}
+
+template <int D, int BITS, int GP>
+cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
+  const size_t smem = smem_for<D>(p);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static size_t configured[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > configured[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, GP>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
+  }
+  const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
+  decode_mma_kernel<D, BITS, GP><<<grid, kMmaThreads, smem, s>>>(p, mma_slots(p.geom.page_bytes, p.g));
+  return cudaGetLastError();
 }
 
 template <int D, int BITS>
-cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
-  const size_t smem = smem_for<D>(p);
-  static size_t configured = 0;
-  if (smem > configured) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured = smem;
+cudaError_t launch_g(const DecodeParams& p, cudaStream_t s) {
+  switch (gqa_pad(p.g)) {
+    case 2: return launch_t<D, BITS, 2>(p, s);
+    case 4: return launch_t<D, BITS, 4>(p, s);
+    default: return launch_t<D, BITS, 8>(p, s);
   }
-  const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
-  decode_mma_kernel<D, BITS><<<grid, kMmaThreads, smem, s>>>(p, mma_slots(p.geom.page_bytes));
-  return cudaGetLastError();
 }
 
 }  // namespace
@@ -513,10 +820,11 @@ size_t decode_mma_smem_bytes(const DecodeParams& p) {
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported) {
-  *supported = (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g <= kMaxGqa;
+  *supported = (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g >= 2 && p.g <= kMaxGqa &&
+               decode_mma_smem_bytes(p) <= kMaxSmem;
   if (!*supported) return cudaSuccess;
-  if (p.D == 64) return p.bits == 4 ? launch_t<64, 4>(p, s) : launch_t<64, 8>(p, s);
-  return p.bits == 4 ? launch_t<128, 4>(p, s) : launch_t<128, 8>(p, s);
+  if (p.D == 64) return p.bits == 4 ? launch_g<64, 4>(p, s) : launch_g<64, 8>(p, s);
+  return p.bits == 4 ? launch_g<128, 4>(p, s) : launch_g<128, 8>(p, s);
 }
 
 }  // namespace kvq

@@ -381,9 +381,10 @@ kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void
   const int kernel = opts ? opts->kernel : 0;
   if (kernel < 0 || kernel > 2) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
   const bool mma_ok = c->cfg.dtype == KVQ_BF16 && (c->cfg.head_dim == 64 || c->cfg.head_dim == 128) &&
-                      c->cfg.group % 32 == 0;
+                      c->cfg.group % 32 == 0 && c->g >= 2;
   if (kernel == 2 && !mma_ok)
-    return fail(KVQ_EUNSUPPORTED, "tensor-core kernel needs bf16, head_dim 64/128 and group %% 32 == 0");
+    return fail(KVQ_EUNSUPPORTED,
+                "tensor-core kernel needs bf16, head_dim 64/128, group %% 32 == 0 and >= 2 query heads per KV head");
   const bool use_mma = kernel == 2 || (kernel == 0 && mma_ok);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (opts && opts->split_start) {
@@ -407,14 +408,14 @@ kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void
     p.seq_begin = bt.s0;
     p.n_seqs = bt.n;
     fill_counters(c, bt.s0, bt.n, p.ctr);
-    cudaError_t e;
+    cudaError_t e = cudaSuccess;
+    int supported = 0;
     if (use_mma) {
-      int supported = 0;
       e = kvq::launch_decode_mma(p, s, &supported);
-      if (e == cudaSuccess && !supported) return fail(KVQ_EUNSUPPORTED, "tensor-core kernel not applicable");
-    } else {
-      e = kvq::launch_decode_simt(p, c->cfg.dtype, s);
+      if (e == cudaSuccess && !supported && kernel == 2)
+        return fail(KVQ_EUNSUPPORTED, "tensor-core kernel does not fit this configuration (shared memory)");
     }
+    if (e == cudaSuccess && !supported) e = kvq::launch_decode_simt(p, c->cfg.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
     g_launches += 1;
     batches.push_back(bt);
@@ -520,7 +521,7 @@ kvq_status kvq_decode_attention_noalloc(kvq_cache* c, const void* q, float* out,
   float* scratch = nullptr;
   kvq_status st = noalloc_scratch(c->device, &scratch);
   if (st != KVQ_OK) return st;
-  const bool use_mma = c->cfg.dtype == KVQ_BF16 && (D == 64 || D == 128) && c->cfg.group % 32 == 0;
+  const bool use_mma = c->cfg.dtype == KVQ_BF16 && (D == 64 || D == 128) && c->cfg.group % 32 == 0 && c->g >= 2;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   for (int s0 = 0; s0 < B; s0 += kvq::kMaxSeqsPerLaunch) {
     const int n = std::min(kvq::kMaxSeqsPerLaunch, B - s0);
@@ -534,13 +535,10 @@ kvq_status kvq_decode_attention_noalloc(kvq_cache* c, const void* q, float* out,
     p.seq_begin = s0;
     p.n_seqs = n;
     fill_counters(c, s0, n, p.ctr);
-    cudaError_t e;
-    if (use_mma) {
-      int supported = 0;
-      e = kvq::launch_decode_mma(p, s, &supported);
-    } else {
-      e = kvq::launch_decode_simt(p, c->cfg.dtype, s);
-    }
+    cudaError_t e = cudaSuccess;
+    int supported = 0;
+    if (use_mma) e = kvq::launch_decode_mma(p, s, &supported);
+    if (e == cudaSuccess && !supported) e = kvq::launch_decode_simt(p, c->cfg.dtype, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode split launch");
     g_launches += 1;
   }
