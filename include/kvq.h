@@ -132,9 +132,11 @@ typedef struct kvq_cache kvq_cache; /* opaque host handle */
  *
  * Group page: one per (sequence, KV head, flushed group), written once by the
  * flush and never again.  With bits = 4 (qmax <= 7) or 8, in order:
+ *   Codes are stored offset binary: code + 8 in a nibble (1..15 for qmax 7),
+ *   code + 128 in a byte.
  *   1. Key codes: G rows (token order) of head_dim*bits/8 bytes.  4-bit: byte i
- *      holds channel 2i in bits 0-3 and channel 2i+1 in bits 4-7 (two's
- *      complement nibbles); 8-bit: byte c is channel c.
+ *      holds channel 2i in bits 0-3 and channel 2i+1 in bits 4-7; 8-bit: byte c
+ *      is channel c.
  *   2. Value codes in sub-tiles of 32 tokens (the last sub-tile holds G mod 32
  *      tokens if G is not a multiple of 32).  A sub-tile of n tokens is head_dim
  *      rows (channel order) of n*bits/8 bytes.  4-bit rows are little-endian

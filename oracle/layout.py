@@ -6,9 +6,11 @@ it to compare the GPU cache's raw bytes with the oracle's codes and scales.
 
 Layout of one group page (G tokens, D channels, ``bits`` = 4 or 8):
 
+Codes are stored offset binary: code + 8 in a nibble, code + 128 in a byte.
+
 1. Key codes, G rows in token order, D*bits/8 bytes each.  4-bit: byte i
-   holds channel 2i in bits 0-3 and channel 2i+1 in bits 4-7, as two's
-   complement nibbles.  8-bit: byte c is channel c (two's complement).
+   holds channel 2i in bits 0-3 and channel 2i+1 in bits 4-7.  8-bit: byte c
+   is channel c.
 2. Value codes, in sub-tiles of 32 tokens (the last sub-tile holds G mod 32
    tokens when G is not a multiple of 32).  A sub-tile of n tokens is D rows
    (channel order) of n*bits/8 bytes.  4-bit rows are little-endian 32-bit
@@ -25,7 +27,11 @@ import numpy as np
 
 
 def _nibble(code: int) -> int:
-    return int(code) & 0xF
+    return (int(code) + 8) & 0xF
+
+
+def _byte(code: int) -> int:
+    return (int(code) + 128) & 0xFF
 
 
 def pack_key_codes(codes: np.ndarray, bits: int) -> bytes:
@@ -38,7 +44,7 @@ def pack_key_codes(codes: np.ndarray, bits: int) -> bytes:
                 out.append(_nibble(codes[t, 2 * i]) | (_nibble(codes[t, 2 * i + 1]) << 4))
         else:
             for c in range(D):
-                out.append(int(codes[t, c]) & 0xFF)
+                out.append(_byte(codes[t, c]))
     return bytes(out)
 
 
@@ -63,7 +69,7 @@ def pack_value_codes(codes: np.ndarray, bits: int) -> bytes:
                     out += word.to_bytes(4, "little")
             else:
                 for i in range(n):
-                    out.append(int(codes[start + i, c]) & 0xFF)
+                    out.append(_byte(codes[start + i, c]))
     return bytes(out)
 
 

@@ -24,25 +24,45 @@ namespace {
 
 constexpr int kAppendThreads = 256;
 
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-
 __device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
   float r = rintf(__fmul_rn(x, scale));
   r = fminf(fmaxf(r, -qmax), qmax);
   return (int)r;
 }
 
-// Stage the G x D tile of tokens [t_first, t_first + G) as fp32 in shared memory.
+// 16 bytes of elements -> fp32 into shared memory.
+__device__ __forceinline__ void store_f32(float* dst, const uint4& raw, float) {
+  const float* f = reinterpret_cast<const float*>(&raw);
+  dst[0] = f[0];
+  dst[1] = f[1];
+  dst[2] = f[2];
+  dst[3] = f[3];
+}
+__device__ __forceinline__ void store_f32(float* dst, const uint4& raw, __nv_bfloat16) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    dst[2 * e] = f.x;
+    dst[2 * e + 1] = f.y;
+  }
+}
+
+// Stage the G x D tile of tokens [t_first, t_first + G) as fp32 in shared
+// memory, 16 bytes per load.  Tokens below T0 come from the ring: a group
+// starts at a multiple of G and the ring length is a multiple of G, so its
+// rows are contiguous there.  Later tokens come from the input.
 template <typename T>
-__device__ void load_group(float* tile, const T* ring, const T* input, int64_t t_first, int64_t T0,
-                           int G, int D, int Rcap) {
-  const int n = G * D;
-  for (int idx = threadIdx.x; idx < n; idx += blockDim.x) {
-    const int tl = idx / D, c = idx - tl * D;
-    const int64_t t = t_first + tl;
-    const T v = t < T0 ? ring[(t % Rcap) * D + c] : input[(t - T0) * D + c];
-    tile[idx] = to_f32(v);
+__device__ void load_group(float* tile, const T* ring, const T* input, int t_first, int T0, int G, int D,
+                           int Rcap) {
+  constexpr int kVec = 16 / sizeof(T);
+  const int per_row = D / kVec;
+  const int ring_row0 = t_first % Rcap;
+  for (int idx = threadIdx.x; idx < G * per_row; idx += blockDim.x) {
+    const int tl = idx / per_row, c = (idx - tl * per_row) * kVec;
+    const int t = t_first + tl;
+    const T* src = t < T0 ? ring + (size_t)(ring_row0 + tl) * D + c : input + (size_t)(t - T0) * D + c;
+    store_f32(tile + tl * D + c, *reinterpret_cast<const uint4*>(src), T());
   }
 }
 
@@ -53,12 +73,13 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   const int h = blockIdx.z;
   const int b = p.seq_begin + i;
   const int D = p.D, G = p.G, Rcap = p.Rcap;
-  const int64_t T0 = p.old[i].total;
-  const int64_t Q0 = p.old[i].quantized;
-  const int64_t n = p.n;
-  const int64_t F = flush_groups(T0 - Q0, n, p.R, G);
-  const int64_t Q1 = Q0 + F * G;
-  const int64_t T1 = T0 + n;
+  // token counts fit in 32 bits (capacities are below 2^31)
+  const int T0 = p.old[i].total;
+  const int Q0 = p.old[i].quantized;
+  const int n = (int)p.n;
+  const int F = (int)flush_groups(T0 - Q0, n, p.R, G);
+  const int Q1 = Q0 + F * G;
+  const int T1 = T0 + n;
   const int64_t unit = (int64_t)b * p.Hkv + h;
   const T* in_k = reinterpret_cast<const T*>(p.new_k) + ((int64_t)i * p.Hkv + h) * n * D;
   const T* in_v = reinterpret_cast<const T*>(p.new_v) + ((int64_t)i * p.Hkv + h) * n * D;
@@ -66,23 +87,26 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   T* ring_v = reinterpret_cast<T*>(p.ring_v) + unit * Rcap * D;
 
   if ((int)blockIdx.x >= p.flush_blocks) {
-    // Window block: the new tokens that stay in the residual window.
-    const int64_t t_lo = Q1 > T0 ? Q1 : T0;
-    const int64_t count = (T1 - t_lo) * D;
-    for (int64_t idx = threadIdx.x; idx < count; idx += blockDim.x) {
-      const int64_t t = t_lo + idx / D;
-      const int c = (int)(idx % D);
-      const int64_t src = (t - T0) * D + c;
-      const int64_t dst = (t % Rcap) * D + c;
-      ring_k[dst] = in_k[src];
-      ring_v[dst] = in_v[src];
+    // Window block: the new tokens that stay in the residual window, copied
+    // 16 bytes at a time.
+    constexpr int kVec = 16 / sizeof(T);
+    const int per_row = D / kVec;
+    const int t_lo = Q1 > T0 ? Q1 : T0;
+    const int count = (T1 - t_lo) * per_row;
+    for (int idx = threadIdx.x; idx < count; idx += blockDim.x) {
+      const int r = idx / per_row, c = (idx - r * per_row) * kVec;
+      const int t = t_lo + r;
+      const size_t src = (size_t)(t - T0) * D + c;
+      const size_t dst = (size_t)(t % Rcap) * D + c;
+      *reinterpret_cast<uint4*>(ring_k + dst) = *reinterpret_cast<const uint4*>(in_k + src);
+      *reinterpret_cast<uint4*>(ring_v + dst) = *reinterpret_cast<const uint4*>(in_v + src);
     }
     return;
   }
 
-  const int64_t j = blockIdx.x;
+  const int j = blockIdx.x;
   if (j >= F) return;
-  const int64_t t_first = Q0 + j * G;
+  const int t_first = Q0 + j * G;
   const PageGeom& geom = p.geom;
   uint8_t* page = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride +
                   (t_first / G) * geom.page_bytes;
@@ -90,6 +114,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   float* sK = tile + G * D;
   float* sV = sK + D;
   const float qmax = (float)p.qmax;
+  constexpr int kBias = BITS == 4 ? 8 : 128;  // stored offset binary: code + bias
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
   // ---- Key: per-channel absmax over the group's tokens --------------------
@@ -113,7 +138,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
       for (int k = 0; k < kPerWord; ++k) {
         const int c = w * kPerWord + k;
         const int code = quantize_one(tile[t * D + c], sK[c], qmax);
-        word |= ((uint32_t)code & ((1u << BITS) - 1u)) << (BITS * k);
+        word |= ((uint32_t)(code + kBias)) << (BITS * k);
       }
       kc[idx] = word;
     }
@@ -148,7 +173,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
           for (int jn = 0; jn < 8; ++jn) {
             const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
             const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
-            word |= ((uint32_t)code & 0xFu) << (4 * jn);
+            word |= ((uint32_t)(code + kBias)) << (4 * jn);
           }
           vc[idx] = word;
         }
@@ -161,7 +186,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
           for (int k = 0; k < 4; ++k) {
             const int tok = 32 * st + 4 * w + k;
             const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
-            word |= ((uint32_t)code & 0xFFu) << (8 * k);
+            word |= ((uint32_t)(code + kBias)) << (8 * k);
           }
           vc[idx] = word;
         }

@@ -105,30 +105,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // ---- codes as f16 subnormals --------------------------------------------
-// A stored code is two's complement; adding the bias (8 for 4-bit, 128 for
-// 8-bit) makes it an unsigned u in [1, 2*bias).  A 16-bit half whose bits are
-// just u (exponent 0) is the binary16 subnormal u * 2^-24, exactly; u << 4 is
-// 16 * u * 2^-24.  So masking the biased word yields MMA operands without any
-// floating-point conversion; the 2^-24, the x16 of the second nibble position
-// (cancelled by a 1/16 on the matching B rows) and the bias are undone after
-// the MMA: S = 2^24 * S' - bias * sum(B),  O = 2^24 * O' - bias * sum(p').
+// A stored code is offset binary: u = code + bias (bias 8 for 4-bit, 128 for
+// 8-bit), u in [1, 2*bias).  A 16-bit half whose bits are just u (exponent 0)
+// is the binary16 subnormal u * 2^-24, exactly; u << 4 is 16 * u * 2^-24.  So
+// masking the stored word yields MMA operands without any floating-point
+// conversion; the 2^-24, the x16 of the second nibble position (cancelled by a
+// 1/16 on the matching B rows) and the bias are undone after the MMA:
+// S = 2^24 * S' - bias * sum(B),  O = 2^24 * O' - bias * sum(p').
 
 // 4-bit: word of eight nibbles -> r[j] = (nibble j, nibble j + 4) as f16x2;
 // r[1] and r[3] carry an extra factor 16.
 __device__ __forceinline__ void nibble_regs(uint32_t w, uint32_t (&r)[4]) {
-  const uint32_t t = w ^ 0x88888888u;
-  const uint32_t t2 = t >> 8;
-  r[0] = t & 0x000F000Fu;
-  r[1] = t & 0x00F000F0u;
-  r[2] = t2 & 0x000F000Fu;
-  r[3] = t2 & 0x00F000F0u;
+  const uint32_t w2 = w >> 8;
+  r[0] = w & 0x000F000Fu;
+  r[1] = w & 0x00F000F0u;
+  r[2] = w2 & 0x000F000Fu;
+  r[3] = w2 & 0x00F000F0u;
 }
 
 // 8-bit: word of four bytes -> r[0] = (byte 0, byte 2), r[1] = (byte 1, byte 3).
 __device__ __forceinline__ void byte_regs(uint32_t w, uint32_t (&r)[2]) {
-  const uint32_t t = w ^ 0x80808080u;
-  r[0] = t & 0x00FF00FFu;
-  r[1] = (t >> 8) & 0x00FF00FFu;
+  r[0] = w & 0x00FF00FFu;
+  r[1] = (w >> 8) & 0x00FF00FFu;
 }
 
 __device__ __forceinline__ float fast_rcp(float x) {
@@ -229,26 +227,34 @@ __device__ __forceinline__ constexpr int token_row_gap() {
 template <int D>
 struct WarpState {
   float O[D / 16][4];  // O'^T accumulators (biased codes, scaled by 2^-24)
+  float C[4];          // 2^-24 * sum of the p / sV each column fed to O' (for the bias)
   float m0, m1;        // running max of the thread's two columns (base 2)
   float l0, l1;        // running sum of p (partial over this thread's rows)
-  float q0, q1;        // running sum of p / sV (partial), for the bias
 };
 
-// A group of up to PB pages (already in shared memory) of one warp.
-template <int D, int BITS, int GP>
-__device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BITS, GP>::PB], int npages,
-                                          const PageGeom& geom, int G, const float (&qreg)[D / 4],
-                                          float* rsc, int lane, int gid, int tig, WarpState<D>& st) {
+// A group of PB pages (FULL) or of npages < PB pages (the tail of a warp's
+// run), already in shared memory.
+template <int D, int BITS, int GP, bool FULL>
+__device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BITS, GP>::PB], int npages_rt,
+                                          const PageGeom& geom, int G, const float4* q4, float* rsc, int lane,
+                                          int gid, int tig, WarpState<D>& st) {
   using S = Shape<D, BITS, GP>;
   constexpr float kTwo24 = 16777216.f;
+  const int npages = FULL ? S::PB : npages_rt;
   // ---- reciprocal Key scales, cooperatively, in a bank-friendly order -------
-  // chunk i (channels tig*kChan + 4i .. +3) of slice tig goes to float4 slot i*4 + tig
+  // chunk i (channels tig*kChan + 4i .. +3) of slice tig goes to float4 slot
+  // i*4 + tig.  For 4-bit codes the odd channels meet the x16 registers, so
+  // their reciprocals carry the compensating 1/16.
+  static_assert((S::PB * S::kChunks) % 32 == 0 || S::PB * S::kChunks < 32, "chunk split");
 #pragma unroll
-  for (int q = lane; q < S::PB * S::kChunks; q += 32) {
+  for (int it = 0; it < (S::PB * S::kChunks + 31) / 32; ++it) {
+    const int q = lane + 32 * it;
     const int j = q / S::kChunks, cc = q - j * S::kChunks;
-    if (j < npages) {
+    if (q < S::PB * S::kChunks && j < npages) {
       const float4 s4 = reinterpret_cast<const float4*>(pg[j] + geom.kscale_off)[cc];
-      const float4 r4 = make_float4(fast_rcp(s4.x), fast_rcp(s4.y), fast_rcp(s4.z), fast_rcp(s4.w));
+      constexpr float kOdd = BITS == 4 ? 0.0625f : 1.f;
+      const float4 r4 =
+          make_float4(fast_rcp(s4.x), fast_rcp(s4.y) * kOdd, fast_rcp(s4.z), fast_rcp(s4.w) * kOdd);
       const int tg = cc / (S::kChan / 4), i = cc - tg * (S::kChan / 4);
       reinterpret_cast<float4*>(rsc + j * D)[i * 4 + tg] = r4;
     }
@@ -258,19 +264,23 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
   uint32_t bh[S::kSteps][2], bl[S::kSteps][2];
   float beta0, beta1;
   {
-    const int jb = min(gid / GP, npages - 1);
+    const int jb = FULL ? gid / GP : min(gid / GP, npages - 1);
     const float4* rj = reinterpret_cast<const float4*>(rsc + jb * D);
     float qk[S::kChan];
-    float beta = 0.f;
+    float be = 0.f, bo = 0.f;  // sums over even / odd channels
+    const int hq = gid % GP;
 #pragma unroll
     for (int i = 0; i < S::kChan / 4; ++i) {
       const float4 r = rj[i * 4 + tig];
-      qk[4 * i + 0] = qreg[4 * i + 0] * r.x;
-      qk[4 * i + 1] = qreg[4 * i + 1] * r.y;
-      qk[4 * i + 2] = qreg[4 * i + 2] * r.z;
-      qk[4 * i + 3] = qreg[4 * i + 3] * r.w;
-      beta += (qk[4 * i + 0] + qk[4 * i + 1]) + (qk[4 * i + 2] + qk[4 * i + 3]);
+      const float4 qv = q4[(i * GP + hq) * 4 + tig];
+      qk[4 * i + 0] = qv.x * r.x;
+      qk[4 * i + 1] = qv.y * r.y;
+      qk[4 * i + 2] = qv.z * r.z;
+      qk[4 * i + 3] = qv.w * r.w;
+      be += qk[4 * i + 0] + qk[4 * i + 2];
+      bo += qk[4 * i + 1] + qk[4 * i + 3];
     }
+    float beta = BITS == 4 ? fmaf(bo, 16.f, be) : be + bo;
     beta += __shfl_xor_sync(0xffffffffu, beta, 1);
     beta += __shfl_xor_sync(0xffffffffu, beta, 2);
     beta0 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig));
@@ -279,8 +289,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
     for (int kk = 0; kk < S::kSteps; ++kk) {
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
-        const float f = (BITS == 4 && r == 1) ? 0.0625f : 1.f;
-        const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)] * f, x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)] * f;
+        const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)], x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)];
         const __half2 hi = __floats2half2_rn(x0, x1);
         const float2 back = __half22float2(hi);
         const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
@@ -290,12 +299,16 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
     }
   }
   const int sj = (2 * tig) / GP;                  // this thread's stream (both columns)
-  const int vpage = min(sj, npages - 1);          // a valid page for its Value scales
+  const int vpage = FULL ? sj : min(sj, npages - 1);  // a valid page for its Value scales
   const uint8_t* vpg = pg[0];
 #pragma unroll
   for (int j = 1; j < S::PB; ++j)
     if (j == vpage) vpg = pg[j];
   constexpr int kGap = token_row_gap<BITS>();
+  // A operand of the p/sV counter: the value 1 (or 16 on the x16 k-slots) in
+  // every element, as 2^-24-scaled subnormals like the codes
+  constexpr uint32_t kOneLo = 0x00010001u;
+  constexpr uint32_t kOneHi = BITS == 4 ? 0x00100010u : 0x00010001u;
 
   for (int sub = 0; sub < G / 32; ++sub) {
     // ---- scores of every page; keep each column's own page ------------------
@@ -304,7 +317,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
     for (int mb = 0; mb < 2; ++mb) ss[mb][0] = ss[mb][1] = ss[mb][2] = ss[mb][3] = -INFINITY;
 #pragma unroll
     for (int j = 0; j < S::PB; ++j) {
-      if (j >= npages) break;
+      if (!FULL && j >= npages) break;
       const uint8_t* kc = pg[j] + sub * 32 * S::kRowBytes;
       uint32_t wa[2][S::kWords], wb[2][S::kWords];
       float s[2][4];
@@ -342,14 +355,13 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
           }
         }
       }
-      if (sj == j) {
+      const bool mine = sj == j;
 #pragma unroll
-        for (int mb = 0; mb < 2; ++mb) {
-          ss[mb][0] = fmaf(s[mb][0], kTwo24, -beta0);
-          ss[mb][1] = fmaf(s[mb][1], kTwo24, -beta1);
-          ss[mb][2] = fmaf(s[mb][2], kTwo24, -beta0);
-          ss[mb][3] = fmaf(s[mb][3], kTwo24, -beta1);
-        }
+      for (int mb = 0; mb < 2; ++mb) {
+        ss[mb][0] = mine ? fmaf(s[mb][0], kTwo24, -beta0) : ss[mb][0];
+        ss[mb][1] = mine ? fmaf(s[mb][1], kTwo24, -beta1) : ss[mb][1];
+        ss[mb][2] = mine ? fmaf(s[mb][2], kTwo24, -beta0) : ss[mb][2];
+        ss[mb][3] = mine ? fmaf(s[mb][3], kTwo24, -beta1) : ss[mb][3];
       }
     }
     // ---- online softmax (base 2) over the 32 tokens of each column ----------
@@ -360,11 +372,31 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
-    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-    const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = fast_exp2(st.m0 - ms0), a1 = fast_exp2(st.m1 - ms1);
-    st.m0 = mn0;
-    st.m1 = mn1;
+    // Lazy rescaling: the reference max m moves only when a score exceeds it
+    // by more than kSlack (weights then stay below 2^kSlack, well inside f16);
+    // l and O always share the same m, so the final o = O / l is exact.
+    constexpr float kSlack = 8.f;
+    if (__any_sync(0xffffffffu, mx0 > st.m0 + kSlack || mx1 > st.m1 + kSlack)) {
+      const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
+      const float a0 = st.m0 == -INFINITY ? 0.f : fast_exp2(st.m0 - mn0);
+      const float a1 = st.m1 == -INFINITY ? 0.f : fast_exp2(st.m1 - mn1);
+      st.m0 = mn0;
+      st.m1 = mn1;
+      st.l0 *= a0;
+      st.l1 *= a1;
+#pragma unroll
+      for (int mt = 0; mt < S::kSteps; ++mt) {
+        st.O[mt][0] *= a0;
+        st.O[mt][1] *= a1;
+        st.O[mt][2] *= a0;
+        st.O[mt][3] *= a1;
+      }
+      st.C[0] *= a0;
+      st.C[1] *= a1;
+      st.C[2] *= a0;
+      st.C[3] *= a1;
+    }
+    const float ms0 = st.m0 == -INFINITY ? 0.f : st.m0, ms1 = st.m1 == -INFINITY ? 0.f : st.m1;
     float pr[2][4];
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
@@ -373,48 +405,30 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       pr[mb][2] = fast_exp2(ss[mb][2] - ms0);
       pr[mb][3] = fast_exp2(ss[mb][3] - ms1);
     }
-    st.l0 = fmaf(st.l0, a0, (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]));
-    st.l1 = fmaf(st.l1, a1, (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]));
-    if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
-#pragma unroll
-      for (int mt = 0; mt < S::kSteps; ++mt) {
-        st.O[mt][0] *= a0;
-        st.O[mt][1] *= a1;
-        st.O[mt][2] *= a0;
-        st.O[mt][3] *= a1;
-      }
-    }
-    // ---- p / sV (Value scale of this thread's stream page) ------------------
+    st.l0 += (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]);
+    st.l1 += (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]);
+    // ---- p / sV (Value scale of this thread's stream page), f16 -------------
     const float* vscale = reinterpret_cast<const float*>(vpg + geom.vscale_off) + sub * 32;
     uint32_t pk[2][2];
-    float psum0 = 0.f, psum1 = 0.f;
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
       const int r0 = token_row0<BITS>(gid, mb);
-      const float i0 = fast_rcp(vscale[r0]), i1 = fast_rcp(vscale[r0 + kGap]);
-      const float p00 = pr[mb][0] * i0, p01 = pr[mb][1] * i0, p10 = pr[mb][2] * i1, p11 = pr[mb][3] * i1;
-      const float f = BITS == 4 ? 0.0625f : 1.f;  // rows fed by the x16 registers
-      pk[mb][0] = pack_f16x2(p00, p01);
-      pk[mb][1] = pack_f16x2(p10 * f, p11 * f);
-      // the bias correction must subtract exactly what the MMA adds: sum the
-      // f16-rounded values
-      const float2 r0v = __half22float2(*reinterpret_cast<const __half2*>(&pk[mb][0]));
-      const float2 r1v = __half22float2(*reinterpret_cast<const __half2*>(&pk[mb][1]));
-      psum0 += r0v.x + r1v.x * (1.f / f);
-      psum1 += r0v.y + r1v.y * (1.f / f);
+      const float i0 = fast_rcp(vscale[r0]);
+      const float i1 = fast_rcp(vscale[r0 + kGap]) * (BITS == 4 ? 0.0625f : 1.f);  // x16 rows
+      pk[mb][0] = pack_f16x2(pr[mb][0] * i0, pr[mb][1] * i0);
+      pk[mb][1] = pack_f16x2(pr[mb][2] * i1, pr[mb][3] * i1);
     }
-    st.q0 = fmaf(st.q0, a0, psum0);
-    st.q1 = fmaf(st.q1, a1, psum1);
     // ---- O'^T += V'^T P' for every page, P' masked to the page's columns ------
 #pragma unroll
     for (int j = 0; j < S::PB; ++j) {
-      if (j >= npages) break;
+      if (!FULL && j >= npages) break;
       const bool mine = sj == j;
       uint32_t bp[2][2];
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
         bp[mb][0] = transpose8x8(mine ? pk[mb][0] : 0u);
         bp[mb][1] = transpose8x8(mine ? pk[mb][1] : 0u);
+        mma16816(st.C, kOneLo, kOneLo, kOneHi, kOneHi, bp[mb][0], bp[mb][1]);
       }
       const uint8_t* vc = pg[j] + geom.code_bytes + sub * S::kSubBytes;
 #pragma unroll
@@ -576,7 +590,7 @@ __device__ __forceinline__ void merge_streams(WarpState<D>& st, int off) {
 }
 
 template <int D, int BITS, int GP>
-__global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodeParams p, int slots) {
+__global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const DecodeParams p, int slots) {
   using S = Shape<D, BITS, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int u = blockIdx.y;
@@ -594,15 +608,17 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* scratch = reinterpret_cast<float*>(smem + 128 * ((kMmaWarps * slots * 8 + 127) / 128));
   float* my_rsc = scratch + warp * S::PB * D;
-  uint8_t* buf = reinterpret_cast<uint8_t*>(scratch + kMmaWarps * S::PB * D);
+  float4* q4 = reinterpret_cast<float4*>(scratch + kMmaWarps * S::PB * D);  // GP * D floats
+  uint8_t* buf = reinterpret_cast<uint8_t*>(scratch + kMmaWarps * S::PB * D + GP * D);
   uint8_t* my_buf = buf + (size_t)warp * slots * page_bytes;
   const uint32_t my_bar = smem_addr(bars + warp * slots);
 
   WarpState<D> st;
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
+  st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
   st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = st.q0 = st.q1 = 0.f;
+  st.l0 = st.l1 = 0.f;
   bool ok = true;
 
   if (win) {
@@ -613,25 +629,18 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
       st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
     }
   } else {
-  // query slice of head (gid % GP) -- a real head of this KV head even for the
-  // padding columns, so every value stays finite -- channels tig*D/4 .., pre-scaled
-  float qreg[S::kChan];
-  {
-    const int hq = (gid % GP) % g;
-    const __nv_bfloat16* q =
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g + hq) * D + tig * S::kChan;
-#pragma unroll
-    for (int c = 0; c < S::kChan; c += 8) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(q + c);
-      const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(v[e]);
-        qreg[c + 2 * e] = f.x * p.qk_scale;
-        qreg[c + 2 * e + 1] = f.y * p.qk_scale;
-      }
-    }
+  // queries of the GP column heads (head n % g for the padding columns, so every
+  // value stays finite), pre-scaled, in shared memory: channel c of head n goes
+  // to float4 ((i * GP + n) * 4 + tig) with tig = c / (D/4), i = (c % (D/4)) / 4,
+  // so the lanes that read together hit distinct banks
+  for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) {
+    const int n = idx / D, c = idx - n * D;
+    const __nv_bfloat16* qrow =
+        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D;
+    const int tg = c / S::kChan, i4 = (c - tg * S::kChan) >> 2;
+    reinterpret_cast<float*>(q4)[((i4 * GP + n) * 4 + tg) * 4 + (c & 3)] = __bfloat162float(qrow[c]) * p.qk_scale;
   }
+  __syncthreads();
 
   const uint8_t* unit_pages = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride;
   const int npg = pg1 - pg0;
@@ -648,37 +657,68 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
   }
   __syncwarp();
 
-  int k = 0;
+  // Pages are consumed in issue order; page k sits in slot k mod slots, and
+  // bit t of ``phases`` is the parity slot t's barrier completes next.  Every
+  // lane keeps the same counters; lane 0 issues the copies.
+  int k = 0, sidx = 0, consumed = 0, issued = slots < my_n ? slots : my_n;
+  uint32_t phases = 0;
+  const uint8_t* next_src = unit_pages + (int64_t)(pg0 + warp + issued * kMmaWarps) * page_bytes;
   for (; k < my_n; k += S::PB) {
     const int np = min(S::PB, my_n - k);
+    int sl[S::PB];
     const uint8_t* pgs[S::PB];
 #pragma unroll
-    for (int j = 0; j < S::PB; ++j) pgs[j] = my_buf + (size_t)((k + min(j, np - 1)) % slots) * page_bytes;
-    for (int j = 0; j < np && ok; ++j)
-      ok = mbar_wait(my_bar + 8 * ((k + j) % slots), (uint32_t)(((k + j) / slots) & 1));
-    if (!ok) break;
-    mma_group<D, BITS, GP>(pgs, np, geom, p.G, qreg, my_rsc, lane, gid, tig, st);
-    __syncwarp();
-    if (lane == 0) {
-      fence_proxy_async();
-      for (int j = 0; j < np; ++j) {
-        const int kk = k + j;
-        if (kk + slots < my_n) {
-          mbar_expect_tx(my_bar + 8 * (kk % slots), page_bytes);
-          bulk_load(smem_addr(my_buf + (size_t)(kk % slots) * page_bytes),
-                    unit_pages + (int64_t)(pg0 + warp + (kk + slots) * kMmaWarps) * page_bytes, page_bytes,
-                    my_bar + 8 * (kk % slots));
+    for (int j = 0; j < S::PB; ++j) {
+      int t = sidx + (j < np ? j : np - 1);
+      if (t >= slots) t -= slots;
+      sl[j] = t;
+      pgs[j] = my_buf + (size_t)t * page_bytes;
+    }
+#pragma unroll
+    for (int j = 0; j < S::PB; ++j) {
+      if (j < np && ok) {
+        ok = mbar_wait(my_bar + 8 * sl[j], (phases >> sl[j]) & 1u);
+        if (ok) {
+          phases ^= 1u << sl[j];
+          ++consumed;
         }
       }
     }
+    if (!ok) break;
+    if (np == S::PB)
+      mma_group<D, BITS, GP, true>(pgs, np, geom, p.G, q4, my_rsc, lane, gid, tig, st);
+    else
+      mma_group<D, BITS, GP, false>(pgs, np, geom, p.G, q4, my_rsc, lane, gid, tig, st);
+    __syncwarp();
+    // refill the freed slots with the next pages of this warp's run
+    const int refill = min(np, my_n - issued);
+    if (lane == 0 && refill > 0) {
+      fence_proxy_async();
+#pragma unroll
+      for (int j = 0; j < S::PB; ++j) {
+        if (j < refill) {
+          mbar_expect_tx(my_bar + 8 * sl[j], page_bytes);
+          bulk_load(smem_addr(my_buf + (size_t)sl[j] * page_bytes),
+                    next_src + (int64_t)j * kMmaWarps * page_bytes, page_bytes, my_bar + 8 * sl[j]);
+        }
+      }
+    }
+    next_src += (int64_t)refill * kMmaWarps * page_bytes;
+    issued += refill;
+    sidx += np;
+    if (sidx >= slots) sidx -= slots;
   }
   if (!ok) {
     // drain the copies still in flight (bounded), report, and contribute nothing
-    const int issued = min(my_n, k + slots);
-    for (int kk = k; kk < issued; ++kk) mbar_wait(my_bar + 8 * (kk % slots), (uint32_t)((kk / slots) & 1));
+    for (int kk = consumed; kk < issued; ++kk) {
+      const int t = kk % slots;
+      mbar_wait(my_bar + 8 * t, (phases >> t) & 1u);
+      phases ^= 1u << t;
+    }
     if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
     st.m0 = st.m1 = -INFINITY;
-    st.l0 = st.l1 = st.q0 = st.q1 = 0.f;
+    st.l0 = st.l1 = 0.f;
+    st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
   }
@@ -687,12 +727,12 @@ __global__ void __launch_bounds__(kMmaThreads) decode_mma_kernel(const DecodePar
   for (int off = 4; off < 32; off <<= 1) {
     st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
     st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
-    st.q0 += __shfl_xor_sync(0xffffffffu, st.q0, off);
-    st.q1 += __shfl_xor_sync(0xffffffffu, st.q1, off);
   }
   {
+    // C holds 2^-24 * sum of p/sV per column (every row of the counter MMA
+    // carries the full sum), so the bias term is bias * 2^24 * C
     constexpr float kTwo24 = 16777216.f;
-    const float c0 = S::kBias * st.q0, c1 = S::kBias * st.q1;
+    const float c0 = S::kBias * kTwo24 * st.C[0], c1 = S::kBias * kTwo24 * st.C[1];
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       st.O[mt][0] = fmaf(st.O[mt][0], kTwo24, -c0);
@@ -782,7 +822,7 @@ size_t smem_for(const DecodeParams& p) {
   const size_t window = (size_t)kMmaWarps * 32 * D * 2;  // per warp 16 K rows + 16 V rows of bf16
   if (pages < merge) pages = merge;
   if (pages < window) pages = window;
-  const size_t scratch = (size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D * sizeof(float);
+  const size_t scratch = ((size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D + (size_t)gqa_pad(p.g) * D) * sizeof(float);
   return 128 * ((kMmaWarps * slots * 8 + 127) / 128) + scratch + pages;
 }
 

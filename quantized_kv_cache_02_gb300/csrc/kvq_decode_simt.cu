@@ -35,49 +35,47 @@ cudaError_t launch_bits(const DecodeParams& p, cudaStream_t s) {
 
 constexpr int kCombineThreads = 128;
 
+// Merge of the split partials (o[D], m, l) of one (sequence, query head):
+// M = max m_s, L = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M) / L
+// ("KV Cache 与自回归视频生成" section 05, FlashDecoding).  One CTA per
+// (sequence, query head), one thread per channel; the slot loops are unrolled
+// so their loads overlap.  A sequence without tokens gets zeros.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
   const int i = blockIdx.x / p.Hq;
   const int hq = blockIdx.x - i * p.Hq;
   const int b = p.seq_begin + i;
   const int h = hq / p.g, j = hq - h * p.g;
   const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-  const int P = Q0 / p.G;
-  const int nsplit = (P + p.chunk_pages - 1) / p.chunk_pages;
-  const bool has_win = T0 > Q0;
+  const int nsplit = (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
+  const int nslots = nsplit + (T0 > Q0 ? 1 : 0);
   const int D = p.D;
   const int64_t unit = (int64_t)b * p.Hkv + h;
   const float* base = p.partials + unit * p.max_splits * (int64_t)p.g * (D + 2) + (int64_t)j * (D + 2);
   const int64_t stride = (int64_t)p.g * (D + 2);
-  float* out = p.out + ((int64_t)b * p.Hq + hq) * D;
-
+  auto row = [&](int k) { return base + (k < nsplit ? k : p.max_splits - 1) * stride; };
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, base[s * stride + D]);
-  if (has_win) M = fmaxf(M, base[(p.max_splits - 1) * stride + D]);
+#pragma unroll 4
+  for (int k = 0; k < nslots; ++k) M = fmaxf(M, row(k)[D]);
+  const float Ms = M == -INFINITY ? 0.f : M;
   float L = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const float ms = base[s * stride + D];
-      if (ms != -INFINITY) L = fmaf(base[s * stride + D + 1], exp2f(ms - M), L);
-    }
-    if (has_win) {
-      const float ms = base[(p.max_splits - 1) * stride + D];
-      if (ms != -INFINITY) L = fmaf(base[(p.max_splits - 1) * stride + D + 1], exp2f(ms - M), L);
+  float o[2] = {0.f, 0.f};
+#pragma unroll 4
+  for (int k = 0; k < nslots; ++k) {
+    const float* r = row(k);
+    const float f = exp2f(r[D] - Ms);
+    L = fmaf(r[D + 1], f, L);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int c = threadIdx.x + e * kCombineThreads;
+      if (c < D) o[e] = fmaf(r[c], f, o[e]);
     }
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float o = 0.f;
-    if (M != -INFINITY) {
-      for (int s = 0; s < nsplit; ++s) {
-        const float ms = base[s * stride + D];
-        if (ms != -INFINITY) o = fmaf(base[s * stride + c], exp2f(ms - M), o);
-      }
-      if (has_win) {
-        const float ms = base[(p.max_splits - 1) * stride + D];
-        if (ms != -INFINITY) o = fmaf(base[(p.max_splits - 1) * stride + c], exp2f(ms - M), o);
-      }
-    }
-    out[c] = o * inv;
+  float* out = p.out + ((int64_t)b * p.Hq + hq) * D;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int c = threadIdx.x + e * kCombineThreads;
+    if (c < D) out[c] = o[e] * inv;
   }
 }
 

@@ -170,6 +170,9 @@ void plan_splits(const kvq_cache* c, int s0, int n, int requested, int* chunk, i
   }
   ch = std::max<int64_t>(ch, (pmax + c->max_splits - 2) / std::max(1, c->max_splits - 1));
   ch = std::max<int64_t>(ch, 1);
+  // whole page groups for each of the tensor-core kernel's 4 warps (8 pages =
+  // 4 warps x 2 pages at g = 4): every warp of a CTA gets the same work
+  if (requested <= 0 && ch > 8) ch = (ch + 7) / 8 * 8;
   *chunk = (int)ch;
   *grid_splits = (int)((pmax + ch - 1) / ch);
 }
@@ -646,8 +649,8 @@ kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, con
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_fail(e, "kvq_export_unit");
 
-  auto sext = [bits](uint32_t v) -> int8_t {
-    return bits == 4 ? (int8_t)(((int)(v & 0xF) ^ 8) - 8) : (int8_t)(v & 0xFF);
+  auto sext = [bits](uint32_t v) -> int8_t {  // offset binary -> signed code
+    return bits == 4 ? (int8_t)((int)(v & 0xF) - 8) : (int8_t)((int)(v & 0xFF) - 128);
   };
   for (int64_t pg = 0; pg < P; ++pg) {
     const uint8_t* page = pages.data() + pg * c->geom.page_bytes;

@@ -20,15 +20,16 @@ constexpr int kSimtWarps = kSimtThreads / 32;
 __device__ __forceinline__ float ld_f32(const float* p, int64_t i) { return p[i]; }
 __device__ __forceinline__ float ld_f32(const __nv_bfloat16* p, int64_t i) { return __bfloat162float(p[i]); }
 
-// Signed code of channel c of token tl (group-local) of a page.
+// Signed code of channel c of token tl (group-local) of a page (stored as
+// offset binary: code + 8 per nibble, code + 128 per byte).
 template <int BITS>
 __device__ __forceinline__ int key_code(const uint8_t* page, int tl, int c, int D) {
   if (BITS == 4) {
     const uint8_t byte = page[(int64_t)tl * (D / 2) + (c >> 1)];
     const int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
-    return (nib ^ 8) - 8;
+    return nib - 8;
   } else {
-    return (int)(int8_t)page[(int64_t)tl * D + c];
+    return (int)page[(int64_t)tl * D + c] - 128;
   }
 }
 
@@ -42,9 +43,9 @@ __device__ __forceinline__ int value_code(const uint8_t* vbase, int G, int tl, i
     const int jn = (k >> 1) + 4 * (k & 1);  // nibble that holds token offset k
     const uint32_t word = reinterpret_cast<const uint32_t*>(sub)[c * (n_st / 8) + w];
     const int nib = (word >> (4 * jn)) & 0xF;
-    return (nib ^ 8) - 8;
+    return nib - 8;
   } else {
-    return (int)(int8_t)sub[c * n_st + o];
+    return (int)sub[c * n_st + o] - 128;
   }
 }
 
@@ -85,7 +86,7 @@ __host__ __device__ constexpr int simt_scratch_floats() {
 // pages [pg0, pg1) of the quantized prefix.
 
 template <typename T, int BITS, int CPL>
-__device__ void simt_item(const DecodeParams& p, int i, int h, bool win, int pg0, int pg1, int slot,
+__device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, int pg0, int pg1, int slot,
                           float* scratch) {
   float (*qs)[CPL * 32] = reinterpret_cast<float (*)[CPL * 32]>(scratch);
   float (*wm)[kMaxGqa] = reinterpret_cast<float (*)[kMaxGqa]>(scratch + kMaxGqa * CPL * 32);

@@ -404,17 +404,18 @@ def test_current_token_is_attended():
 # --------------------------------------------------------------------------
 
 def test_layout_key_nibbles():
+    # offset binary: nibble = code + 8, byte = code + 128
     codes = np.int8([[1, -1, -7, 7]])
-    assert L.pack_key_codes(codes, 4) == bytes([0xF1, 0x79])
-    assert L.pack_key_codes(codes, 8) == bytes([0x01, 0xFF, 0xF9, 0x07])
+    assert L.pack_key_codes(codes, 4) == bytes([0x79, 0xF1])
+    assert L.pack_key_codes(codes, 8) == bytes([0x81, 0x7F, 0x79, 0x87])
 
 
 def test_layout_value_word_order():
     codes = np.arange(8, dtype=np.int8).reshape(8, 1)          # tokens 0..7 of one channel
-    # nibbles hold tokens 0,2,4,6,1,3,5,7 -> word 0x75316420
-    assert L.pack_value_codes(codes, 4) == (0x75316420).to_bytes(4, "little")
+    # nibbles hold tokens 0,2,4,6,1,3,5,7, each code + 8 -> word 0xFDB9ECA8
+    assert L.pack_value_codes(codes, 4) == (0xFDB9ECA8).to_bytes(4, "little")
     codes2 = np.arange(64, dtype=np.int8).reshape(32, 2) - 32   # 32 tokens x 2 channels
     out = L.pack_value_codes(codes2, 8)
-    assert out[:32] == bytes((int(c) & 0xFF) for c in codes2[:, 0])
-    assert out[32:] == bytes((int(c) & 0xFF) for c in codes2[:, 1])
+    assert out[:32] == bytes((int(c) + 128) for c in codes2[:, 0])
+    assert out[32:] == bytes((int(c) + 128) for c in codes2[:, 1])
     assert len(L.pack_group_page(codes2, codes2, np.ones(2), np.ones(32), 8)) == L.page_bytes(32, 2, 8)
