@@ -177,7 +177,7 @@ def host_cpu_name():
     return "unknown"
 
 
-def cpu_baseline(steps=60, warmup=1):
+def cpu_baseline(steps=250, warmup=1):
     units = [(0, 0)]
     gbs, res = run_oracle_sample(units, steps, warmup)
     return {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

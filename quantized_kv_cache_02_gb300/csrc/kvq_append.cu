@@ -133,12 +133,19 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
     uint32_t* kc = reinterpret_cast<uint32_t*>(page);
     for (int idx = threadIdx.x; idx < G * words_per_row; idx += blockDim.x) {
       const int t = idx / words_per_row, w = idx - t * words_per_row;
+      // the word's channels as float4 reads (consecutive threads, consecutive addresses)
+      const float4* src = reinterpret_cast<const float4*>(tile + t * D + w * kPerWord);
+      const float4* sc = reinterpret_cast<const float4*>(sK + w * kPerWord);
       uint32_t word = 0;
 #pragma unroll
-      for (int k = 0; k < kPerWord; ++k) {
-        const int c = w * kPerWord + k;
-        const int code = quantize_one(tile[t * D + c], sK[c], qmax);
-        word |= ((uint32_t)(code + kBias)) << (BITS * k);
+      for (int k4 = 0; k4 < kPerWord / 4; ++k4) {
+        const float4 x = src[k4], s4 = sc[k4];
+        const int c0 = quantize_one(x.x, s4.x, qmax), c1 = quantize_one(x.y, s4.y, qmax);
+        const int c2 = quantize_one(x.z, s4.z, qmax), c3 = quantize_one(x.w, s4.w, qmax);
+        word |= ((uint32_t)(c0 + kBias)) << (BITS * (4 * k4 + 0));
+        word |= ((uint32_t)(c1 + kBias)) << (BITS * (4 * k4 + 1));
+        word |= ((uint32_t)(c2 + kBias)) << (BITS * (4 * k4 + 2));
+        word |= ((uint32_t)(c3 + kBias)) << (BITS * (4 * k4 + 3));
       }
       kc[idx] = word;
     }
@@ -166,8 +173,9 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
       uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
       if (BITS == 4) {
         const int nw = n_st / 8;  // words per channel row
+        // channel fastest across threads: each token row is read at consecutive addresses
         for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
-          const int c = idx / nw, w = idx - c * nw;
+          const int w = idx / D, c = idx - w * D;
           uint32_t word = 0;
 #pragma unroll
           for (int jn = 0; jn < 8; ++jn) {
@@ -175,12 +183,12 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
             const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
             word |= ((uint32_t)(code + kBias)) << (4 * jn);
           }
-          vc[idx] = word;
+          vc[c * nw + w] = word;
         }
       } else {
         const int nw = n_st / 4;
         for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
-          const int c = idx / nw, w = idx - c * nw;
+          const int w = idx / D, c = idx - w * D;
           uint32_t word = 0;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
             const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
             word |= ((uint32_t)(code + kBias)) << (8 * k);
           }
-          vc[idx] = word;
+          vc[c * nw + w] = word;
         }
       }
     }
