@@ -216,6 +216,7 @@ def run_ours(args):
 
     import quantized_kv_cache_02_gb300 as kvq
     from kvq_inputs.device import DeviceInputs
+    from quantized_kv_cache_02_gb300.shard import job_totals, shard_range
     from kvq_inputs.gen import InputSpec
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -229,17 +230,20 @@ def run_ours(args):
     if args.layers:
         w["layers"] = args.layers
         w["name"] = f"{w['name']}_layers{args.layers}"
-    L, B, H, Hq, D = w["layers"], w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"]
+    L, H, Hq, D = w["layers"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"]
     K, W = args.steps, args.warmup
-    # each rank runs its own batch of sequences (weak scaling): seeds differ by rank
-    spec = InputSpec(seed=w["seed"] + 1000 * rank, n_kv_heads=H, n_q_heads=Hq, head_dim=D)
+    # weak scaling: the global batch grows with the ranks, each rank owns a
+    # contiguous shard of it (inputs drawn by global sequence index)
+    shard = shard_range(w["batch"] * world, world, rank)
+    B, s0 = shard.count, shard.begin
+    spec = InputSpec(seed=w["seed"], n_kv_heads=H, n_q_heads=Hq, head_dim=D)
     dev = DeviceInputs(spec)
     T0 = w["context"] - W - K // 2        # midpoint of the timed steps at `context`
     n_e2e = K
     cap = T0 + W + K + n_e2e + 8
     caches = [kvq.KVQCache(B, H, Hq, D, w["residual_len"], w["group"], w["qmax"], cap) for _ in range(L)]
     for l, c in enumerate(caches):
-        Kp, Vp = dev.kv_block(l, 0, B, 0, T0)
+        Kp, Vp = dev.kv_block(l, s0, B, 0, T0)
         c.append(Kp, Vp, 0)
         del Kp, Vp
     torch.cuda.synchronize()
@@ -248,14 +252,14 @@ def run_ours(args):
     steps_total = W + K
     new_k, new_v, qs = [], [], []
     for l in range(L):
-        Kn, Vn = dev.kv_block(l, 0, B, T0, steps_total)
+        Kn, Vn = dev.kv_block(l, s0, B, T0, steps_total)
         new_k.append([Kn[:, :, s:s + 1].contiguous() for s in range(steps_total)])
         new_v.append([Vn[:, :, s:s + 1].contiguous() for s in range(steps_total)])
-        qs.append([dev.q_block(l, 0, B, s) for s in range(steps_total)])
+        qs.append([dev.q_block(l, s0, B, s) for s in range(steps_total)])
         del Kn, Vn
     outs = [torch.empty(B, Hq, D, dtype=torch.float32, device="cuda") for _ in range(L)]
     stream = torch.cuda.current_stream()
-    ev_pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L * K)]
+    ev_pool = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     for e0, e1 in ev_pool:  # torch creates the CUDA event on first record
         e0.record(stream)
         e1.record(stream)
@@ -267,10 +271,14 @@ def run_ours(args):
     def one_step(s, timed_index=None):
         for l in range(L):
             caches[l].append(new_k[l][s], new_v[l][s], 0)
-            if timed_index is None:
+            # the split kernel of one layer per timed step is bracketed by events
+            # (layer = step mod L): an event between two launches stops the next
+            # one from starting while the previous drains, so the other layers run
+            # without them
+            if timed_index is None or l != timed_index % L:
                 caches[l].decode_attention(qs[l][s], out=outs[l])
             else:
-                e0, e1 = ev_pool[timed_index * L + l]
+                e0, e1 = ev_pool[timed_index]
                 caches[l].decode_attention(qs[l][s], out=outs[l], split_start=e0.cuda_event, split_stop=e1.cuda_event)
 
     for s in range(W):
@@ -318,19 +326,30 @@ def run_ours(args):
     assert Qsim == counters()[0], "host byte model out of step with the cache counters"
 
     # ---- end to end through the C ABI with host buffers ----------------------
+    # Each step's inputs (K, V, q of every layer) sit in one pinned host buffer
+    # and go up in one copy; the step's outputs come back in one copy.  Copies
+    # run on their own streams, double-buffered, so step s + 1's upload and
+    # step s - 1's download overlap step s's kernels.
     n_ring = min(8, steps_total)
-    pin_k = [torch.empty(B, H, 1, D, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring * L)]
-    pin_v = [torch.empty(B, H, 1, D, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring * L)]
-    pin_q = [torch.empty(B, Hq, D, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring * L)]
-    for i in range(n_ring * L):
-        l, s = i % L, i // L
-        pin_k[i].copy_(new_k[l][s])
-        pin_v[i].copy_(new_v[l][s])
-        pin_q[i].copy_(qs[l][s])
-    host_out = [torch.empty(B, Hq, D, dtype=torch.float32).pin_memory() for _ in range(L)]
-    dk = [torch.empty(B, H, 1, D, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
-    dv = [torch.empty(B, H, 1, D, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
-    dq = [torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    kv_el, q_el = B * H * D, B * Hq * D
+    per_layer = 2 * kv_el + q_el
+    pin_in = [torch.empty(L * per_layer, dtype=torch.bfloat16).pin_memory() for _ in range(n_ring)]
+    for r in range(n_ring):
+        for l in range(L):
+            o = l * per_layer
+            pin_in[r][o:o + kv_el].copy_(new_k[l][r].reshape(-1))
+            pin_in[r][o + kv_el:o + 2 * kv_el].copy_(new_v[l][r].reshape(-1))
+            pin_in[r][o + 2 * kv_el:o + per_layer].copy_(qs[l][r].reshape(-1))
+    dev_in = [torch.empty(L * per_layer, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    dev_out = [torch.empty(L, B, Hq, D, dtype=torch.float32, device="cuda") for _ in range(2)]
+    host_out = [torch.empty(L, B, Hq, D, dtype=torch.float32).pin_memory() for _ in range(2)]
+    views = [[(dev_in[i][l * per_layer:l * per_layer + kv_el].view(B, H, 1, D),
+               dev_in[i][l * per_layer + kv_el:l * per_layer + 2 * kv_el].view(B, H, 1, D),
+               dev_in[i][l * per_layer + 2 * kv_el:(l + 1) * per_layer].view(B, Hq, D)) for l in range(L)]
+             for i in range(2)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    ev_in, ev_done, ev_host = [ev(), ev()], [ev(), ev()], [ev(), ev()]
     qb0, wb0 = counters()
     e2e_bytes = 0
     Qs2 = [row[:] for row in qb0]
@@ -349,35 +368,49 @@ def run_ours(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    up.wait_event(e0)
+    with torch.cuda.stream(up):
+        dev_in[0].copy_(pin_in[0], non_blocking=True)
+        ev_in[0].record(up)
     for s in range(n_e2e):
+        cur = s % 2
+        if s + 1 < n_e2e:
+            nxt = 1 - cur
+            if s >= 1:
+                up.wait_event(ev_done[nxt])        # step s - 1 has consumed dev_in[nxt]
+            with torch.cuda.stream(up):
+                dev_in[nxt].copy_(pin_in[(s + 1) % n_ring], non_blocking=True)
+                ev_in[nxt].record(up)
+        stream.wait_event(ev_in[cur])
+        if s >= 2:
+            stream.wait_event(ev_host[cur])        # step s - 2's download has left dev_out[cur]
         for l in range(L):
-            i = (s % n_ring) * L + l
-            dk[l].copy_(pin_k[i], non_blocking=True)
-            dv[l].copy_(pin_v[i], non_blocking=True)
-            dq[l].copy_(pin_q[i], non_blocking=True)
-            caches[l].append(dk[l], dv[l], 0)
-            caches[l].decode_attention(dq[l], out=outs[l])
-            host_out[l].copy_(outs[l], non_blocking=True)
+            k_l, v_l, q_l = views[cur][l]
+            caches[l].append(k_l, v_l, 0)
+            caches[l].decode_attention(q_l, out=dev_out[cur][l])
+        ev_done[cur].record(stream)
+        down.wait_event(ev_done[cur])
+        with torch.cuda.stream(down):
+            host_out[cur].copy_(dev_out[cur], non_blocking=True)
+            ev_host[cur].record(down)
+    stream.wait_event(ev_host[0])
+    stream.wait_event(ev_host[1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    h2d = L * (2 * B * H * D * 2 + B * Hq * D * 2)
-    d2h = L * B * Hq * D * 4
+    h2d, _ = job_totals(L * per_layer * 2, 0.0, dist if world > 1 else None, device="cuda")
+    h2d = int(h2d)
+    d2h, _ = job_totals(L * q_el * 4, 0.0, dist if world > 1 else None, device="cuda")
+    d2h = int(d2h)
     assert np.isfinite(host_out[0].numpy()).all()
 
-    # ---- reduce over ranks --------------------------------------------------
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return t.item()
-
-    ms_max = max_over_ranks(ms)
-    e2e_max = max_over_ranks(e2e_ms)
-    total_bytes = sum(step_b) * world
+    # ---- reduce over ranks: bytes summed, time of the slowest rank ----------
+    pg = dist if world > 1 else None
+    total_bytes, ms_max = job_totals(sum(step_b), ms, pg, device="cuda")
+    e2e_total, e2e_max = job_totals(e2e_bytes, e2e_ms, pg, device="cuda")
+    global_batch, _ = job_totals(B, 0.0, pg, device="cuda")
     value = total_bytes / (ms_max / 1e3) / 1e9
-    e2e_value = e2e_bytes * world / (e2e_max / 1e3) / 1e9
+    e2e_value = e2e_total / (e2e_max / 1e3) / 1e9
     split_avg_ms = sum(split_ms) / len(split_ms)
     achieved = (sum(split_b) / len(split_b)) / (split_avg_ms / 1e3) / 1e9
     peaks = {}
@@ -401,7 +434,7 @@ def run_ours(args):
         "warmup": W,
         "ms_per_step": round(ms_max / K, 5),
         "us_per_step": round(1e3 * ms_max / K, 2),
-        "tokens_per_s": round(world * B * K / (ms_max / 1e3), 1),
+        "tokens_per_s": round(global_batch * K / (ms_max / 1e3), 1),
         "frac_of_8TBs": round(value / world / 8000.0, 4),
         "frac_of_measured_hbm": round(value / world / peak, 4),
         "higher_is_better": True,
@@ -409,17 +442,18 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16 inputs, 4-bit codes, fp32 accumulate",
         "data": "synthetic (seeded: K channel outliers, V per-token scales)",
-        "config": {"workload": w["name"], "layers": L, "global_batch": B * world, "seq_len": w["context"],
+        "config": {"workload": w["name"], "layers": L, "global_batch": int(global_batch), "seq_len": w["context"],
                    "context_mean_timed": T0 + W + (K - 1) / 2 + 1, "n_kv_heads": H, "n_q_heads": Hq,
                    "head_dim": D, "residual_len": w["residual_len"], "group": w["group"], "qmax": w["qmax"],
-                   "parallelism": f"replicas x{world} (independent sequences, no collective)",
+                   "parallelism": f"dp{world} (global batch sharded by sequence, no collective on the data path)",
                    "l2": "working set per step ~10 GB >> 129 MB L2 (no flush needed)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": load_traffic(),
                      "kernel": "decode_mma_kernel<128,4> (split, one layer per launch)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": round(sum(split_b) / len(split_b)),
-                     "avg_launch_ms": round(split_avg_ms, 5)},
+                     "avg_launch_ms": round(split_avg_ms, 5),
+                     "timed_launches": len(split_ms)},
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_max / n_e2e, 5),

@@ -69,6 +69,8 @@ __device__ void load_group(float* tile, const T* ring, const T* input, int t_fir
 template <typename T, int BITS>
 __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
   extern __shared__ float smem[];
+  pdl_wait();
+  pdl_release();
   const int i = blockIdx.y;
   const int h = blockIdx.z;
   const int b = p.seq_begin + i;
@@ -209,8 +211,7 @@ template <typename T, int BITS>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
   const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
   const size_t smem = p.flush_blocks ? ((size_t)p.G * p.D + p.D + p.G) * sizeof(float) : 0;
-  append_kernel<T, BITS><<<grid, kAppendThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel<T, BITS>, grid, dim3(kAppendThreads), smem, s, p);
 }
 
 template <typename T, int BITS>

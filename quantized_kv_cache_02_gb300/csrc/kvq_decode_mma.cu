@@ -14,10 +14,10 @@
 // which is q.k/sqrt(d) and p.v over restored values k = code/sK, v = code/sV
 // ("KV Cache Quantization Strategies", restore; "KV Cache 与自回归视频生成"
 // 3.1 and attn_step) with both scales folded into the f16 MMA operand that
-// is not the code (q/sK as an f16 hi + lo pair, p/sV as one f16).  Codes are
-// exact small integers in f16; the nibble to f16 conversion writes the biased
-// nibble into the mantissa of 1024.0 and subtracts 1032.0 (IEEE binary16:
-// 0x6400 | u == 1024 + u for u < 1024).
+// is not the code (q/sK as an f16 hi + lo pair, p/sV as one f16).  Codes
+// enter the MMA as f16 subnormals cut straight out of the stored word (see
+// "codes as f16 subnormals" below); the bias and the 2^-24 are undone once per
+// page for S and once per run for O.
 // Matrix shapes: S = A(K codes: 16 tokens x 16 channels) * B(q: 16 x 8 heads),
 // O^T = A(V codes^T: 16 channels x 16 tokens) * B(P^T: 16 tokens x 8 heads);
 // P goes from the S accumulator layout to the B layout with movmatrix.trans.
@@ -320,13 +320,16 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       if (!FULL && j >= npages) break;
       const uint8_t* kc = pg[j] + sub * 32 * S::kRowBytes;
       uint32_t wa[2][S::kWords], wb[2][S::kWords];
-      float s[2][4];
+      // hi and lo halves of q accumulate separately: two dependent MMA chains
+      // of half the length, summed once per sub-tile
+      float s[2][4], s2[2][4];
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
         const int r0 = token_row0<BITS>(gid, mb);
         lds_words<S::kWords>(kc + r0 * S::kRowBytes + tig * (S::kRowBytes / 4), wa[mb]);
         lds_words<S::kWords>(kc + (r0 + kGap) * S::kRowBytes + tig * (S::kRowBytes / 4), wb[mb]);
         s[mb][0] = s[mb][1] = s[mb][2] = s[mb][3] = 0.f;
+        s2[mb][0] = s2[mb][1] = s2[mb][2] = s2[mb][3] = 0.f;
       }
       if (BITS == 4) {
 #pragma unroll
@@ -337,11 +340,15 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
             nibble_regs(wa[mb][i], ra);
             nibble_regs(wb[mb][i], rb);
             mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bh[2 * i][0], bh[2 * i][1]);
-            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bl[2 * i][0], bl[2 * i][1]);
+            mma16816(s2[mb], ra[0], rb[0], ra[1], rb[1], bl[2 * i][0], bl[2 * i][1]);
             mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bh[2 * i + 1][0], bh[2 * i + 1][1]);
-            mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bl[2 * i + 1][0], bl[2 * i + 1][1]);
+            mma16816(s2[mb], ra[2], rb[2], ra[3], rb[3], bl[2 * i + 1][0], bl[2 * i + 1][1]);
           }
         }
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[mb][e] += s2[mb][e];
       } else {
 #pragma unroll
         for (int kk = 0; kk < S::kWords; ++kk) {
@@ -593,6 +600,8 @@ template <int D, int BITS, int GP>
 __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const DecodeParams p, int slots) {
   using S = Shape<D, BITS, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();
+  pdl_release();
   const int u = blockIdx.y;
   const int i = u / p.Hkv, h = u - i * p.Hkv;
   bool win;
@@ -840,8 +849,8 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
     configured[dev] = smem;
   }
   const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
-  decode_mma_kernel<D, BITS, GP><<<grid, kMmaThreads, smem, s>>>(p, mma_slots(p.geom.page_bytes, p.g));
-  return cudaGetLastError();
+  return launch_pdl(decode_mma_kernel<D, BITS, GP>, grid, dim3(kMmaThreads), smem, s, p,
+                    mma_slots(p.geom.page_bytes, p.g));
 }
 
 template <int D, int BITS>

@@ -13,6 +13,8 @@ namespace {
 
 template <typename T, int BITS, int CPL>
 __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const DecodeParams p) {
+  pdl_wait();
+  pdl_release();
   const int u = blockIdx.y;
   const int i = u / p.Hkv, h = u - i * p.Hkv;
   bool win;
@@ -26,11 +28,11 @@ template <typename T, int BITS>
 cudaError_t launch_bits(const DecodeParams& p, cudaStream_t s) {
   const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
   const int cpl = (p.D + 31) / 32;
-  if (cpl <= 1) decode_simt_kernel<T, BITS, 1><<<grid, kSimtThreads, 0, s>>>(p);
-  else if (cpl <= 2) decode_simt_kernel<T, BITS, 2><<<grid, kSimtThreads, 0, s>>>(p);
-  else if (cpl <= 4) decode_simt_kernel<T, BITS, 4><<<grid, kSimtThreads, 0, s>>>(p);
-  else decode_simt_kernel<T, BITS, 8><<<grid, kSimtThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  const dim3 block(kSimtThreads);
+  if (cpl <= 1) return launch_pdl(decode_simt_kernel<T, BITS, 1>, grid, block, 0, s, p);
+  if (cpl <= 2) return launch_pdl(decode_simt_kernel<T, BITS, 2>, grid, block, 0, s, p);
+  if (cpl <= 4) return launch_pdl(decode_simt_kernel<T, BITS, 4>, grid, block, 0, s, p);
+  return launch_pdl(decode_simt_kernel<T, BITS, 8>, grid, block, 0, s, p);
 }
 
 constexpr int kCombineThreads = 128;
@@ -41,6 +43,8 @@ constexpr int kCombineThreads = 128;
 // (sequence, query head), one thread per channel; the slot loops are unrolled
 // so their loads overlap.  A sequence without tokens gets zeros.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+  pdl_wait();
+  pdl_release();
   const int i = blockIdx.x / p.Hq;
   const int hq = blockIdx.x - i * p.Hq;
   const int b = p.seq_begin + i;
@@ -87,8 +91,7 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s)
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-  combine_kernel<<<p.n_seqs * p.Hq, kCombineThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(p.n_seqs * p.Hq), dim3(kCombineThreads), 0, s, p);
 }
 
 }  // namespace kvq

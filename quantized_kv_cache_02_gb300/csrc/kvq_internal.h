@@ -99,7 +99,31 @@ struct CombineParams {
   SeqCounters ctr[kMaxSeqsPerLaunch];
 };
 
-// Launchers (defined in the kernel translation units). Return cudaGetLastError().
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with the programmatic stream serialization attribute and begins with
+// pdl_wait(), which returns once the previous kernel in the stream has
+// finished and its writes are visible: stream order is kept, but the launch
+// and CTA start-up overlap the predecessor's last wave.  pdl_release() lets
+// the next kernel be scheduled once every CTA of this grid has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Launchers (defined in the kernel translation units). Return the launch's error code.
 cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s);
 cudaError_t configure_append(int dtype, int bits, size_t smem_bytes);
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s);
