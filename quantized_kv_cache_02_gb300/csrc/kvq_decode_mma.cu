@@ -372,18 +372,20 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       }
     }
     // ---- online softmax (base 2) over the 32 tokens of each column ----------
-    float mx0 = fmaxf(fmaxf(ss[0][0], ss[0][2]), fmaxf(ss[1][0], ss[1][2]));
-    float mx1 = fmaxf(fmaxf(ss[0][1], ss[0][3]), fmaxf(ss[1][1], ss[1][3]));
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
     // Lazy rescaling: the reference max m moves only when a score exceeds it
     // by more than kSlack (weights then stay below 2^kSlack, well inside f16);
-    // l and O always share the same m, so the final o = O / l is exact.
+    // l and O always share the same m, so the final o = O / l is exact.  Each
+    // lane tests its own scores; the column maxima are reduced across the
+    // warp only when some lane asks for a move.
     constexpr float kSlack = 8.f;
+    float mx0 = fmaxf(fmaxf(ss[0][0], ss[0][2]), fmaxf(ss[1][0], ss[1][2]));
+    float mx1 = fmaxf(fmaxf(ss[0][1], ss[0][3]), fmaxf(ss[1][1], ss[1][3]));
     if (__any_sync(0xffffffffu, mx0 > st.m0 + kSlack || mx1 > st.m1 + kSlack)) {
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+      }
       const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
       const float a0 = st.m0 == -INFINITY ? 0.f : fast_exp2(st.m0 - mn0);
       const float a1 = st.m1 == -INFINITY ? 0.f : fast_exp2(st.m1 - mn1);
@@ -602,11 +604,16 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   extern __shared__ __align__(128) uint8_t smem[];
   pdl_wait();
   pdl_release();
-  const int u = blockIdx.y;
+  // column-major over (split column, unit): every unit's first chunk, then
+  // every unit's second, ..., the windows last, so the last wave holds the
+  // shortest items
+  const int n_units = p.n_seqs * p.Hkv;
+  const int col = blockIdx.x / n_units;
+  const int u = blockIdx.x - col * n_units;
   const int i = u / p.Hkv, h = u - i * p.Hkv;
   bool win;
   int pg0, pg1, slot;
-  if (!split_item(p, blockIdx.x, i, &win, &pg0, &pg1, &slot)) return;
+  if (!split_item(p, col, i, &win, &pg0, &pg1, &slot)) return;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
@@ -848,7 +855,7 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
-  const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
+  const dim3 grid((p.grid_splits + 1) * p.n_seqs * p.Hkv);
   return launch_pdl(decode_mma_kernel<D, BITS, GP>, grid, dim3(kMmaThreads), smem, s, p,
                     mma_slots(p.geom.page_bytes, p.g));
 }
