@@ -209,6 +209,45 @@ def load_traffic():
     return t.get("dram_bytes_per_launch_full_size")
 
 
+def foil_layer(torch, cache, q, w, B, H, D, stream, iters=20):
+    """The read path the fused kernel replaces, on one layer's cache as it
+    stands: kvq_restore to dense bf16 tensors, then the dense bf16 decode
+    attention, against the fused decode (split + combine) of the same cache.
+    The restored tensors are > 1 GB, so every pass streams from HBM."""
+    tot = [cache.seq_state(b)["total"] for b in range(B)]
+    qn = [cache.seq_state(b)["quantized"] for b in range(B)]
+    G = w["group"]
+    stride = max(tot)
+    k = torch.empty(B, H, stride, D, dtype=torch.bfloat16, device="cuda")
+    v = torch.empty_like(k)
+    out = torch.empty(B, w["n_q_heads"], D, dtype=torch.float32, device="cuda")
+    page = 2 * G * D // 2 + 4 * D + 4 * G
+    restore_bytes = H * sum((qq // G) * page + (t - qq) * 2 * D * 2 + t * 2 * D * 2 for t, qq in zip(tot, qn))
+    dense_bytes = H * sum(t * 2 * D * 2 for t in tot) + B * w["n_q_heads"] * D * (2 + 4)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / iters
+
+    r_ms = timed(lambda: cache.restore(t_stride=stride, out_dtype="bf16", k_out=k, v_out=v))
+    d_ms = timed(lambda: cache.dense_decode_attention(k, v, q, out=out))
+    f_ms = timed(lambda: cache.decode_attention(q, out=out))
+    del k, v
+    return {"what": "dequantize-to-HBM read path on one layer: kvq_restore to dense bf16 + dense bf16 decode "
+                    "attention (kvq_dense_decode_attention), vs the fused decode (split + combine) on the same cache",
+            "restore_ms": round(r_ms, 5), "restore_gbs": round(restore_bytes / (r_ms / 1e3) / 1e9, 1),
+            "dense_attention_ms": round(d_ms, 5), "dense_attention_gbs": round(dense_bytes / (d_ms / 1e3) / 1e9, 1),
+            "fused_ms": round(f_ms, 5), "foil_over_fused": round((r_ms + d_ms) / f_ms, 2)}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -404,6 +443,9 @@ def run_ours(args):
     d2h = int(d2h)
     assert np.isfinite(host_out[0].numpy()).all()
 
+    # ---- foil: dequantize to HBM, then standard attention (one layer) --------
+    foil = foil_layer(torch, caches[0], qs[0][0], w, B, H, D, stream) if not args.no_foil else None
+
     # ---- reduce over ranks: bytes summed, time of the slowest rank ----------
     pg = dist if world > 1 else None
     total_bytes, ms_max = job_totals(sum(step_b), ms, pg, device="cuda")
@@ -459,6 +501,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_max / n_e2e, 5),
                 "context_mean": T0 + W + K + (n_e2e - 1) / 2 + 1},
         "gpu_launches": int(launches),
+        "foil": foil,
         "device_status": int(status),
     }
     if not args.no_cpu_baseline:
@@ -501,6 +544,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-foil", action="store_true", help="skip the dequantize-to-HBM foil measurement")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; 0 = all 32)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -125,6 +125,16 @@ typedef struct kvq_decode_opts {
   void* split_stop;    /* optional cudaEvent_t recorded just after it */
 } kvq_decode_opts;
 
+/* Result of kvq_compare (the datawhale page's compare ledger). */
+typedef struct kvq_compare_t {
+  double key_mse, value_mse;        /* mean of (x - restore(quantize(x)))^2 */
+  int64_t n_key_scales;             /* batch * heads * (tokens / group_len) * head_dim */
+  int64_t n_value_scales;           /* batch * heads * tokens */
+  int64_t raw_bytes;                /* Key + Value elements * dtype bytes */
+  int64_t container_quantized_bytes;/* one byte per code + 4 bytes per scale */
+  int64_t packed_quantized_bytes;   /* (codes + 1) / 2 + 4 bytes per scale (two codes a byte) */
+} kvq_compare_t;
+
 typedef struct kvq_cache kvq_cache; /* opaque host handle */
 
 /*
@@ -233,6 +243,48 @@ kvq_status kvq_export_pages(const kvq_cache* cache, int32_t seq, int32_t kv_head
  * reported an error; non-zero codes come from bounded waits that gave up.
  * Returns KVQ_EDEVICE when the word is non-zero. */
 kvq_status kvq_device_status(const kvq_cache* cache, int32_t* out_word, void* stream);
+
+/* Dequantize-to-HBM, step 1 ("KV Cache 量化与压缩" section 06, read path (a);
+ * "54. KV Cache Quantization Strategies", restore).  Writes the held Keys and
+ * Values of sequences [seq_begin, seq_begin + n_seqs) as dense device tensors
+ * k_out, v_out [n_seqs][n_kv_heads][t_stride][head_dim] of out_dtype.
+ * Row t < quantized is code / max(scale, eps) computed in fp32 (Key codes over
+ * their group's per-channel scales, Value codes over their per-token scales),
+ * rounded to nearest even for KVQ_BF16; rows quantized <= t < total are the
+ * residual window as held, converted to out_dtype.  Rows >= total are left
+ * untouched.  t_stride >= the largest total in the range.  The buffers are the
+ * caller's (16-byte aligned).  Errors before any launch: KVQ_EINVAL (bad range,
+ * NULL or misaligned pointer, t_stride too small, unknown dtype). */
+kvq_status kvq_restore(const kvq_cache* cache, int32_t seq_begin, int32_t n_seqs, void* k_out, void* v_out,
+                       int64_t t_stride, kvq_dtype out_dtype, void* stream);
+
+/* Dequantize-to-HBM, step 2: the standard decode attention over dense bf16
+ * Key/Value tensors k, v [batch][n_kv_heads][t_stride][head_dim] (all
+ * sequences, as kvq_restore writes them), each sequence's length taken from
+ * this cache's counters.  The read path the fused kvq_decode_attention
+ * replaces, kept as its measured foil ("KV Cache 量化与压缩" section 06 compares
+ * the two): q and out as in kvq_decode_attention.  Uses the arena's split
+ * scratch region.  Needs a bf16 cache with head_dim 64 or 128, else
+ * KVQ_EUNSUPPORTED; KVQ_EINVAL for NULL or misaligned pointers or a t_stride
+ * below the largest held length. */
+kvq_status kvq_dense_decode_attention(kvq_cache* cache, const void* k, const void* v, int64_t t_stride,
+                                      const void* q, float* out, void* stream);
+
+/* The datawhale page's compare ("54. KV Cache Quantization Strategies",
+ * compare), on the GPU.  key, value: device [batch][heads][tokens][head_dim]
+ * of dtype.  Key is quantized per channel over runs of ``group`` tokens
+ * (group = 0: over all ``tokens``, the page's choice; otherwise group must
+ * divide tokens), Value per token over head_dim, with the cache's quantizer
+ * (scale = qmax / max(absmax, eps), code = clamp(rint(x * scale))); restored as
+ * code / max(scale, eps).  The squared errors are rounded in fp32 and summed in
+ * fp64 (the order of the sum is not fixed).  The byte counts follow the page
+ * (packed bytes assume two codes a byte whatever qmax).  workspace: 16 bytes
+ * of 8-byte aligned device memory.  Synchronizes ``stream``.  Errors:
+ * KVQ_EINVAL for a bad shape, dtype, qmax, eps, group or pointer;
+ * KVQ_EUNSUPPORTED when batch * heads > 65535. */
+kvq_status kvq_compare(const void* key, const void* value, int64_t batch, int32_t heads, int64_t tokens,
+                       int32_t head_dim, kvq_dtype dtype, int32_t qmax, float eps, int32_t group,
+                       void* workspace, kvq_compare_t* out, void* stream);
 
 /* Size in bytes of one group page for this configuration (0 if invalid). */
 size_t kvq_page_bytes(const kvq_config* cfg);

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "KVQ_OK", 1: "KVQ_EINVAL", 2: "KVQ_ECAPACITY", 3: "KVQ_ENOMEM
 EXPORTED = ("kvq_required_bytes", "kvq_create", "kvq_append", "kvq_decode_attention",
             "kvq_decode_attention_ex", "kvq_bytes", "kvq_ledger", "kvq_seq_state", "kvq_export_unit",
             "kvq_export_pages", "kvq_device_status", "kvq_page_bytes", "kvq_kernel_launches", "kvq_destroy",
-            "kvq_last_error", "kvq_decode_attention_noalloc")
+            "kvq_last_error", "kvq_decode_attention_noalloc", "kvq_restore", "kvq_dense_decode_attention",
+            "kvq_compare")
 
 
 class kvq_config(ctypes.Structure):
@@ -49,6 +50,12 @@ class kvq_unit_view(ctypes.Structure):
 class kvq_decode_opts(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("chunk_pages", ctypes.c_int32), ("split_start", ctypes.c_void_p),
                 ("split_stop", ctypes.c_void_p)]
+
+
+class kvq_compare_t(ctypes.Structure):
+    _fields_ = [("key_mse", ctypes.c_double), ("value_mse", ctypes.c_double)] + [
+        (n, ctypes.c_int64) for n in ("n_key_scales", "n_value_scales", "raw_bytes", "container_quantized_bytes",
+                                      "packed_quantized_bytes")]
 
 
 class KVQError(RuntimeError):
@@ -84,6 +91,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_page_bytes": ([P(kvq_config)], SZ),
         "kvq_kernel_launches": ([], ctypes.c_uint64),
         "kvq_decode_attention_noalloc": ([V, V, V, V], ctypes.c_int),
+        "kvq_restore": ([V, I32, I32, V, V, I64, ctypes.c_int, V], ctypes.c_int),
+        "kvq_dense_decode_attention": ([V, V, V, I64, V, V, V], ctypes.c_int),
+        "kvq_compare": ([V, V, I64, I32, I64, I32, ctypes.c_int, I32, ctypes.c_float, I32, V, P(kvq_compare_t), V],
+                        ctypes.c_int),
         "kvq_destroy": ([V], None),
         "kvq_last_error": ([], ctypes.c_char_p),
     }
@@ -182,6 +193,35 @@ def kvq_device_status(handle, stream) -> int:
     return word.value
 
 
+def kvq_restore(handle, seq_begin, n_seqs, k_ptr, v_ptr, t_stride, out_dtype, stream) -> None:
+    _check(load_library().kvq_restore(handle, seq_begin, n_seqs, k_ptr, v_ptr, t_stride, out_dtype, stream))
+
+
+def kvq_dense_decode_attention(handle, k_ptr, v_ptr, t_stride, q_ptr, out_ptr, stream) -> None:
+    _check(load_library().kvq_dense_decode_attention(handle, k_ptr, v_ptr, t_stride, q_ptr, out_ptr, stream))
+
+
+def kvq_compare(key_ptr, value_ptr, batch, heads, tokens, head_dim, dtype, qmax, eps, group, workspace_ptr,
+                stream) -> dict:
+    out = kvq_compare_t()
+    _check(load_library().kvq_compare(key_ptr, value_ptr, batch, heads, tokens, head_dim, dtype, qmax, eps, group,
+                                      workspace_ptr, ctypes.byref(out), stream))
+    return {n: getattr(out, n) for n, _ in kvq_compare_t._fields_}
+
+
+def compare(key, value, qmax=7, eps=1e-8, group=0) -> dict:
+    """The page's compare on device tensors key, value [batch, heads, tokens,
+    head_dim] (bf16 or fp32, contiguous, same shape and dtype)."""
+    import torch
+    assert key.is_cuda and key.shape == value.shape and key.dtype == value.dtype
+    assert key.is_contiguous() and value.is_contiguous() and key.dim() == 4
+    dt = {torch.bfloat16: KVQ_BF16, torch.float32: KVQ_FP32}[key.dtype]
+    ws = torch.empty(2, dtype=torch.float64, device=key.device)
+    b, h, t, d = key.shape
+    return kvq_compare(key.data_ptr(), value.data_ptr(), b, h, t, d, dt, qmax, eps, group, ws.data_ptr(),
+                       torch.cuda.current_stream(key.device).cuda_stream)
+
+
 def kvq_kernel_launches() -> int:
     return load_library().kvq_kernel_launches()
 
@@ -243,6 +283,37 @@ class KVQCache:
         else:
             kvq_decode_attention_ex(self.handle, q.data_ptr(), out.data_ptr(), self._stream(), kernel, chunk_pages,
                                     split_start, split_stop)
+        return out
+
+    def restore(self, seq_begin=0, n_seqs=None, t_stride=None, out_dtype="bf16", k_out=None, v_out=None):
+        """Dense restored Keys and Values [n_seqs, n_kv_heads, t_stride, head_dim]
+        (rows past each sequence's length are left as allocated)."""
+        n_seqs = self.cfg.batch - seq_begin if n_seqs is None else n_seqs
+        if t_stride is None:
+            t_stride = max(1, max(self.seq_state(b)["total"] for b in range(seq_begin, seq_begin + n_seqs)))
+        dt = self.torch.bfloat16 if out_dtype == "bf16" else self.torch.float32
+        shape = (n_seqs, self.cfg.n_kv_heads, t_stride, self.cfg.head_dim)
+        if k_out is None:
+            k_out = self.torch.zeros(shape, dtype=dt, device=self.device)
+        if v_out is None:
+            v_out = self.torch.zeros(shape, dtype=dt, device=self.device)
+        assert tuple(k_out.shape) == shape and tuple(v_out.shape) == shape
+        assert k_out.dtype == dt and v_out.dtype == dt and k_out.is_contiguous() and v_out.is_contiguous()
+        kvq_restore(self.handle, seq_begin, n_seqs, k_out.data_ptr(), v_out.data_ptr(), t_stride,
+                    KVQ_BF16 if out_dtype == "bf16" else KVQ_FP32, self._stream())
+        return k_out, v_out
+
+    def dense_decode_attention(self, k, v, q, out=None):
+        """Standard decode attention over dense restored k, v [batch, n_kv_heads,
+        t_stride, head_dim] (bf16), lengths from this cache."""
+        shape = (self.cfg.batch, self.cfg.n_q_heads, self.cfg.head_dim)
+        self._check_input(q, shape)
+        assert k.shape == v.shape and k.dim() == 4 and k.shape[:2] == (self.cfg.batch, self.cfg.n_kv_heads)
+        assert k.dtype == self.dtype and v.dtype == self.dtype and k.is_contiguous() and v.is_contiguous()
+        if out is None:
+            out = self.torch.empty(shape, dtype=self.torch.float32, device=self.device)
+        kvq_dense_decode_attention(self.handle, k.data_ptr(), v.data_ptr(), k.shape[2], q.data_ptr(), out.data_ptr(),
+                                   self._stream())
         return out
 
     def bytes(self):

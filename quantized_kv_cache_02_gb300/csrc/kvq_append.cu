@@ -207,6 +207,78 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   }
 }
 
+// The datawhale page's compare ("54. KV Cache Quantization Strategies",
+// compare): quantize a Key/Value pair with the flush's quantizer (Key per
+// channel over group_len tokens, Value per token over head_dim), restore
+// (code / max(scale, eps)) and sum the squared errors (x - x_hat)^2, each
+// difference and square rounded in fp32 as the page computes them, the sums
+// in fp64.  One CTA per (Key-scale group, row); rows are the flattened
+// [batch, heads] of the input.
+constexpr int kCompareThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const T* p, int64_t i) {
+  if constexpr (sizeof(T) == 2) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p)[i]);
+  else return reinterpret_cast<const float*>(p)[i];
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kCompareThreads) compare_kernel(const CompareParams p) {
+  __shared__ double red[2][kCompareThreads / 32];
+  pdl_wait();
+  pdl_release();
+  const int D = p.D, L = p.group_len;
+  const float qmax = (float)p.qmax;
+  const int64_t base = ((int64_t)blockIdx.y * p.tokens + (int64_t)blockIdx.x * L) * D;
+  const T* kx = reinterpret_cast<const T*>(p.key) + base;
+  const T* vx = reinterpret_cast<const T*>(p.value) + base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  double ek = 0.0, ev = 0.0;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float a = 0.f;
+    for (int t = 0; t < L; ++t) a = fmaxf(a, fabsf(load_f32(kx, (int64_t)t * D + c)));
+    const float scale = __fdiv_rn(qmax, fmaxf(a, p.eps));
+    const float r = fmaxf(scale, p.eps);
+    for (int t = 0; t < L; ++t) {
+      const float x = load_f32(kx, (int64_t)t * D + c);
+      const float e = __fsub_rn(x, __fdiv_rn((float)quantize_one(x, scale, qmax), r));
+      ek += (double)__fmul_rn(e, e);
+    }
+  }
+  for (int t = warp; t < L; t += nwarps) {
+    float a = 0.f;
+    for (int c = lane; c < D; c += 32) a = fmaxf(a, fabsf(load_f32(vx, (int64_t)t * D + c)));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float scale = __fdiv_rn(qmax, fmaxf(a, p.eps));
+    const float r = fmaxf(scale, p.eps);
+    for (int c = lane; c < D; c += 32) {
+      const float x = load_f32(vx, (int64_t)t * D + c);
+      const float e = __fsub_rn(x, __fdiv_rn((float)quantize_one(x, scale, qmax), r));
+      ev += (double)__fmul_rn(e, e);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ek += __shfl_xor_sync(0xffffffffu, ek, o);
+    ev += __shfl_xor_sync(0xffffffffu, ev, o);
+  }
+  if (lane == 0) {
+    red[0][warp] = ek;
+    red[1][warp] = ev;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double sk = 0.0, sv = 0.0;
+    for (int w = 0; w < nwarps; ++w) {
+      sk += red[0][w];
+      sv += red[1][w];
+    }
+    atomicAdd(p.sums, sk);
+    atomicAdd(p.sums + 1, sv);
+  }
+}
+
 template <typename T, int BITS>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
   const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
@@ -225,6 +297,12 @@ cudaError_t configure_t(size_t smem) {
 cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s) {
   if (dtype == 0) return p.bits == 4 ? launch_t<__nv_bfloat16, 4>(p, s) : launch_t<__nv_bfloat16, 8>(p, s);
   return p.bits == 4 ? launch_t<float, 4>(p, s) : launch_t<float, 8>(p, s);
+}
+
+cudaError_t launch_compare(const CompareParams& p, int64_t rows, cudaStream_t s) {
+  const dim3 grid((unsigned)(p.tokens / p.group_len), (unsigned)rows);
+  if (p.dtype == 0) return launch_pdl(compare_kernel<__nv_bfloat16>, grid, dim3(kCompareThreads), 0, s, p);
+  return launch_pdl(compare_kernel<float>, grid, dim3(kCompareThreads), 0, s, p);
 }
 
 cudaError_t configure_append(int dtype, int bits, size_t smem_bytes) {

@@ -161,8 +161,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
 
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -467,50 +465,69 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
   }
 }
 
-// The residual window of a unit on the tensor cores.  Steps of 16 tokens:
-// the bf16 Key/Value rows are copied from the ring into a per-warp shared
-// buffer (16-byte chunks XOR-swizzled by row so ldmatrix is conflict free;
-// rows past the window are zero-filled), then S = K q with bf16 MMAs (q is
-// the bf16 input, so every product is exact), the same online softmax as the
-// pages, and O^T += V^T P with V^T read by ldmatrix.trans and P as a bf16
-// hi + lo pair.  Column n holds head (n % GP) % g; only n < g is kept.
-template <int D, int GP>
-__device__ __forceinline__ void window_mma(const DecodeParams& p, int i, int h, int lane, int warp, int gid,
-                                           int tig, uint8_t* wbuf, WarpState<D>& st) {
+// A run of bf16 Key/Value rows on the tensor cores: the residual window of a
+// unit (rows in its ring) or a range of a dense restored cache.  Steps of 16
+// tokens: the rows are copied into a per-warp shared buffer with cp.async
+// (16-byte chunks XOR-swizzled by row so ldmatrix is conflict free; rows past
+// the run are zero-filled), double-buffered so the next step's copy overlaps
+// this step's math when NBUF = 2; then S = K q with bf16 MMAs (q is the bf16 input, so every
+// product is exact), the same online softmax as the pages, and O^T += V^T P
+// with V^T read by ldmatrix.trans and P as a bf16 hi + lo pair.  Row t of the
+// run is row (row0 + t) mod ring of kbase / vbase (RING), else row0 + t.
+// Column n holds head (n % GP) % g of the unit; only n < g is kept.
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+template <int D, int GP, int NBUF, bool RING>
+__device__ __forceinline__ void rows_mma(const DecodeParams& p, const __nv_bfloat16* kbase,
+                                         const __nv_bfloat16* vbase, int64_t row0, int ring, int n,
+                                         const __nv_bfloat16* qunit, int lane, int warp, int gid, int tig,
+                                         uint8_t* wbuf, WarpState<D>& st) {
   constexpr int kRow = D * 2;             // bytes of one bf16 row
   constexpr int kChunks = kRow / 16;      // 16-byte chunks per row
-  const int b = p.seq_begin + i;
-  const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-  const int W = (int)(T0 - Q0);
-  const int64_t unit = (int64_t)b * p.Hkv + h;
-  const __nv_bfloat16* rk = reinterpret_cast<const __nv_bfloat16*>(p.ring_k) + unit * p.Rcap * D;
-  const __nv_bfloat16* rv = reinterpret_cast<const __nv_bfloat16*>(p.ring_v) + unit * p.Rcap * D;
+  constexpr int kBuf = 32 * kRow;         // one step: 16 K rows + 16 V rows
   uint32_t bq[D / 16][2];
   {
-    const __nv_bfloat16* q = reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                             ((int64_t)b * p.Hq + (int64_t)h * p.g + (gid % GP) % p.g) * D;
+    const __nv_bfloat16* q = qunit + (int64_t)((gid % GP) % p.g) * D;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       bq[kk][0] = *reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig);
       bq[kk][1] = *reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig + 8);
     }
   }
-  uint8_t* kb = wbuf;
-  uint8_t* vb = wbuf + 16 * kRow;
-  const uint32_t kb_s = smem_addr(kb), vb_s = smem_addr(vb);
-  const int nsteps = (W + 15) / 16;
-  for (int stp = warp; stp < nsteps; stp += kMmaWarps) {
+  const uint32_t buf_s = smem_addr(wbuf);
+  const int nsteps = (n + 15) / 16;
+  // copies of step stp into buffer half ``half``
+  auto issue = [&](int stp, int half) {
     const int t0 = stp * 16;
+    const uint32_t kb = buf_s + half * kBuf, vb = kb + 16 * kRow;
     for (int idx = lane; idx < 16 * kChunks; idx += 32) {
       const int r = idx / kChunks, c = idx - r * kChunks;
-      const bool valid = t0 + r < W;
-      const int64_t row = (Q0 + t0 + (valid ? r : 0)) % p.Rcap;
+      const bool valid = t0 + r < n;
+      const int64_t t = row0 + t0 + (valid ? r : 0);
+      const int64_t row = RING ? t % ring : t;
       const uint32_t off = r * kRow + ((c ^ (r & 7)) * 16);
-      cp_async16(kb_s + off, rk + row * D + c * 8, valid ? 16u : 0u);
-      cp_async16(vb_s + off, rv + row * D + c * 8, valid ? 16u : 0u);
+      cp_async16(kb + off, kbase + row * D + c * 8, valid ? 16u : 0u);
+      cp_async16(vb + off, vbase + row * D + c * 8, valid ? 16u : 0u);
     }
-    cp_async_wait_all();
+    cp_async_commit();
+  };
+  if (NBUF == 2 && warp < nsteps) issue(warp, 0);
+  int half = 0;
+  for (int stp = warp; stp < nsteps; stp += kMmaWarps, half ^= (NBUF - 1)) {
+    if (NBUF == 1) {
+      issue(stp, 0);
+      cp_async_wait_group<0>();
+    } else if (stp + kMmaWarps < nsteps) {
+      issue(stp + kMmaWarps, half ^ 1);
+      cp_async_wait_group<1>();
+    } else {
+      cp_async_wait_group<0>();
+    }
     __syncwarp();
+    const int t0 = stp * 16;
+    const uint32_t kb_s = buf_s + half * kBuf, vb_s = kb_s + 16 * kRow;
     float s[4] = {0.f, 0.f, 0.f, 0.f};
     {
       const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -521,7 +538,7 @@ __device__ __forceinline__ void window_mma(const DecodeParams& p, int i, int h, 
         mma16816_bf16(s, a[0], a[1], a[2], a[3], bq[kk][0], bq[kk][1]);
       }
     }
-    const bool v0 = t0 + gid < W, v1 = t0 + gid + 8 < W;
+    const bool v0 = t0 + gid < n, v1 = t0 + gid + 8 < n;
     s[0] = v0 ? s[0] * p.qk_scale : -INFINITY;
     s[1] = v0 ? s[1] * p.qk_scale : -INFINITY;
     s[2] = v1 ? s[2] * p.qk_scale : -INFINITY;
@@ -567,7 +584,13 @@ __device__ __forceinline__ void window_mma(const DecodeParams& p, int i, int h, 
         mma16816_bf16(st.O[mt], a[0], a[1], a[2], a[3], bl[0], bl[1]);
       }
     }
-    __syncwarp();  // the buffer is refilled by the next step
+    __syncwarp();  // the buffer is refilled by a later step
+  }
+  // sums over the thread's rows -> over the warp's rows
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
+    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
   }
 }
 
@@ -597,6 +620,70 @@ __device__ __forceinline__ void merge_streams(WarpState<D>& st, int off) {
     st.O[mt][3] = st.O[mt][3] * fa1 + o3 * fb1;
   }
 }
+
+// Fold the four warps' (m, l, O) of the stream-0 columns into one partial
+// (o = sum O, m, l per query head) of slot ``slot`` of ``unit``.  ``buf`` is
+// shared memory no warp still reads (kMmaWarps * kMaxGqa * (D + 2) floats).
+template <int D, int GP>
+__device__ __forceinline__ void write_partial(const DecodeParams& p, int64_t unit, int slot, int warp,
+                                              int gid, int tig, const WarpState<D>& st, uint8_t* buf) {
+  const int g = p.g;
+
+  float* mrg = reinterpret_cast<float*>(buf);  // [kMmaWarps][kMaxGqa][D + 2]
+  const int hd0 = 2 * tig, hd1 = 2 * tig + 1;  // heads of the stream-0 columns
+  float* mw = mrg + (size_t)warp * kMaxGqa * (D + 2);
+  const bool stream0 = 2 * tig < GP;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    const int c_lo = 16 * mt + gid;
+    if (stream0 && hd0 < g) {
+      mw[hd0 * (D + 2) + c_lo] = st.O[mt][0];
+      mw[hd0 * (D + 2) + c_lo + 8] = st.O[mt][2];
+    }
+    if (stream0 && hd1 < g) {
+      mw[hd1 * (D + 2) + c_lo] = st.O[mt][1];
+      mw[hd1 * (D + 2) + c_lo + 8] = st.O[mt][3];
+    }
+  }
+  if (gid == 0 && stream0) {
+    if (hd0 < g) {
+      mw[hd0 * (D + 2) + D] = st.m0;
+      mw[hd0 * (D + 2) + D + 1] = st.l0;
+    }
+    if (hd1 < g) {
+      mw[hd1 * (D + 2) + D] = st.m1;
+      mw[hd1 * (D + 2) + D + 1] = st.l1;
+    }
+  }
+  __syncthreads();
+  float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * (D + 2);
+  for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
+    const int j = idx / D, c = idx - j * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, mrg[((size_t)w * kMaxGqa + j) * (D + 2) + D]);
+    float L = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kMmaWarps; ++w) {
+        const float* r = mrg + ((size_t)w * kMaxGqa + j) * (D + 2);
+        if (r[D] == -INFINITY) continue;
+        const float f = exp2f(r[D] - M);
+        L = fmaf(r[D + 1], f, L);
+        O = fmaf(r[c], f, O);
+      }
+    }
+    part[(int64_t)j * (D + 2) + c] = O;
+    if (c == 0) {
+      part[(int64_t)j * (D + 2) + D] = M;
+      part[(int64_t)j * (D + 2) + D + 1] = L;
+    }
+  }
+}
+
+// Per-warp shared bytes of rows_mma: NBUF steps of 16 Key + 16 Value bf16 rows.
+template <int D, int NBUF>
+constexpr int kRowsBuf = NBUF * 32 * D * 2;
 
 template <int D, int BITS, int GP>
 __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const DecodeParams p, int slots) {
@@ -638,12 +725,12 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   bool ok = true;
 
   if (win) {
-    window_mma<D, GP>(p, i, h, lane, warp, gid, tig, buf + (size_t)warp * 32 * D * 2, st);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
-      st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
-    }
+    const int64_t unit = (int64_t)b * p.Hkv + h;
+    const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+    rows_mma<D, GP, 1, true>(p, reinterpret_cast<const __nv_bfloat16*>(p.ring_k) + unit * p.Rcap * D,
+                    reinterpret_cast<const __nv_bfloat16*>(p.ring_v) + unit * p.Rcap * D, Q0, p.Rcap,
+                    (int)(T0 - Q0), reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * g) * D,
+                    lane, warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st);
   } else {
   // queries of the GP column heads (head n % g for the padding columns, so every
   // value stays finite), pre-scaled, in shared memory: channel c of head n goes
@@ -762,61 +849,79 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   for (int off = GP / 2; off < 4; off <<= 1) merge_streams<D>(st, off);
   }  // page path
   __syncthreads();  // every warp is done with its slots: reuse them for the merge
+  write_partial<D, GP>(p, (int64_t)b * p.Hkv + h, slot, warp, gid, tig, st, buf);
+}
 
-  float* mrg = reinterpret_cast<float*>(buf);  // [kMmaWarps][kMaxGqa][D + 2]
-  const int hd0 = 2 * tig, hd1 = 2 * tig + 1;  // heads of the stream-0 columns
-  float* mw = mrg + (size_t)warp * kMaxGqa * (D + 2);
-  const bool stream0 = 2 * tig < GP;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    const int c_lo = 16 * mt + gid;
-    if (stream0 && hd0 < g) {
-      mw[hd0 * (D + 2) + c_lo] = st.O[mt][0];
-      mw[hd0 * (D + 2) + c_lo + 8] = st.O[mt][2];
-    }
-    if (stream0 && hd1 < g) {
-      mw[hd1 * (D + 2) + c_lo] = st.O[mt][1];
-      mw[hd1 * (D + 2) + c_lo + 8] = st.O[mt][3];
-    }
-  }
-  if (gid == 0 && stream0) {
-    if (hd0 < g) {
-      mw[hd0 * (D + 2) + D] = st.m0;
-      mw[hd0 * (D + 2) + D + 1] = st.l0;
-    }
-    if (hd1 < g) {
-      mw[hd1 * (D + 2) + D] = st.m1;
-      mw[hd1 * (D + 2) + D + 1] = st.l1;
-    }
-  }
-  __syncthreads();
+// Decode attention over a dense bf16 Key/Value cache ([batch][Hkv][t_stride][D],
+// as kvq_restore writes it): the second half of the dequantize-to-HBM read
+// path, kept as the measured foil of the fused kernel.  One CTA per
+// (token chunk, unit), column-major like the fused kernel; its four warps take
+// 16-token steps round robin through rows_mma (double-buffered) and the CTA
+// writes the chunk's partial to slot ``chunk``.
+template <int D, int GP>
+__global__ void __launch_bounds__(kMmaThreads) decode_dense_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  pdl_wait();
+  pdl_release();
+  const int n_units = p.n_seqs * p.Hkv;
+  const int col = blockIdx.x / n_units;
+  const int u = blockIdx.x - col * n_units;
+  const int i = u / p.Hkv, h = u - i * p.Hkv;
+  const int64_t T0 = p.ctr[i].total;
+  const int64_t t_begin = (int64_t)col * p.dense_chunk;
+  if (t_begin >= T0) return;
+  const int n = T0 - t_begin < p.dense_chunk ? (int)(T0 - t_begin) : p.dense_chunk;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int b = p.seq_begin + i;
   const int64_t unit = (int64_t)b * p.Hkv + h;
-  float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * (D + 2);
-  for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
-    const int j = idx / D, c = idx - j * D;
-    float M = -INFINITY;
+  WarpState<D> st;
 #pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, mrg[((size_t)w * kMaxGqa + j) * (D + 2) + D]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kMmaWarps; ++w) {
-        const float* r = mrg + ((size_t)w * kMaxGqa + j) * (D + 2);
-        if (r[D] == -INFINITY) continue;
-        const float f = exp2f(r[D] - M);
-        L = fmaf(r[D + 1], f, L);
-        O = fmaf(r[c], f, O);
-      }
-    }
-    part[(int64_t)j * (D + 2) + c] = O;
-    if (c == 0) {
-      part[(int64_t)j * (D + 2) + D] = M;
-      part[(int64_t)j * (D + 2) + D + 1] = L;
-    }
+  for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
+  st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
+  st.m0 = st.m1 = -INFINITY;
+  st.l0 = st.l1 = 0.f;
+  rows_mma<D, GP, 2, false>(p, reinterpret_cast<const __nv_bfloat16*>(p.dense_k) + unit * p.t_stride * D,
+                            reinterpret_cast<const __nv_bfloat16*>(p.dense_v) + unit * p.t_stride * D, t_begin, 0,
+                            n, reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * p.g) * D, lane,
+                            warp, gid, tig, smem + (size_t)warp * kRowsBuf<D, 2>, st);
+  __syncthreads();  // every warp is done with its buffers: reuse them for the merge
+  write_partial<D, GP>(p, unit, col, warp, gid, tig, st, smem);
+}
+
+template <int D>
+size_t dense_smem() {
+  const size_t rows = (size_t)kMmaWarps * kRowsBuf<D, 2>;
+  const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
+  return rows > merge ? rows : merge;
+}
+
+template <int D, int GP>
+cudaError_t launch_dense_t(const DecodeParams& p, int cols, cudaStream_t s) {
+  const size_t smem = dense_smem<D>();
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static size_t configured[64] = {};
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (smem > configured[dev]) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(decode_dense_kernel<D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = smem;
   }
+  return launch_pdl(decode_dense_kernel<D, GP>, dim3(cols * p.n_seqs * p.Hkv), dim3(kMmaThreads), smem, s, p);
 }
 
 int gqa_pad(int g) { return g <= 2 ? 2 : g <= 4 ? 4 : 8; }
+
+template <int D>
+cudaError_t launch_dense_g(const DecodeParams& p, int cols, cudaStream_t s) {
+  switch (gqa_pad(p.g)) {
+    case 2: return launch_dense_t<D, 2>(p, cols, s);
+    case 4: return launch_dense_t<D, 4>(p, cols, s);
+    default: return launch_dense_t<D, 8>(p, cols, s);
+  }
+}
 
 // Shared-memory page slots per warp: about 60 KB of pages per CTA, at least
 // one group (8 / padded g pages) and at most 8.
@@ -835,7 +940,7 @@ size_t smem_for(const DecodeParams& p) {
   const int slots = mma_slots(p.geom.page_bytes, p.g);
   size_t pages = (size_t)kMmaWarps * slots * p.geom.page_bytes;
   const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
-  const size_t window = (size_t)kMmaWarps * 32 * D * 2;  // per warp 16 K rows + 16 V rows of bf16
+  const size_t window = (size_t)kMmaWarps * kRowsBuf<D, 1>;
   if (pages < merge) pages = merge;
   if (pages < window) pages = window;
   const size_t scratch = ((size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D + (size_t)gqa_pad(p.g) * D) * sizeof(float);
@@ -873,6 +978,16 @@ cudaError_t launch_g(const DecodeParams& p, cudaStream_t s) {
 
 size_t decode_mma_smem_bytes(const DecodeParams& p) {
   return p.D == 64 ? smem_for<64>(p) : smem_for<128>(p);
+}
+
+cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supported) {
+  *supported = (p.D == 64 || p.D == 128) && p.g <= kMaxGqa && p.dense_chunk > 0;
+  if (!*supported) return cudaSuccess;
+  int64_t tmax = 0;
+  for (int i = 0; i < p.n_seqs; ++i) tmax = p.ctr[i].total > tmax ? p.ctr[i].total : tmax;
+  const int cols = (int)((tmax + p.dense_chunk - 1) / p.dense_chunk);
+  if (cols == 0) return cudaSuccess;
+  return p.D == 64 ? launch_dense_g<64>(p, cols, s) : launch_dense_g<128>(p, cols, s);
 }
 
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported) {

@@ -50,8 +50,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
   const int b = p.seq_begin + i;
   const int h = hq / p.g, j = hq - h * p.g;
   const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-  const int nsplit = (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
-  const int nslots = nsplit + (T0 > Q0 ? 1 : 0);
+  const int nsplit = p.dense_chunk > 0 ? (T0 + p.dense_chunk - 1) / p.dense_chunk
+                                      : (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
+  const int nslots = nsplit + (p.dense_chunk == 0 && T0 > Q0 ? 1 : 0);
   const int D = p.D;
   const int64_t unit = (int64_t)b * p.Hkv + h;
   const float* base = p.partials + unit * p.max_splits * (int64_t)p.g * (D + 2) + (int64_t)j * (D + 2);

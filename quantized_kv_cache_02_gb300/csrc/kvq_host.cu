@@ -717,4 +717,167 @@ kvq_status kvq_device_status(const kvq_cache* c, int32_t* out_word, void* stream
   return KVQ_OK;
 }
 
+kvq_status kvq_restore(const kvq_cache* c, int32_t seq_begin, int32_t n_seqs, void* k_out, void* v_out,
+                       int64_t t_stride, kvq_dtype out_dtype, void* stream) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (n_seqs <= 0 || seq_begin < 0 || seq_begin + (int64_t)n_seqs > c->cfg.batch)
+    return fail(KVQ_EINVAL, "sequence range [%d, %d) is outside [0, %d)", seq_begin, seq_begin + n_seqs,
+                c->cfg.batch);
+  if (out_dtype != KVQ_BF16 && out_dtype != KVQ_FP32) return fail(KVQ_EINVAL, "unknown out_dtype %d", out_dtype);
+  if (!aligned16(k_out) || !aligned16(v_out))
+    return fail(KVQ_EINVAL, "k_out / v_out must be non-NULL 16-byte aligned device pointers");
+  int64_t tmax = 0, pmax = 0;
+  for (int b = seq_begin; b < seq_begin + n_seqs; ++b) {
+    tmax = std::max<int64_t>(tmax, c->total[b]);
+    pmax = std::max<int64_t>(pmax, c->quantized[b] / c->cfg.group);
+  }
+  if (t_stride < tmax || t_stride < 1)
+    return fail(KVQ_EINVAL, "t_stride %lld is below the largest held length %lld", (long long)t_stride,
+                (long long)tmax);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t unit_elems = t_stride * c->cfg.head_dim;
+  const int osz = out_dtype == KVQ_BF16 ? 2 : 4;
+  for (int s0 = seq_begin; s0 < seq_begin + n_seqs; s0 += kvq::kMaxSeqsPerLaunch) {
+    const int n = std::min(kvq::kMaxSeqsPerLaunch, seq_begin + n_seqs - s0);
+    kvq::RestoreParams p;
+    memset(&p, 0, sizeof p);
+    p.D = c->cfg.head_dim;
+    p.Hkv = c->cfg.n_kv_heads;
+    p.G = c->cfg.group;
+    p.Rcap = c->rcap;
+    p.bits = c->bits;
+    p.eps = c->cfg.eps;
+    p.geom = c->geom;
+    p.pages = c->pages;
+    p.layout = c->layout;
+    p.ring_k = c->ring_k;
+    p.ring_v = c->ring_v;
+    p.in_dtype = c->cfg.dtype == KVQ_BF16 ? 0 : 1;
+    p.out_dtype = out_dtype == KVQ_BF16 ? 0 : 1;
+    const int64_t off = (int64_t)(s0 - seq_begin) * c->cfg.n_kv_heads * unit_elems * osz;
+    p.k_out = static_cast<uint8_t*>(k_out) + off;
+    p.v_out = static_cast<uint8_t*>(v_out) + off;
+    p.t_stride = t_stride;
+    p.page_cols = (int)pmax;
+    p.seq_begin = s0;
+    p.n_seqs = n;
+    fill_counters(c, s0, n, p.ctr);
+    const cudaError_t e = kvq::launch_restore(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "restore launch");
+    g_launches += 1;
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_dense_decode_attention(kvq_cache* c, const void* k, const void* v, int64_t t_stride, const void* q,
+                                      float* out, void* stream) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out))
+    return fail(KVQ_EINVAL, "k / v / q / out must be non-NULL 16-byte aligned device pointers");
+  if (c->cfg.dtype != KVQ_BF16 || (c->cfg.head_dim != 64 && c->cfg.head_dim != 128))
+    return fail(KVQ_EUNSUPPORTED, "dense decode needs a bf16 cache with head_dim 64 or 128");
+  int64_t tmax = 0, total = 0;
+  for (int b = 0; b < c->cfg.batch; ++b) {
+    tmax = std::max<int64_t>(tmax, c->total[b]);
+    total += (int64_t)c->total[b] * c->cfg.n_kv_heads;
+  }
+  if (t_stride < tmax || t_stride < 1)
+    return fail(KVQ_EINVAL, "t_stride %lld is below the largest held length %lld", (long long)t_stride,
+                (long long)tmax);
+  // chunks of whole 64-token rounds (16 tokens per warp step, 4 warps), about
+  // 8 CTAs per SM over the batch, and never more chunks than split slots
+  int64_t chunk = std::max<int64_t>(256, (total + (int64_t)c->n_sm * 8 - 1) / ((int64_t)c->n_sm * 8));
+  chunk = std::max<int64_t>(chunk, (tmax + c->max_splits - 1) / c->max_splits);
+  chunk = (chunk + 63) / 64 * 64;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int s0 = 0; s0 < c->cfg.batch; s0 += kvq::kMaxSeqsPerLaunch) {
+    const int n = std::min(kvq::kMaxSeqsPerLaunch, c->cfg.batch - s0);
+    kvq::DecodeParams p;
+    base_decode_params(c, &p);
+    p.q = q;
+    p.dense_k = k;
+    p.dense_v = v;
+    p.t_stride = t_stride;
+    p.dense_chunk = (int)chunk;
+    p.seq_begin = s0;
+    p.n_seqs = n;
+    fill_counters(c, s0, n, p.ctr);
+    int supported = 0;
+    const cudaError_t e = kvq::launch_decode_dense(p, s, &supported);
+    if (e != cudaSuccess) return cuda_fail(e, "dense decode launch");
+    if (!supported) return fail(KVQ_EUNSUPPORTED, "dense decode does not support this configuration");
+    g_launches += 1;
+  }
+  for (int s0 = 0; s0 < c->cfg.batch; s0 += kvq::kMaxSeqsPerLaunch) {
+    kvq::CombineParams cp;
+    memset(&cp, 0, sizeof cp);
+    cp.D = c->cfg.head_dim;
+    cp.Hkv = c->cfg.n_kv_heads;
+    cp.Hq = c->cfg.n_q_heads;
+    cp.g = c->g;
+    cp.G = c->cfg.group;
+    cp.max_splits = c->max_splits;
+    cp.dense_chunk = (int)chunk;
+    cp.partials = c->partials;
+    cp.out = out;
+    cp.seq_begin = s0;
+    cp.n_seqs = std::min(kvq::kMaxSeqsPerLaunch, c->cfg.batch - s0);
+    fill_counters(c, s0, cp.n_seqs, cp.ctr);
+    const cudaError_t e = kvq::launch_combine(cp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    g_launches += 1;
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_compare(const void* key, const void* value, int64_t batch, int32_t heads, int64_t tokens,
+                       int32_t head_dim, kvq_dtype dtype, int32_t qmax, float eps, int32_t group, void* workspace,
+                       kvq_compare_t* out, void* stream) {
+  if (!out) return fail(KVQ_EINVAL, "out is NULL");
+  if (batch < 1 || heads < 1 || tokens < 1 || head_dim < 1)
+    return fail(KVQ_EINVAL, "shape must be positive (batch %lld, heads %d, tokens %lld, head_dim %d)",
+                (long long)batch, heads, (long long)tokens, head_dim);
+  if (dtype != KVQ_BF16 && dtype != KVQ_FP32) return fail(KVQ_EINVAL, "unknown dtype %d", dtype);
+  if (qmax < 1 || qmax > 127) return fail(KVQ_EINVAL, "qmax must be in [1, 127] (got %d)", qmax);
+  if (!(eps > 0.f) || !std::isfinite(eps)) return fail(KVQ_EINVAL, "eps must be positive and finite");
+  if (group < 0 || (group > 0 && tokens % group != 0))
+    return fail(KVQ_EINVAL, "group %d must be 0 or divide tokens %lld", group, (long long)tokens);
+  if (batch * heads > 65535) return fail(KVQ_EUNSUPPORTED, "batch * heads must be <= 65535");
+  if (!key || !value || !workspace || ((uintptr_t)workspace & 7u) != 0)
+    return fail(KVQ_EINVAL, "key / value / workspace must be non-NULL device pointers (workspace 8-byte aligned)");
+  const int64_t group_len = group > 0 ? group : tokens;
+  if (tokens / group_len > 0x7fffffff) return fail(KVQ_EUNSUPPORTED, "too many Key-scale groups");
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  kvq::CompareParams p;
+  memset(&p, 0, sizeof p);
+  p.key = key;
+  p.value = value;
+  p.tokens = tokens;
+  p.D = head_dim;
+  p.dtype = dtype == KVQ_BF16 ? 0 : 1;
+  p.qmax = qmax;
+  p.group_len = (int32_t)group_len;
+  p.eps = eps;
+  p.sums = static_cast<double*>(workspace);
+  double sums[2] = {0.0, 0.0};
+  cudaError_t e = cudaMemsetAsync(workspace, 0, 2 * sizeof(double), s);
+  if (e == cudaSuccess) e = kvq::launch_compare(p, batch * heads, s);
+  if (e == cudaSuccess) g_launches += 1;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(sums, workspace, sizeof sums, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "kvq_compare");
+  const int64_t n = batch * heads * tokens * head_dim;
+  const int64_t n_kscales = batch * heads * (tokens / group_len) * head_dim;
+  const int64_t n_vscales = batch * heads * tokens;
+  const int64_t scale_bytes = 4 * (n_kscales + n_vscales);
+  out->key_mse = sums[0] / (double)n;
+  out->value_mse = sums[1] / (double)n;
+  out->n_key_scales = n_kscales;
+  out->n_value_scales = n_vscales;
+  out->raw_bytes = 2 * n * (dtype == KVQ_BF16 ? 2 : 4);
+  out->container_quantized_bytes = 2 * n + scale_bytes;
+  out->packed_quantized_bytes = (2 * n + 1) / 2 + scale_bytes;
+  return KVQ_OK;
+}
+
 }  // extern "C"

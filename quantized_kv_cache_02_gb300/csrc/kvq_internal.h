@@ -88,11 +88,17 @@ struct DecodeParams {
   int32_t grid_splits;         // quantized split columns in this launch (window column after)
   int32_t seq_begin, n_seqs;
   int32_t* status;
+  // dense restored cache (decode_dense_kernel only): [batch][Hkv][t_stride][D]
+  const void* dense_k;
+  const void* dense_v;
+  int64_t t_stride;
+  int32_t dense_chunk;         // tokens per dense split
   SeqCounters ctr[kMaxSeqsPerLaunch];
 };
 
 struct CombineParams {
   int32_t D, Hkv, Hq, g, G, max_splits, chunk_pages;
+  int32_t dense_chunk;         // > 0: slots are dense token chunks, no window slot
   const float* partials;
   float* out;                  // [batch][Hq][D]
   int32_t seq_begin, n_seqs;
@@ -123,6 +129,37 @@ cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t sm
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// Dequantize a cache into dense tensors (kvq_restore).  Grid: one CTA per
+// (page column, unit) plus a window column.
+struct RestoreParams {
+  int32_t D, Hkv, G, Rcap, bits;
+  float eps;
+  PageGeom geom;
+  const uint8_t* pages;
+  const SeqLayout* layout;
+  const void* ring_k;          // cache dtype
+  const void* ring_v;
+  int32_t in_dtype, out_dtype; // 0 bf16, 1 fp32
+  void* k_out;                 // [n_seqs][Hkv][t_stride][D] (out dtype)
+  void* v_out;
+  int64_t t_stride;
+  int32_t page_cols;           // grid columns for pages (the window column follows)
+  int32_t seq_begin, n_seqs;
+  SeqCounters ctr[kMaxSeqsPerLaunch];
+};
+
+// The datawhale page's compare: quantize a Key/Value pair, restore, sum the
+// squared errors (kvq_compare).
+struct CompareParams {
+  const void* key;             // [rows][tokens][D] (dtype)
+  const void* value;
+  int64_t tokens;
+  int32_t D, dtype, qmax;
+  int32_t group_len;           // tokens per Key scale (a divisor of tokens)
+  float eps;
+  double* sums;                // [2]: Key, Value squared-error sums (accumulated)
+};
+
 // Launchers (defined in the kernel translation units). Return the launch's error code.
 cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s);
 cudaError_t configure_append(int dtype, int bits, size_t smem_bytes);
@@ -130,5 +167,8 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s)
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported);
 size_t decode_mma_smem_bytes(const DecodeParams& p);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
+cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supported);
+cudaError_t launch_restore(const RestoreParams& p, cudaStream_t s);
+cudaError_t launch_compare(const CompareParams& p, int64_t rows, cudaStream_t s);
 
 }  // namespace kvq

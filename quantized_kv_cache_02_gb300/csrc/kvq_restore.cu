@@ -1,0 +1,161 @@
+// Dequantize a cache into dense Key/Value tensors (kvq_restore): the first
+// half of the dequantize-to-HBM read path ("KV Cache 量化与压缩" section 06,
+// path (a)), kept as the measured foil of the fused decode kernel.
+//
+// Row t < quantized of a unit is restore(code, scale) = code / max(scale, eps)
+// in fp32 ("54. KV Cache Quantization Strategies", restore): Key codes over the
+// page's per-channel scales, Value codes over the per-token scales; rows from
+// quantized to total are the residual window as held.  A CTA per (page column,
+// unit) stages its group page in shared memory with 16-byte loads, decodes the
+// offset-binary codes of the layout in kvq.h (the channel-major Value codes
+// through a shared [G][D] tile) and writes 8 channels per thread (16- or
+// 32-byte stores); the last grid column copies the window rows.
+
+#include <cuda_bf16.h>
+
+#include "kvq_internal.h"
+
+namespace kvq {
+namespace {
+
+constexpr int kRestoreThreads = 256;
+
+__device__ __forceinline__ int key_code_at(const uint8_t* page, int t, int c, int D, int bits) {
+  if (bits == 4) {
+    const uint8_t byte = page[t * (D / 2) + c / 2];
+    return (int)((c & 1) ? byte >> 4 : byte & 0xF) - 8;
+  }
+  return (int)page[t * D + c] - 128;
+}
+
+__device__ __forceinline__ void store8(void* out, int64_t elem, const float (&x)[8], int out_dtype) {
+  if (out_dtype == 0) {
+    uint4 w;
+    uint32_t* u = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+      u[e] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + elem) = w;
+  } else {
+    float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + elem);
+    o[0] = make_float4(x[0], x[1], x[2], x[3]);
+    o[1] = make_float4(x[4], x[5], x[6], x[7]);
+  }
+}
+
+__device__ __forceinline__ void load8(const void* in, int64_t elem, float (&x)[8], int in_dtype) {
+  if (in_dtype == 0) {
+    const uint4 w = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(in) + elem);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      x[2 * e] = f.x;
+      x[2 * e + 1] = f.y;
+    }
+  } else {
+    const float4* f = reinterpret_cast<const float4*>(reinterpret_cast<const float*>(in) + elem);
+    const float4 a = f[0], b = f[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+__global__ void __launch_bounds__(kRestoreThreads) restore_kernel(const RestoreParams p) {
+  extern __shared__ __align__(16) uint8_t page[];
+  pdl_wait();
+  pdl_release();
+  const int n_units = p.n_seqs * p.Hkv;
+  const int col = blockIdx.x / n_units;
+  const int u = blockIdx.x - col * n_units;
+  const int i = u / p.Hkv, h = u - i * p.Hkv;
+  const int b = p.seq_begin + i;
+  const int D = p.D, G = p.G;
+  const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+  const int64_t out_unit = ((int64_t)i * p.Hkv + h) * p.t_stride;  // first row of the unit in the output
+  const int per_row = D / 8;
+
+  if (col == p.page_cols) {
+    // the window rows, as held in the ring
+    const int64_t unit = (int64_t)b * p.Hkv + h;
+    const int esz = p.in_dtype == 0 ? 2 : 4;
+    const uint8_t* rk = reinterpret_cast<const uint8_t*>(p.ring_k) + unit * p.Rcap * D * esz;
+    const uint8_t* rv = reinterpret_cast<const uint8_t*>(p.ring_v) + unit * p.Rcap * D * esz;
+    for (int idx = threadIdx.x; idx < (T0 - Q0) * per_row; idx += blockDim.x) {
+      const int r = idx / per_row, c8 = (idx - r * per_row) * 8;
+      const int t = Q0 + r;
+      const int64_t src = (int64_t)(t % p.Rcap) * D + c8;
+      float x[8];
+      load8(rk, src, x, p.in_dtype);
+      store8(p.k_out, (out_unit + t) * D + c8, x, p.out_dtype);
+      load8(rv, src, x, p.in_dtype);
+      store8(p.v_out, (out_unit + t) * D + c8, x, p.out_dtype);
+    }
+    return;
+  }
+  if (col >= Q0 / G) return;
+  const PageGeom& geom = p.geom;
+  const uint8_t* src = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride + (int64_t)col * geom.page_bytes;
+  for (int o = threadIdx.x * 16; o < geom.page_bytes; o += blockDim.x * 16)
+    *reinterpret_cast<uint4*>(page + o) = *reinterpret_cast<const uint4*>(src + o);
+  __syncthreads();
+  const float* ks = reinterpret_cast<const float*>(page + geom.kscale_off);
+  const float* vs = reinterpret_cast<const float*>(page + geom.vscale_off);
+  const uint8_t* vbase = page + geom.code_bytes;
+  float* vtile = reinterpret_cast<float*>(page + ((geom.page_bytes + 15) / 16) * 16);  // [G][D]
+  const int64_t row0 = out_unit + (int64_t)col * G;
+  // Value codes: one thread per (channel, 32-bit word of its sub-tile row), the
+  // word's tokens restored into a [G][D] tile (consecutive threads, consecutive
+  // channels: no bank conflicts on the tile)
+  const int wpt = 32 / p.bits;  // codes per word
+  for (int idx = threadIdx.x; idx < G * D / wpt; idx += blockDim.x) {
+    const int wi = idx / D, c = idx - wi * D;  // word index along the tokens, channel
+    const int t0 = wi * wpt;
+    const int st = t0 / 32, n_st = min(32, G - 32 * st);
+    const uint8_t* sub = vbase + (size_t)st * 32 * D * p.bits / 8;
+    const uint32_t word = reinterpret_cast<const uint32_t*>(sub)[c * (n_st / wpt) + (t0 - 32 * st) / wpt];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (j >= wpt) break;
+      int t, code;
+      if (p.bits == 4) {
+        t = t0 + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
+        code = (int)((word >> (4 * j)) & 0xF) - 8;
+      } else {
+        t = t0 + j;
+        code = (int)((word >> (8 * j)) & 0xFF) - 128;
+      }
+      vtile[t * D + c] = __fdiv_rn((float)code, fmaxf(vs[t], p.eps));
+    }
+  }
+  // Key codes: one thread per (token, 8 channels); then both rows go out as
+  // 16-byte (bf16) or 32-byte (fp32) stores
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * per_row; idx += blockDim.x) {
+    const int t = idx / per_row, c8 = (idx - t * per_row) * 8;
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      x[e] = __fdiv_rn((float)key_code_at(page, t, c8 + e, D, p.bits), fmaxf(ks[c8 + e], p.eps));
+    store8(p.k_out, (row0 + t) * D + c8, x, p.out_dtype);
+    const float4 a = *reinterpret_cast<const float4*>(vtile + t * D + c8);
+    const float4 b4 = *reinterpret_cast<const float4*>(vtile + t * D + c8 + 4);
+    const float y[8] = {a.x, a.y, a.z, a.w, b4.x, b4.y, b4.z, b4.w};
+    store8(p.v_out, (row0 + t) * D + c8, y, p.out_dtype);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_restore(const RestoreParams& p, cudaStream_t s) {
+  const size_t smem = (size_t)(p.geom.page_bytes + 15) / 16 * 16 + (size_t)p.G * p.D * sizeof(float);
+  if (smem > 48 * 1024) {
+    const cudaError_t e = cudaFuncSetAttribute(restore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(restore_kernel, dim3((p.page_cols + 1) * p.n_seqs * p.Hkv), dim3(kRestoreThreads), smem, s, p);
+}
+
+}  // namespace kvq

@@ -104,3 +104,24 @@ def test_capacity_validation_and_null_handles():
     caps = (ctypes.c_int64 * 2)(64, 64)
     rc = lib.kvq_create(ctypes.byref(cfg), caps, ctypes.cast(buf, ctypes.c_void_p), 16, ctypes.byref(handle))
     assert rc != kvq.binding.KVQ_OK and handle.value is None
+
+
+def test_restore_dense_and_compare_validate_before_any_launch():
+    lib = kvq.load_library()
+    assert lib.kvq_restore(None, 0, 1, None, None, 8, 0, None) == kvq.binding.KVQ_EINVAL
+    assert lib.kvq_dense_decode_attention(None, None, None, 8, None, None, None) == kvq.binding.KVQ_EINVAL
+    out = kvq.binding.kvq_compare_t()
+    ws = ctypes.c_void_p(64)  # never dereferenced: every case below fails validation first
+    good = dict(batch=1, heads=2, tokens=32, head_dim=16, dtype=0, qmax=7, eps=1e-8, group=0)
+
+    def call(**kw):
+        a = {**good, **kw}
+        return lib.kvq_compare(ws, ws, a["batch"], a["heads"], a["tokens"], a["head_dim"], a["dtype"], a["qmax"],
+                               a["eps"], a["group"], ws, ctypes.byref(out), None)
+
+    for bad in [dict(batch=0), dict(tokens=0), dict(head_dim=0), dict(dtype=5), dict(qmax=0), dict(qmax=128),
+                dict(eps=0.0), dict(group=-1), dict(group=5)]:
+        assert call(**bad) == kvq.binding.KVQ_EINVAL, bad
+    assert call(batch=70000) == kvq.binding.KVQ_EUNSUPPORTED
+    assert lib.kvq_compare(None, ws, 1, 2, 32, 16, 0, 7, 1e-8, 0, ws, ctypes.byref(out), None) == kvq.binding.KVQ_EINVAL
+    assert lib.kvq_compare(ws, ws, 1, 2, 32, 16, 0, 7, 1e-8, 0, ws, None, None) == kvq.binding.KVQ_EINVAL
