@@ -73,7 +73,8 @@ typedef struct kvq_config {
   int32_t head_dim;     /* d: a multiple of 16, 16 <= d <= 256 */
   int32_t residual_len; /* R > 0: tokens kept at input precision */
   int32_t group;        /* G > 0, a multiple of 8: tokens quantized together */
-  int32_t qmax;         /* 1..7: signed 4-bit codes, two per byte;
+  int32_t qmax;         /* 1: signed 2-bit codes (-1, 0, 1), four per byte;
+                           2..7: signed 4-bit codes, two per byte;
                            8..127: signed 8-bit codes */
   int32_t dtype;        /* kvq_dtype of inputs and window */
   float eps;            /* absmax floor for the scale, e.g. 1e-8f (> 0) */
@@ -141,18 +142,21 @@ typedef struct kvq_cache kvq_cache; /* opaque host handle */
  * Device-memory layout (documented so that pages can be inspected).
  *
  * Group page: one per (sequence, KV head, flushed group), written once by the
- * flush and never again.  With bits = 4 (qmax <= 7) or 8, in order:
- *   Codes are stored offset binary: code + 8 in a nibble (1..15 for qmax 7),
- *   code + 128 in a byte.
- *   1. Key codes: G rows (token order) of head_dim*bits/8 bytes.  4-bit: byte i
- *      holds channel 2i in bits 0-3 and channel 2i+1 in bits 4-7; 8-bit: byte c
- *      is channel c.
+ * flush and never again.  With bits = 2 (qmax <= 1, KIVI's 2-bit codes), 4
+ * (qmax <= 7) or 8, in order:
+ *   Codes are stored offset binary: code + 2 in two bits (1..3 for qmax 1),
+ *   code + 8 in a nibble (1..15 for qmax 7), code + 128 in a byte.
+ *   1. Key codes: G rows (token order) of head_dim*bits/8 bytes.  2-bit: byte
+ *      i holds channel 4i+k in bits 2k..2k+1; 4-bit: byte i holds channel 2i in
+ *      bits 0-3 and channel 2i+1 in bits 4-7; 8-bit: byte c is channel c.
  *   2. Value codes in sub-tiles of 32 tokens (the last sub-tile holds G mod 32
  *      tokens if G is not a multiple of 32).  A sub-tile of n tokens is head_dim
  *      rows (channel order) of n*bits/8 bytes.  4-bit rows are little-endian
  *      32-bit words; word w covers tokens 8w..8w+7 of the sub-tile and its
  *      nibble j holds token 8w+2j for j < 4 and token 8w+2(j-4)+1 for j >= 4.
- *      8-bit rows hold token i in byte i.
+ *      2-bit rows are little-endian 16-bit pieces; piece p covers tokens
+ *      8p..8p+7, its bits 2f..2f+1 hold token 8p+2f and bits 8+2f..9+2f token
+ *      8p+2f+1 (f = 0..3).  8-bit rows hold token i in byte i.
  *   3. Key scales: head_dim fp32.   4. Value scales: G fp32.
  *   Page size = 2*G*head_dim*bits/8 + 4*head_dim + 4*G bytes.
  * Pages of one unit are contiguous and in token order.

@@ -375,12 +375,20 @@ def grouped_counts(total: int, residual_length: int, group: int):
     return quantized, total - quantized
 
 
+def code_bits(qmax: int) -> int:
+    """Bits of one stored code: the fewest of 2, 4, 8 that hold the 2*qmax + 1
+    levels -qmax..qmax."""
+    return 2 if qmax <= 1 else 4 if qmax <= 7 else 8
+
+
 def held_ledger(totals, n_kv_heads: int, head_dim: int, residual_length: int, group: int,
                 qmax: int, window_element_bytes: int) -> dict:
     """Bytes a grouped-mode cache holds for sequences of the given lengths:
-    codes (4-bit packed when qmax <= 7, else int8), fp32 Key scales (one per
-    channel per group), fp32 Value scales (one per token) and the window."""
-    bits = 4 if qmax <= 7 else 8
+    codes (2-bit packed when qmax <= 1 -- KIVI's 2-bit codes, "KV Cache 量化与压缩"
+    section 04 --, 4-bit packed when qmax <= 7, else int8), fp32 Key scales
+    (one per channel per group), fp32 Value scales (one per token) and the
+    window."""
+    bits = code_bits(qmax)
     code = n_scales = window_elems = 0
     for total in totals:
         quantized, window = grouped_counts(int(total), residual_length, group)

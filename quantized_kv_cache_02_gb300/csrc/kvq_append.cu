@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   float* sK = tile + G * D;
   float* sV = sK + D;
   const float qmax = (float)p.qmax;
-  constexpr int kBias = BITS == 4 ? 8 : 128;  // stored offset binary: code + bias
+  constexpr int kBias = BITS == 2 ? 2 : BITS == 4 ? 8 : 128;  // stored offset binary: code + bias
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
 
   // ---- Key: per-channel absmax over the group's tokens --------------------
@@ -173,7 +173,22 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
     for (int st = 0; st < n_sub; ++st) {
       const int n_st = min(32, G - 32 * st);
       uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
-      if (BITS == 4) {
+      if (BITS == 2) {
+        // 16-bit pieces of 8 tokens: even tokens in the low byte, odd in the high
+        const int np = n_st / 8;  // pieces per channel row
+        uint16_t* vp = reinterpret_cast<uint16_t*>(vc);
+        for (int idx = threadIdx.x; idx < D * np; idx += blockDim.x) {
+          const int w = idx / D, c = idx - w * D;
+          uint32_t piece = 0;
+#pragma unroll
+          for (int f = 0; f < 4; ++f) {
+            const int te = 32 * st + 8 * w + 2 * f;
+            piece |= ((uint32_t)(quantize_one(tile[te * D + c], sV[te], qmax) + kBias)) << (2 * f);
+            piece |= ((uint32_t)(quantize_one(tile[(te + 1) * D + c], sV[te + 1], qmax) + kBias)) << (8 + 2 * f);
+          }
+          vp[c * np + w] = (uint16_t)piece;
+        }
+      } else if (BITS == 4) {
         const int nw = n_st / 8;  // words per channel row
         // channel fastest across threads: each token row is read at consecutive addresses
         for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
@@ -295,7 +310,11 @@ cudaError_t configure_t(size_t smem) {
 }  // namespace
 
 cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s) {
-  if (dtype == 0) return p.bits == 4 ? launch_t<__nv_bfloat16, 4>(p, s) : launch_t<__nv_bfloat16, 8>(p, s);
+  if (dtype == 0) {
+    if (p.bits == 2) return launch_t<__nv_bfloat16, 2>(p, s);
+    return p.bits == 4 ? launch_t<__nv_bfloat16, 4>(p, s) : launch_t<__nv_bfloat16, 8>(p, s);
+  }
+  if (p.bits == 2) return launch_t<float, 2>(p, s);
   return p.bits == 4 ? launch_t<float, 4>(p, s) : launch_t<float, 8>(p, s);
 }
 
@@ -306,7 +325,11 @@ cudaError_t launch_compare(const CompareParams& p, int64_t rows, cudaStream_t s)
 }
 
 cudaError_t configure_append(int dtype, int bits, size_t smem_bytes) {
-  if (dtype == 0) return bits == 4 ? configure_t<__nv_bfloat16, 4>(smem_bytes) : configure_t<__nv_bfloat16, 8>(smem_bytes);
+  if (dtype == 0) {
+    if (bits == 2) return configure_t<__nv_bfloat16, 2>(smem_bytes);
+    return bits == 4 ? configure_t<__nv_bfloat16, 4>(smem_bytes) : configure_t<__nv_bfloat16, 8>(smem_bytes);
+  }
+  if (bits == 2) return configure_t<float, 2>(smem_bytes);
   return bits == 4 ? configure_t<float, 4>(smem_bytes) : configure_t<float, 8>(smem_bytes);
 }
 

@@ -123,6 +123,49 @@ __device__ __forceinline__ void nibble_regs(uint32_t w, uint32_t (&r)[4]) {
   r[3] = w2 & 0x00F000F0u;
 }
 
+// 2-bit: word of sixteen 2-bit fields (four per byte) -> r[j] = (field j of
+// byte 0, field j of byte 2), r[4 + j] = (field j of byte 1, of byte 3), each
+// carrying a factor 4^j.
+__device__ __forceinline__ void crumb_regs(uint32_t w, uint32_t (&r)[8]) {
+  const uint32_t w2 = w >> 8;
+  r[0] = w & 0x00030003u;
+  r[1] = w & 0x000C000Cu;
+  r[2] = w & 0x00300030u;
+  r[3] = w & 0x00C000C0u;
+  r[4] = w2 & 0x00030003u;
+  r[5] = w2 & 0x000C000Cu;
+  r[6] = w2 & 0x00300030u;
+  r[7] = w2 & 0x00C000C0u;
+}
+
+// 2-bit registers hold u * 4^j * 2^-24 with u = code + 2; subtracting
+// 2 * 4^j * 2^-24 (f16 subnormal arithmetic on small integers is exact) leaves
+// code * 4^j * 2^-24.  With codes of -1..1 and per-group absmax scales, a
+// channel holding one huge outlier adds 2 * q / sK to every token's biased
+// score, and the fp32 accumulation of that term would cost more precision
+// than the subtraction here.
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ void unbias_crumbs(uint32_t (&r)[8]) {
+#pragma unroll
+  for (int m = 0; m < 8; ++m) r[m] = hsub2(r[m], 0x00020002u << (2 * (m & 3)));
+}
+
+// 2-bit Value piece (16 bits: even tokens of an 8-token span in the low byte,
+// odd tokens in the high byte) -> r[j] = (token 2j, token 2j + 1), factor 4^j.
+__device__ __forceinline__ void piece_regs(uint32_t piece, uint32_t (&r)[4]) {
+  const uint32_t x = __byte_perm(piece, 0u, 0x4140);  // bytes (b0, 0, b1, 0)
+  r[0] = x & 0x00030003u;
+  r[1] = x & 0x000C000Cu;
+  r[2] = x & 0x00300030u;
+  r[3] = x & 0x00C000C0u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) r[j] = hsub2(r[j], 0x00020002u << (2 * j));
+}
+
 // 8-bit: word of four bytes -> r[0] = (byte 0, byte 2), r[1] = (byte 1, byte 3).
 __device__ __forceinline__ void byte_regs(uint32_t w, uint32_t (&r)[2]) {
   r[0] = w & 0x00FF00FFu;
@@ -168,8 +211,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 template <int N>
 __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[N]) {
-  static_assert(N % 2 == 0, "word count");
-  if constexpr (N % 4 == 0) {
+  static_assert(N == 1 || N % 2 == 0, "word count");
+  if constexpr (N == 1) {
+    w[0] = *reinterpret_cast<const uint32_t*>(p);
+  } else if constexpr (N % 4 == 0) {
 #pragma unroll
     for (int i = 0; i < N / 4; ++i) {
       const uint4 v = reinterpret_cast<const uint4*>(p)[i];
@@ -200,13 +245,22 @@ struct Shape {
   static constexpr int kChan = D / 4;            // channels of a K row per thread
   static constexpr int kSubBytes = 32 * D * BITS / 8;
   static constexpr int kChunks = D / 4;          // float4 chunks of a page's Key scales
-  static constexpr float kBias = BITS == 4 ? 8.f : 128.f;
+  static constexpr float kBias = BITS == 2 ? 2.f : BITS == 4 ? 8.f : 128.f;
+  // 2-bit: the B operand carries 16 * 4^-j for a code in field j, so that no
+  // q / sK term drops into the f16 subnormals; S is divided by it afterwards
+  static constexpr float kBScale = BITS == 2 ? 16.f : 1.f;
 };
 
 // Channel (in the thread's slice) of element e of k-step kk's B operand:
 // e = 0, 1 -> register 0 (k-slots 2tig, 2tig+1); e = 2, 3 -> register 1.
+// 2-bit: k-step kk = 4i + s takes registers R[2s] (a0) and R[2s + 1] (a2) of
+// word i, R as crumb_regs returns them.
 template <int BITS>
 __device__ __forceinline__ constexpr int kslot_channel(int kk, int e) {
+  if (BITS == 2) {
+    const int m = 2 * (kk & 3) + (e >> 1);
+    return 16 * (kk >> 2) + 4 * (m >> 2) + (m & 3) + 8 * (e & 1);
+  }
   return BITS == 4 ? 8 * (kk >> 1) + 2 * (kk & 1) + (e == 0 ? 0 : e == 1 ? 4 : e == 2 ? 1 : 5)
                    : 4 * kk + (e == 0 ? 0 : e == 1 ? 2 : e == 2 ? 1 : 3);
 }
@@ -215,11 +269,11 @@ __device__ __forceinline__ constexpr int kslot_channel(int kk, int e) {
 // of m-block mb; these orders match how the conversions pair tokens.
 template <int BITS>
 __device__ __forceinline__ int token_row0(int gid, int mb) {
-  return BITS == 4 ? 8 * (gid >> 1) + 4 * mb + (gid & 1) : 8 * (gid >> 1) + 4 * mb + 2 * (gid & 1);
+  return BITS <= 4 ? 8 * (gid >> 1) + 4 * mb + (gid & 1) : 8 * (gid >> 1) + 4 * mb + 2 * (gid & 1);
 }
 template <int BITS>
 __device__ __forceinline__ constexpr int token_row_gap() {
-  return BITS == 4 ? 2 : 1;
+  return BITS <= 4 ? 2 : 1;
 }
 
 template <int D>
@@ -250,9 +304,11 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
     const int j = q / S::kChunks, cc = q - j * S::kChunks;
     if (q < S::PB * S::kChunks && j < npages) {
       const float4 s4 = reinterpret_cast<const float4*>(pg[j] + geom.kscale_off)[cc];
-      constexpr float kOdd = BITS == 4 ? 0.0625f : 1.f;
-      const float4 r4 =
-          make_float4(fast_rcp(s4.x), fast_rcp(s4.y) * kOdd, fast_rcp(s4.z), fast_rcp(s4.w) * kOdd);
+      // the factor that undoes each channel's position in its code word
+      constexpr float f0 = BITS == 2 ? 16.f : 1.f, f1 = BITS == 2 ? 4.f : BITS == 4 ? 0.0625f : 1.f;
+      constexpr float f2 = 1.f, f3 = BITS == 2 ? 0.25f : BITS == 4 ? 0.0625f : 1.f;
+      const float4 r4 = make_float4(fast_rcp(s4.x) * f0, fast_rcp(s4.y) * f1, fast_rcp(s4.z) * f2,
+                                    fast_rcp(s4.w) * f3);
       const int tg = cc / (S::kChan / 4), i = cc - tg * (S::kChan / 4);
       reinterpret_cast<float4*>(rsc + j * D)[i * 4 + tg] = r4;
     }
@@ -265,7 +321,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
     const int jb = FULL ? gid / GP : min(gid / GP, npages - 1);
     const float4* rj = reinterpret_cast<const float4*>(rsc + jb * D);
     float qk[S::kChan];
-    float be = 0.f, bo = 0.f;  // sums over even / odd channels
+    float bs[4] = {0.f, 0.f, 0.f, 0.f};  // sums over channels 4i + k
     const int hq = gid % GP;
 #pragma unroll
     for (int i = 0; i < S::kChan / 4; ++i) {
@@ -275,14 +331,22 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       qk[4 * i + 1] = qv.y * r.y;
       qk[4 * i + 2] = qv.z * r.z;
       qk[4 * i + 3] = qv.w * r.w;
-      be += qk[4 * i + 0] + qk[4 * i + 2];
-      bo += qk[4 * i + 1] + qk[4 * i + 3];
+      bs[0] += qk[4 * i + 0];
+      bs[1] += qk[4 * i + 1];
+      bs[2] += qk[4 * i + 2];
+      bs[3] += qk[4 * i + 3];
     }
-    float beta = BITS == 4 ? fmaf(bo, 16.f, be) : be + bo;
-    beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-    beta += __shfl_xor_sync(0xffffffffu, beta, 2);
-    beta0 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig));
-    beta1 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig + 1));
+    // sum of q / sK with the position factors taken back out
+    if constexpr (BITS == 2) {
+      // 2-bit codes enter the MMA already signed: no bias to take out
+      beta0 = beta1 = 0.f;
+    } else {
+      float beta = BITS == 4 ? (bs[0] + bs[2]) + 16.f * (bs[1] + bs[3]) : (bs[0] + bs[2]) + (bs[1] + bs[3]);
+      beta += __shfl_xor_sync(0xffffffffu, beta, 1);
+      beta += __shfl_xor_sync(0xffffffffu, beta, 2);
+      beta0 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig));
+      beta1 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig + 1));
+    }
 #pragma unroll
     for (int kk = 0; kk < S::kSteps; ++kk) {
 #pragma unroll
@@ -329,7 +393,29 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
         s[mb][0] = s[mb][1] = s[mb][2] = s[mb][3] = 0.f;
         s2[mb][0] = s2[mb][1] = s2[mb][2] = s2[mb][3] = 0.f;
       }
-      if (BITS == 4) {
+      if (BITS == 2) {
+#pragma unroll
+        for (int i = 0; i < S::kWords; ++i) {
+#pragma unroll
+          for (int mb = 0; mb < 2; ++mb) {
+            uint32_t ra[8], rb[8];
+            crumb_regs(wa[mb][i], ra);
+            crumb_regs(wb[mb][i], rb);
+            unbias_crumbs(ra);
+            unbias_crumbs(rb);
+#pragma unroll
+            for (int st2 = 0; st2 < 4; ++st2) {
+              const int kk = 4 * i + st2;
+              mma16816(s[mb], ra[2 * st2], rb[2 * st2], ra[2 * st2 + 1], rb[2 * st2 + 1], bh[kk][0], bh[kk][1]);
+              mma16816(s2[mb], ra[2 * st2], rb[2 * st2], ra[2 * st2 + 1], rb[2 * st2 + 1], bl[kk][0], bl[kk][1]);
+            }
+          }
+        }
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[mb][e] += s2[mb][e];
+      } else if (BITS == 4) {
 #pragma unroll
         for (int i = 0; i < S::kWords; ++i) {
 #pragma unroll
@@ -363,10 +449,11 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       const bool mine = sj == j;
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
-        ss[mb][0] = mine ? fmaf(s[mb][0], kTwo24, -beta0) : ss[mb][0];
-        ss[mb][1] = mine ? fmaf(s[mb][1], kTwo24, -beta1) : ss[mb][1];
-        ss[mb][2] = mine ? fmaf(s[mb][2], kTwo24, -beta0) : ss[mb][2];
-        ss[mb][3] = mine ? fmaf(s[mb][3], kTwo24, -beta1) : ss[mb][3];
+        constexpr float kUnscale = kTwo24 / S::kBScale;
+        ss[mb][0] = mine ? fmaf(s[mb][0], kUnscale, -beta0) : ss[mb][0];
+        ss[mb][1] = mine ? fmaf(s[mb][1], kUnscale, -beta1) : ss[mb][1];
+        ss[mb][2] = mine ? fmaf(s[mb][2], kUnscale, -beta0) : ss[mb][2];
+        ss[mb][3] = mine ? fmaf(s[mb][3], kUnscale, -beta1) : ss[mb][3];
       }
     }
     // ---- online softmax (base 2) over the 32 tokens of each column ----------
@@ -420,8 +507,12 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
 #pragma unroll
     for (int mb = 0; mb < 2; ++mb) {
       const int r0 = token_row0<BITS>(gid, mb);
-      const float i0 = fast_rcp(vscale[r0]);
-      const float i1 = fast_rcp(vscale[r0 + kGap]) * (BITS == 4 ? 0.0625f : 1.f);  // x16 rows
+      // undo the code's position factor: 4-bit x16 on the second row of each
+      // pair; 2-bit x1, x4 (m-block 0) and x16, x64 (m-block 1)
+      const float f0 = BITS == 2 ? (mb == 0 ? 1.f : 0.0625f) : 1.f;
+      const float f1 = BITS == 2 ? (mb == 0 ? 0.25f : 0.015625f) : BITS == 4 ? 0.0625f : 1.f;
+      const float i0 = fast_rcp(vscale[r0]) * f0;
+      const float i1 = fast_rcp(vscale[r0 + kGap]) * f1;
       pk[mb][0] = pack_f16x2(pr[mb][0] * i0, pr[mb][1] * i0);
       pk[mb][1] = pack_f16x2(pr[mb][2] * i1, pr[mb][3] * i1);
     }
@@ -435,13 +526,22 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       for (int mb = 0; mb < 2; ++mb) {
         bp[mb][0] = transpose8x8(mine ? pk[mb][0] : 0u);
         bp[mb][1] = transpose8x8(mine ? pk[mb][1] : 0u);
-        mma16816(st.C, kOneLo, kOneLo, kOneHi, kOneHi, bp[mb][0], bp[mb][1]);
+        // the p / sV sum for the Value bias (2-bit codes enter signed: none)
+        if (BITS != 2) mma16816(st.C, kOneLo, kOneLo, kOneHi, kOneHi, bp[mb][0], bp[mb][1]);
       }
       const uint8_t* vc = pg[j] + geom.code_bytes + sub * S::kSubBytes;
 #pragma unroll
       for (int mt = 0; mt < S::kSteps; ++mt) {
         const int c_lo = 16 * mt + gid, c_hi = c_lo + 8;
-        if (BITS == 4) {
+        if (BITS == 2) {
+          const uint32_t pl = *reinterpret_cast<const uint16_t*>(vc + c_lo * 8 + 2 * tig);
+          const uint32_t ph = *reinterpret_cast<const uint16_t*>(vc + c_hi * 8 + 2 * tig);
+          uint32_t rl[4], rh[4];
+          piece_regs(pl, rl);
+          piece_regs(ph, rh);
+          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
+          mma16816(st.O[mt], rl[2], rh[2], rl[3], rh[3], bp[1][0], bp[1][1]);
+        } else if (BITS == 4) {
           const uint32_t wl = *reinterpret_cast<const uint32_t*>(vc + c_lo * 16 + 4 * tig);
           const uint32_t wh = *reinterpret_cast<const uint32_t*>(vc + c_hi * 16 + 4 * tig);
           uint32_t rl[4], rh[4];
@@ -994,8 +1094,8 @@ cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* suppor
   *supported = (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g >= 2 && p.g <= kMaxGqa &&
                decode_mma_smem_bytes(p) <= kMaxSmem;
   if (!*supported) return cudaSuccess;
-  if (p.D == 64) return p.bits == 4 ? launch_g<64, 4>(p, s) : launch_g<64, 8>(p, s);
-  return p.bits == 4 ? launch_g<128, 4>(p, s) : launch_g<128, 8>(p, s);
+  if (p.D == 64) return p.bits == 2 ? launch_g<64, 2>(p, s) : p.bits == 4 ? launch_g<64, 4>(p, s) : launch_g<64, 8>(p, s);
+  return p.bits == 2 ? launch_g<128, 2>(p, s) : p.bits == 4 ? launch_g<128, 4>(p, s) : launch_g<128, 8>(p, s);
 }
 
 }  // namespace kvq

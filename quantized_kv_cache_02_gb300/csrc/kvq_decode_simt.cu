@@ -87,7 +87,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineP
 }  // namespace
 
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s) {
-  if (dtype == 0) return p.bits == 4 ? launch_bits<__nv_bfloat16, 4>(p, s) : launch_bits<__nv_bfloat16, 8>(p, s);
+  if (dtype == 0) {
+    if (p.bits == 2) return launch_bits<__nv_bfloat16, 2>(p, s);
+    return p.bits == 4 ? launch_bits<__nv_bfloat16, 4>(p, s) : launch_bits<__nv_bfloat16, 8>(p, s);
+  }
+  if (p.bits == 2) return launch_bits<float, 2>(p, s);
   return p.bits == 4 ? launch_bits<float, 4>(p, s) : launch_bits<float, 8>(p, s);
 }
 

@@ -96,7 +96,8 @@ kvq_status check_config(const kvq_config* c) {
   return KVQ_OK;
 }
 
-int bits_of(const kvq_config* c) { return c->qmax <= 7 ? 4 : 8; }
+// Bits of one stored code: 2 (KIVI's 2-bit codes, qmax 1), 4 or 8.
+int bits_of(const kvq_config* c) { return c->qmax <= 1 ? 2 : c->qmax <= 7 ? 4 : 8; }
 int esize_of(const kvq_config* c) { return c->dtype == KVQ_BF16 ? 2 : 4; }
 int rcap_of(const kvq_config* c) {
   return c->group * ((c->residual_len + c->group - 1) / c->group + 1);
@@ -650,7 +651,9 @@ kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, con
   if (e != cudaSuccess) return cuda_fail(e, "kvq_export_unit");
 
   auto sext = [bits](uint32_t v) -> int8_t {  // offset binary -> signed code
-    return bits == 4 ? (int8_t)((int)(v & 0xF) - 8) : (int8_t)((int)(v & 0xFF) - 128);
+    return bits == 2   ? (int8_t)((int)(v & 0x3) - 2)
+           : bits == 4 ? (int8_t)((int)(v & 0xF) - 8)
+                       : (int8_t)((int)(v & 0xFF) - 128);
   };
   for (int64_t pg = 0; pg < P; ++pg) {
     const uint8_t* page = pages.data() + pg * c->geom.page_bytes;
@@ -660,15 +663,20 @@ kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, con
       const int64_t tok = pg * G + t;
       for (int ch = 0; ch < D; ++ch) {
         if (view->k_codes) {
-          const uint32_t byte = bits == 4 ? page[(size_t)t * (D / 2) + ch / 2] : page[(size_t)t * D + ch];
-          view->k_codes[tok * D + ch] = sext(bits == 4 ? (ch & 1 ? byte >> 4 : byte) : byte);
+          const uint32_t byte = page[(size_t)t * (D * bits / 8) + ch * bits / 8];
+          view->k_codes[tok * D + ch] = sext(bits == 8 ? byte : byte >> (bits * (ch % (8 / bits))));
         }
         if (view->v_codes) {
           const uint8_t* vb = page + c->geom.code_bytes;
           const int st_i = t / 32, o = t % 32, n_st = std::min(32, G - 32 * st_i);
           const uint8_t* sub = vb + (size_t)st_i * 32 * D * bits / 8;
           uint32_t code;
-          if (bits == 4) {
+          if (bits == 2) {
+            uint16_t piece;
+            memcpy(&piece, sub + ((size_t)ch * (n_st / 8) + o / 8) * 2, 2);
+            const int k = o % 8;
+            code = (uint32_t)piece >> (8 * (k % 2) + 2 * (k / 2));
+          } else if (bits == 4) {
             uint32_t word;
             memcpy(&word, sub + ((size_t)ch * (n_st / 8) + o / 8) * 4, 4);
             const int k = o % 8, jn = k / 2 + 4 * (k % 2);

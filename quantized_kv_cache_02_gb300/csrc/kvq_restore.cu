@@ -21,6 +21,7 @@ namespace {
 constexpr int kRestoreThreads = 256;
 
 __device__ __forceinline__ int key_code_at(const uint8_t* page, int t, int c, int D, int bits) {
+  if (bits == 2) return (int)((page[t * (D / 4) + c / 4] >> (2 * (c & 3))) & 0x3) - 2;
   if (bits == 4) {
     const uint8_t byte = page[t * (D / 2) + c / 2];
     return (int)((c & 1) ? byte >> 4 : byte & 0xF) - 8;
@@ -105,29 +106,58 @@ __global__ void __launch_bounds__(kRestoreThreads) restore_kernel(const RestoreP
   const float* vs = reinterpret_cast<const float*>(page + geom.vscale_off);
   const uint8_t* vbase = page + geom.code_bytes;
   float* vtile = reinterpret_cast<float*>(page + ((geom.page_bytes + 15) / 16) * 16);  // [G][D]
+  // Restored values m / max(scale, eps) for every magnitude m of a code (2 for
+  // 2-bit, 8 for 4-bit codes): a code c restores to +-table[|c|], which is
+  // exactly c / max(scale, eps) since IEEE division is sign-symmetric.  8-bit
+  // codes (128 magnitudes) divide directly.
+  const int nm = p.bits == 2 ? 2 : p.bits == 4 ? 8 : 0;
+  float* ktab = vtile + G * D;  // [nm][D]
+  float* vtab = ktab + nm * D;  // [G][nm]
+  for (int idx = threadIdx.x; idx < nm * D; idx += blockDim.x) {
+    const int m = idx / D, c = idx - m * D;
+    ktab[idx] = __fdiv_rn((float)m, fmaxf(ks[c], p.eps));
+  }
+  for (int idx = threadIdx.x; idx < nm * G; idx += blockDim.x) {
+    const int t = idx / nm, m = idx - t * nm;
+    vtab[idx] = __fdiv_rn((float)m, fmaxf(vs[t], p.eps));
+  }
+  __syncthreads();
   const int64_t row0 = out_unit + (int64_t)col * G;
-  // Value codes: one thread per (channel, 32-bit word of its sub-tile row), the
-  // word's tokens restored into a [G][D] tile (consecutive threads, consecutive
-  // channels: no bank conflicts on the tile)
-  const int wpt = 32 / p.bits;  // codes per word
-  for (int idx = threadIdx.x; idx < G * D / wpt; idx += blockDim.x) {
-    const int wi = idx / D, c = idx - wi * D;  // word index along the tokens, channel
-    const int t0 = wi * wpt;
+  // Value codes: one thread per (channel, 8-token unit of its sub-tile row: a
+  // 32-bit word at 4 bits, a 16-bit piece at 2 bits; 4 tokens a word at 8
+  // bits), the unit's tokens restored into a [G][D] tile (consecutive threads,
+  // consecutive channels: no bank conflicts on the tile)
+  const int tpu = p.bits == 8 ? 4 : 8;  // tokens per unit
+  for (int idx = threadIdx.x; idx < G * D / tpu; idx += blockDim.x) {
+    const int ui = idx / D, c = idx - ui * D;
+    const int t0 = ui * tpu;
     const int st = t0 / 32, n_st = min(32, G - 32 * st);
-    const uint8_t* sub = vbase + (size_t)st * 32 * D * p.bits / 8;
-    const uint32_t word = reinterpret_cast<const uint32_t*>(sub)[c * (n_st / wpt) + (t0 - 32 * st) / wpt];
+    const uint8_t* row = vbase + (size_t)st * 32 * D * p.bits / 8 + (size_t)c * (n_st * p.bits / 8);
+    const int uo = (t0 - 32 * st) / tpu;
+    const uint32_t unit = p.bits == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(row)[uo]
+                                      : reinterpret_cast<const uint32_t*>(row)[uo];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      if (j >= wpt) break;
+      if (j >= tpu) break;
       int t, code;
-      if (p.bits == 4) {
+      if (p.bits == 2) {
+        t = t0 + 2 * (j & 3) + (j >> 2);
+        code = (int)((unit >> ((j >> 2) * 8 + 2 * (j & 3))) & 0x3) - 2;
+      } else if (p.bits == 4) {
         t = t0 + (j < 4 ? 2 * j : 2 * (j - 4) + 1);
-        code = (int)((word >> (4 * j)) & 0xF) - 8;
+        code = (int)((unit >> (4 * j)) & 0xF) - 8;
       } else {
         t = t0 + j;
-        code = (int)((word >> (8 * j)) & 0xFF) - 128;
+        code = (int)((unit >> (8 * j)) & 0xFF) - 128;
       }
-      vtile[t * D + c] = __fdiv_rn((float)code, fmaxf(vs[t], p.eps));
+      float x;
+      if (nm) {
+        const float r = vtab[t * nm + (code < 0 ? -code : code)];
+        x = code < 0 ? -r : r;
+      } else {
+        x = __fdiv_rn((float)code, fmaxf(vs[t], p.eps));
+      }
+      vtile[t * D + c] = x;
     }
   }
   // Key codes: one thread per (token, 8 channels); then both rows go out as
@@ -137,8 +167,15 @@ __global__ void __launch_bounds__(kRestoreThreads) restore_kernel(const RestoreP
     const int t = idx / per_row, c8 = (idx - t * per_row) * 8;
     float x[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      x[e] = __fdiv_rn((float)key_code_at(page, t, c8 + e, D, p.bits), fmaxf(ks[c8 + e], p.eps));
+    for (int e = 0; e < 8; ++e) {
+      const int code = key_code_at(page, t, c8 + e, D, p.bits);
+      if (nm) {
+        const float r = ktab[(code < 0 ? -code : code) * D + c8 + e];
+        x[e] = code < 0 ? -r : r;
+      } else {
+        x[e] = __fdiv_rn((float)code, fmaxf(ks[c8 + e], p.eps));
+      }
+    }
     store8(p.k_out, (row0 + t) * D + c8, x, p.out_dtype);
     const float4 a = *reinterpret_cast<const float4*>(vtile + t * D + c8);
     const float4 b4 = *reinterpret_cast<const float4*>(vtile + t * D + c8 + 4);
@@ -150,7 +187,9 @@ __global__ void __launch_bounds__(kRestoreThreads) restore_kernel(const RestoreP
 }  // namespace
 
 cudaError_t launch_restore(const RestoreParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)(p.geom.page_bytes + 15) / 16 * 16 + (size_t)p.G * p.D * sizeof(float);
+  const int nm = p.bits == 2 ? 2 : p.bits == 4 ? 8 : 0;
+  const size_t smem = (size_t)(p.geom.page_bytes + 15) / 16 * 16 +
+                      ((size_t)p.G * p.D + (size_t)nm * (p.D + p.G)) * sizeof(float);
   if (smem > 48 * 1024) {
     const cudaError_t e = cudaFuncSetAttribute(restore_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -24,7 +24,10 @@ __device__ __forceinline__ float ld_f32(const __nv_bfloat16* p, int64_t i) { ret
 // offset binary: code + 8 per nibble, code + 128 per byte).
 template <int BITS>
 __device__ __forceinline__ int key_code(const uint8_t* page, int tl, int c, int D) {
-  if (BITS == 4) {
+  if (BITS == 2) {
+    const uint8_t byte = page[(int64_t)tl * (D / 4) + (c >> 2)];
+    return (int)((byte >> (2 * (c & 3))) & 0x3) - 2;
+  } else if (BITS == 4) {
     const uint8_t byte = page[(int64_t)tl * (D / 2) + (c >> 1)];
     const int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
     return nib - 8;
@@ -38,7 +41,12 @@ __device__ __forceinline__ int value_code(const uint8_t* vbase, int G, int tl, i
   const int st = tl >> 5, o = tl & 31;
   const int n_st = min(32, G - 32 * st);
   const uint8_t* sub = vbase + (int64_t)st * 32 * D * BITS / 8;
-  if (BITS == 4) {
+  if (BITS == 2) {
+    // 16-bit pieces of 8 tokens: token 2f in bits 2f, token 2f + 1 in bits 8 + 2f
+    const int k = o & 7;
+    const uint32_t piece = reinterpret_cast<const uint16_t*>(sub)[c * (n_st / 8) + (o >> 3)];
+    return (int)((piece >> (8 * (k & 1) + 2 * (k >> 1))) & 0x3) - 2;
+  } else if (BITS == 4) {
     const int w = o >> 3, k = o & 7;
     const int jn = (k >> 1) + 4 * (k & 1);  // nibble that holds token offset k
     const uint32_t word = reinterpret_cast<const uint32_t*>(sub)[c * (n_st / 8) + w];

@@ -33,15 +33,15 @@ def test_library_exports_every_declared_function():
 
 
 def test_page_bytes_matches_layout_definition():
-    for G, D, qmax in ((32, 128, 7), (64, 128, 127), (128, 128, 7), (8, 16, 7)):
+    for G, D, qmax in ((32, 128, 7), (64, 128, 127), (128, 128, 7), (8, 16, 7), (32, 128, 1), (8, 16, 1)):
         cfg = kvq.make_config(1, 1, 1, D, 8, G, qmax)
-        bits = 4 if qmax <= 7 else 8
-        assert kvq.kvq_page_bytes(cfg) == L.page_bytes(G, D, bits)
+        assert kvq.kvq_page_bytes(cfg) == L.page_bytes(G, D, O.code_bits(qmax))
 
 
 @pytest.mark.parametrize("tokens", [[0], [40, 64, 7], [4096], [8192, 8320, 1, 159]])
 @pytest.mark.parametrize("R,G,qmax,dtype", [(8, 8, 7, kvq.KVQ_FP32), (128, 32, 7, kvq.KVQ_BF16),
-                                            (128, 64, 127, kvq.KVQ_BF16), (256, 128, 7, kvq.KVQ_BF16)])
+                                            (128, 64, 127, kvq.KVQ_BF16), (256, 128, 7, kvq.KVQ_BF16),
+                                            (128, 32, 1, kvq.KVQ_BF16)])
 def test_ledger_matches_oracle(tokens, R, G, qmax, dtype):
     cfg = kvq.make_config(len(tokens), 8, 32, 128, R, G, qmax, dtype)
     got = kvq.kvq_ledger(cfg, tokens)

@@ -410,6 +410,36 @@ def test_layout_key_nibbles():
     assert L.pack_key_codes(codes, 8) == bytes([0x81, 0x7F, 0x79, 0x87])
 
 
+def test_layout_two_bit_key_crumbs():
+    # code + 2 in two bits, channel 4i + k at bits 2k of byte i
+    codes = np.int8([[1, -1, 0, 1, -1, 0, 0, 1]])
+    assert L.pack_key_codes(codes, 2) == bytes([0xE7, 0xE9])
+
+
+def test_layout_two_bit_value_pieces():
+    codes = np.int8([-1, 0, 1, -1, 0, 1, -1, 0]).reshape(8, 1)   # tokens 0..7 of one channel
+    # low byte: tokens 0, 2, 4, 6 (crumbs 1, 3, 2, 1); high byte: tokens 1, 3, 5, 7 (2, 1, 3, 2)
+    assert L.pack_value_codes(codes, 2) == bytes([0x6D, 0xB6])
+    z = np.zeros((32, 16), np.int8)
+    assert L.page_bytes(32, 16, 2) == 448
+    assert len(L.pack_group_page(z, z, np.ones(16), np.ones(32), 2)) == 448
+
+
+def test_code_bits():
+    assert [O.code_bits(q) for q in (1, 2, 7, 8, 127)] == [2, 4, 4, 8, 8]
+
+
+def test_held_ledger_two_bit_codes_halve_the_four_bit_ledger():
+    """The section 05 case with 2-bit codes (qmax = 1): the code bytes halve,
+    scales and window do not change."""
+    four = O.held_ledger([4096], n_kv_heads=8, head_dim=128, residual_length=128, group=128,
+                         qmax=7, window_element_bytes=2)
+    two = O.held_ledger([4096], n_kv_heads=8, head_dim=128, residual_length=128, group=128,
+                        qmax=1, window_element_bytes=2)
+    assert 32 * two["code_bytes"] == 62 * MiB
+    assert two["n_scales"] == four["n_scales"] and two["window_bytes"] == four["window_bytes"]
+
+
 def test_layout_value_word_order():
     codes = np.arange(8, dtype=np.int8).reshape(8, 1)          # tokens 0..7 of one channel
     # nibbles hold tokens 0,2,4,6,1,3,5,7, each code + 8 -> word 0xFDB9ECA8

@@ -79,7 +79,7 @@ class Pair:
         np.testing.assert_array_equal(got["window_k"], wk[h])
         np.testing.assert_array_equal(got["window_v"], wv[h])
         # raw bytes of every group page against the layout encoder
-        bits = 4 if self.qmax <= 7 else 8
+        bits = O.code_bits(self.qmax)
         raw = self.cache.export_pages(b, h)
         G = self.G
         expect = b"".join(
@@ -180,6 +180,50 @@ def test_ragged_8bit(kvq, torch):
             assert_attention_close(got, ref, f"step {step} kernel {kernel}")
     for b in range(4):
         for h in (0, 7):
+            pair.check_unit(b, h)
+    pair.status_ok()
+
+
+# --------------------------------------------------------------------------
+# 2-bit codes (KIVI's 2-bit, qmax = 1): tiny fp32 schedule on the CUDA-core
+# kernel, Llama head shape ragged on both kernels, head_dim 64
+# --------------------------------------------------------------------------
+
+def test_two_bit_tiny_fp32(kvq, torch):
+    spec = gen.InputSpec(seed=21, n_kv_heads=2, n_q_heads=4, head_dim=16, bf16=False)
+    pair = Pair(kvq, torch, 1, 2, 4, 16, 8, 8, 1, 64, dtype="fp32")
+    k, v = spec.kv_block(0, [0], 0, 37)
+    pair.append(k, v)
+    for step in range(12):
+        k, v = spec.kv_block(0, [0], 37 + step, 1)
+        pair.append(k, v)
+        for h in range(2):
+            pair.check_unit(0, h)
+        got, ref = pair.attend(spec.q_block(0, [0], step), kernel=1)
+        assert_attention_close(got, ref, f"2-bit step {step}")
+    pair.status_ok()
+
+
+@pytest.mark.parametrize("D,G,qmax", [(128, 32, 1), (64, 64, 1), (128, 96, 1), (128, 32, 7)])
+def test_two_bit_ragged_both_kernels(kvq, torch, D, G, qmax):
+    """Ragged lengths with Key spikes (x50 entries); qmax 7 runs the same case
+    with 4-bit codes."""
+    spec = gen.InputSpec(seed=22, n_kv_heads=8, n_q_heads=32, head_dim=D, spikes=True)
+    lens = [G * 9 + 5, 3 * G + 128 + 1, 40, 2000]
+    pair = Pair(kvq, torch, 4, 8, 32, D, 128, G, qmax, [n + 8 for n in lens])
+    for b, n in enumerate(lens):
+        k, v = spec.kv_block(0, [b], 0, n)
+        pair.append(k, v, seq_begin=b)
+    for step in range(3):
+        k = np.stack([spec.kv_block(0, [b], lens[b] + step, 1)[0][0] for b in range(4)])
+        v = np.stack([spec.kv_block(0, [b], lens[b] + step, 1)[1][0] for b in range(4)])
+        pair.append(k, v)
+        q = spec.q_block(0, range(4), step)
+        for kernel in (1, 2):
+            got, ref = pair.attend(q, kernel=kernel)
+            assert_attention_close(got, ref, f"qmax {qmax} D {D} G {G} step {step} kernel {kernel}")
+    for b in range(4):
+        for h in (0, 5):
             pair.check_unit(b, h)
     pair.status_ok()
 

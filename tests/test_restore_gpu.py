@@ -71,6 +71,8 @@ def to_bf16_f32(torch, a):
     ("fp32", 7, 8, [0, 5, 45, 17]),            # empty, window only, pages + window
     ("bf16", 7, 32, [300, 700]),               # Llama head shape
     ("bf16", 127, 64, [130, 64 * 5 + 128]),    # 8-bit codes, ragged
+    ("bf16", 1, 32, [500, 129]),               # 2-bit codes
+    ("fp32", 1, 8, [45, 3]),                   # 2-bit codes, fp32 cache
 ])
 def test_restore_fp32_bit_exact(kvq, torch, dtype, qmax, G, lens):
     D, Hkv, Hq, R = (16, 2, 4, 8) if dtype == "fp32" else (128, 8, 32, 128)
