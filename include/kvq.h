@@ -179,6 +179,38 @@ kvq_status kvq_required_bytes(const kvq_config* cfg, const int64_t* capacity_per
 kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
                       size_t device_bytes, kvq_cache** out);
 
+/* Paged cache ("KV Cache 与自回归视频生成" section 05: fixed-size blocks and a
+ * block table per request; "KV Cache 量化与压缩" section 07: low-bit data and
+ * their scales addressed together).  A block is one flushed group of one
+ * sequence for every KV head: n_kv_heads group pages (the layout above) back
+ * to back, so codes and scales travel together.  The arena holds a pool of
+ * ``pool_blocks`` blocks shared by all sequences, a block table row per
+ * sequence (capacity_per_seq[b] / group entries) and the per-sequence residual
+ * windows.  Blocks are taken from the pool when groups flush and returned by
+ * kvq_release; capacity_per_seq[b] only bounds the length of sequence b, the
+ * pool bounds the sum.  Every other call works on a paged cache as on a
+ * contiguous one, with the same results.  kvq_append fails with KVQ_ECAPACITY
+ * (before any launch, state unchanged) when the pool lacks the blocks its
+ * flushes need, and with KVQ_EUNSUPPORTED when one call would flush more than
+ * 4096 groups of one sequence (split such a prefill into several calls).
+ * pool_blocks must be in [1, 2^31); other arguments as kvq_required_bytes /
+ * kvq_create. */
+kvq_status kvq_required_bytes_paged(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks,
+                                    size_t* out_bytes);
+kvq_status kvq_create_paged(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks,
+                            void* device_mem, size_t device_bytes, kvq_cache** out);
+
+/* Empty sequences [seq_begin, seq_begin + n_seqs) (counters to zero); a paged
+ * cache returns their blocks to the pool.  Host bookkeeping only: work already
+ * queued on a stream still sees the old contents, and a later append may
+ * reuse the blocks, so issue everything on one stream (or order the streams)
+ * around a release.  KVQ_EINVAL for a bad range. */
+kvq_status kvq_release(kvq_cache* cache, int32_t seq_begin, int32_t n_seqs);
+
+/* Free and total blocks of a paged cache's pool (both 0 for a contiguous
+ * cache).  Host counters, no device access. */
+kvq_status kvq_pool_state(const kvq_cache* cache, int64_t* free_blocks, int64_t* pool_blocks);
+
 /* Append ``n_tokens`` new tokens to each of the sequences
  * [seq_begin, seq_begin + n_seqs) ("append_and_partition": cat with the window,
  * then flush whole groups).  new_k, new_v: device [n_seqs][n_kv_heads]

@@ -23,7 +23,7 @@ EXPORTED = ("kvq_required_bytes", "kvq_create", "kvq_append", "kvq_decode_attent
             "kvq_decode_attention_ex", "kvq_bytes", "kvq_ledger", "kvq_seq_state", "kvq_export_unit",
             "kvq_export_pages", "kvq_device_status", "kvq_page_bytes", "kvq_kernel_launches", "kvq_destroy",
             "kvq_last_error", "kvq_decode_attention_noalloc", "kvq_restore", "kvq_dense_decode_attention",
-            "kvq_compare")
+            "kvq_compare", "kvq_required_bytes_paged", "kvq_create_paged", "kvq_release", "kvq_pool_state")
 
 
 class kvq_config(ctypes.Structure):
@@ -95,6 +95,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_dense_decode_attention": ([V, V, V, I64, V, V, V], ctypes.c_int),
         "kvq_compare": ([V, V, I64, I32, I64, I32, ctypes.c_int, I32, ctypes.c_float, I32, V, P(kvq_compare_t), V],
                         ctypes.c_int),
+        "kvq_required_bytes_paged": ([P(kvq_config), P(I64), I64, P(SZ)], ctypes.c_int),
+        "kvq_create_paged": ([P(kvq_config), P(I64), I64, V, SZ, P(V)], ctypes.c_int),
+        "kvq_release": ([V, I32, I32], ctypes.c_int),
+        "kvq_pool_state": ([V, P(I64), P(I64)], ctypes.c_int),
         "kvq_destroy": ([V], None),
         "kvq_last_error": ([], ctypes.c_char_p),
     }
@@ -136,6 +140,30 @@ def kvq_ledger(cfg: kvq_config, tokens) -> dict:
 
 def kvq_page_bytes(cfg: kvq_config) -> int:
     return load_library().kvq_page_bytes(ctypes.byref(cfg))
+
+
+def kvq_required_bytes_paged(cfg: kvq_config, capacity, pool_blocks: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().kvq_required_bytes_paged(ctypes.byref(cfg), _i64_array(capacity), pool_blocks,
+                                                   ctypes.byref(out)))
+    return out.value
+
+
+def kvq_create_paged(cfg: kvq_config, capacity, pool_blocks: int, device_ptr: int, device_bytes: int) -> int:
+    handle = ctypes.c_void_p()
+    _check(load_library().kvq_create_paged(ctypes.byref(cfg), _i64_array(capacity), pool_blocks,
+                                           ctypes.c_void_p(device_ptr), device_bytes, ctypes.byref(handle)))
+    return handle.value
+
+
+def kvq_release(handle, seq_begin: int, n_seqs: int) -> None:
+    _check(load_library().kvq_release(handle, seq_begin, n_seqs))
+
+
+def kvq_pool_state(handle) -> tuple:
+    free, total = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(load_library().kvq_pool_state(handle, ctypes.byref(free), ctypes.byref(total)))
+    return free.value, total.value
 
 
 def kvq_create(cfg: kvq_config, capacity, device_ptr: int, device_bytes: int) -> int:
@@ -239,7 +267,9 @@ class KVQCache:
     current stream."""
 
     def __init__(self, batch, n_kv_heads, n_q_heads, head_dim, residual_len, group, qmax, capacity,
-                 dtype="bf16", eps=1e-8, device=None):
+                 dtype="bf16", eps=1e-8, device=None, pool_blocks=0):
+        """pool_blocks > 0 makes a paged cache: ``capacity`` then bounds each
+        sequence's length and the pool of blocks is shared."""
         import torch
         self.torch = torch
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
@@ -249,12 +279,17 @@ class KVQCache:
         if isinstance(capacity, int):
             capacity = [capacity] * batch
         self.capacity = list(capacity)
-        self.nbytes = kvq_required_bytes(self.cfg, self.capacity)
+        self.pool_blocks = pool_blocks
+        self.nbytes = (kvq_required_bytes_paged(self.cfg, self.capacity, pool_blocks) if pool_blocks
+                       else kvq_required_bytes(self.cfg, self.capacity))
         self.arena = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=self.device)
         base = self.arena.data_ptr()
         self._base = (base + 255) // 256 * 256
         with torch.cuda.device(self.device):
-            self.handle = kvq_create(self.cfg, self.capacity, self._base, self.nbytes)
+            if pool_blocks:
+                self.handle = kvq_create_paged(self.cfg, self.capacity, pool_blocks, self._base, self.nbytes)
+            else:
+                self.handle = kvq_create(self.cfg, self.capacity, self._base, self.nbytes)
 
     def _stream(self):
         return self.torch.cuda.current_stream(self.device).cuda_stream
@@ -318,6 +353,13 @@ class KVQCache:
 
     def bytes(self):
         return kvq_bytes(self.handle)
+
+    def release(self, seq_begin=0, n_seqs=1):
+        kvq_release(self.handle, seq_begin, n_seqs)
+
+    def pool_state(self):
+        """(free blocks, pool blocks) of a paged cache."""
+        return kvq_pool_state(self.handle)
 
     def seq_state(self, seq):
         return kvq_seq_state(self.handle, seq)

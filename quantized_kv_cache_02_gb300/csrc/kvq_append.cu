@@ -110,8 +110,15 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   if (j >= F) return;
   const int t_first = Q0 + j * G;
   const PageGeom& geom = p.geom;
-  uint8_t* page = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride +
-                  (t_first / G) * geom.page_bytes;
+  uint8_t* page;
+  if (p.map.table) {
+    // paged: this group's new block, entered in the block table once
+    const int32_t blk = p.blk_ids[p.blk_first[i] + j];
+    page = p.pages + (int64_t)blk * p.map.block_bytes + (int64_t)h * geom.page_bytes;
+    if (h == 0 && threadIdx.x == 0) p.map.table[(int64_t)b * p.map.table_stride + t_first / G] = blk;
+  } else {
+    page = p.pages + page_offset(p.map, geom.page_bytes, b, h, t_first / G);
+  }
   float* tile = smem;
   float* sK = tile + G * D;
   float* sV = sK + D;

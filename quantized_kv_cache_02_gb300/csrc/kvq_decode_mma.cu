@@ -785,7 +785,7 @@ __device__ __forceinline__ void write_partial(const DecodeParams& p, int64_t uni
 template <int D, int NBUF>
 constexpr int kRowsBuf = NBUF * 32 * D * 2;
 
-template <int D, int BITS, int GP>
+template <int D, int BITS, int GP, bool PAGED>
 __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const DecodeParams p, int slots) {
   using S = Shape<D, BITS, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -845,7 +845,13 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   }
   __syncthreads();
 
-  const uint8_t* unit_pages = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride;
+  // source of this warp's pos-th page (pages pg0 + warp, + 4, ...), through
+  // the block table for a paged cache
+  const uint8_t* unit_pages = PAGED ? p.pages : p.pages + page_offset(p.map, page_bytes, b, h, 0);
+  auto src_of = [&](int pos) {
+    const int pg = pg0 + warp + pos * kMmaWarps;
+    return PAGED ? p.pages + page_offset(p.map, page_bytes, b, h, pg) : unit_pages + (int64_t)pg * page_bytes;
+  };
   const int npg = pg1 - pg0;
   const int my_n = warp < npg ? (npg - warp + kMmaWarps - 1) / kMmaWarps : 0;
   if (lane == 0) {
@@ -854,8 +860,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     fence_proxy_async();
     for (int s = 0; s < slots && s < my_n; ++s) {
       mbar_expect_tx(my_bar + 8 * s, page_bytes);
-      bulk_load(smem_addr(my_buf + (size_t)s * page_bytes),
-                unit_pages + (int64_t)(pg0 + warp + s * kMmaWarps) * page_bytes, page_bytes, my_bar + 8 * s);
+      bulk_load(smem_addr(my_buf + (size_t)s * page_bytes), src_of(s), page_bytes, my_bar + 8 * s);
     }
   }
   __syncwarp();
@@ -865,7 +870,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   // lane keeps the same counters; lane 0 issues the copies.
   int k = 0, sidx = 0, consumed = 0, issued = slots < my_n ? slots : my_n;
   uint32_t phases = 0;
-  const uint8_t* next_src = unit_pages + (int64_t)(pg0 + warp + issued * kMmaWarps) * page_bytes;
+  const uint8_t* next_src = PAGED ? nullptr : src_of(issued);  // contiguous: advanced by whole runs
   for (; k < my_n; k += S::PB) {
     const int np = min(S::PB, my_n - k);
     int sl[S::PB];
@@ -901,12 +906,12 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
       for (int j = 0; j < S::PB; ++j) {
         if (j < refill) {
           mbar_expect_tx(my_bar + 8 * sl[j], page_bytes);
-          bulk_load(smem_addr(my_buf + (size_t)sl[j] * page_bytes),
-                    next_src + (int64_t)j * kMmaWarps * page_bytes, page_bytes, my_bar + 8 * sl[j]);
+          const uint8_t* src = PAGED ? src_of(issued + j) : next_src + (int64_t)j * kMmaWarps * page_bytes;
+          bulk_load(smem_addr(my_buf + (size_t)sl[j] * page_bytes), src, page_bytes, my_bar + 8 * sl[j]);
         }
       }
     }
-    next_src += (int64_t)refill * kMmaWarps * page_bytes;
+    if (!PAGED) next_src += (int64_t)refill * kMmaWarps * page_bytes;
     issued += refill;
     sidx += np;
     if (sidx >= slots) sidx -= slots;
@@ -1047,7 +1052,7 @@ size_t smem_for(const DecodeParams& p) {
   return 128 * ((kMmaWarps * slots * 8 + 127) / 128) + scratch + pages;
 }
 
-template <int D, int BITS, int GP>
+template <int D, int BITS, int GP, bool PAGED>
 cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   const size_t smem = smem_for<D>(p);
   int dev = 0;
@@ -1055,22 +1060,22 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
   static size_t configured[64] = {};
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (smem > configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, GP>,
+    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, GP, PAGED>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
   const dim3 grid((p.grid_splits + 1) * p.n_seqs * p.Hkv);
-  return launch_pdl(decode_mma_kernel<D, BITS, GP>, grid, dim3(kMmaThreads), smem, s, p,
+  return launch_pdl(decode_mma_kernel<D, BITS, GP, PAGED>, grid, dim3(kMmaThreads), smem, s, p,
                     mma_slots(p.geom.page_bytes, p.g));
 }
 
 template <int D, int BITS>
 cudaError_t launch_g(const DecodeParams& p, cudaStream_t s) {
   switch (gqa_pad(p.g)) {
-    case 2: return launch_t<D, BITS, 2>(p, s);
-    case 4: return launch_t<D, BITS, 4>(p, s);
-    default: return launch_t<D, BITS, 8>(p, s);
+    case 2: return p.map.table ? launch_t<D, BITS, 2, true>(p, s) : launch_t<D, BITS, 2, false>(p, s);
+    case 4: return p.map.table ? launch_t<D, BITS, 4, true>(p, s) : launch_t<D, BITS, 4, false>(p, s);
+    default: return p.map.table ? launch_t<D, BITS, 8, true>(p, s) : launch_t<D, BITS, 8, false>(p, s);
   }
 }
 

@@ -34,6 +34,14 @@ struct kvq_cache {
   std::vector<int64_t> pages_cap;   // group pages per unit, per sequence
   std::vector<int64_t> page_base;   // byte offset of (seq, head 0, page 0)
   std::vector<int32_t> total, quantized, last_flushed;
+  // paged mode: a pool of blocks (one group of a sequence, every KV head) and
+  // a block table per sequence; free_blocks is a stack of block ids
+  bool paged;
+  int64_t pool_blocks;
+  int32_t table_stride;                      // table entries per sequence
+  int32_t* table;                            // device [batch][table_stride]
+  std::vector<int32_t> free_blocks;
+  std::vector<std::vector<int32_t>> blocks;  // host copy of each sequence's table
   int max_splits;
   int min_chunk_pages;
   int n_sm;
@@ -104,12 +112,17 @@ int rcap_of(const kvq_config* c) {
 }
 
 struct ArenaPlan {
-  size_t status, layout, pages, ring_k, ring_v, partials, total;
+  size_t status, layout, table, pages, ring_k, ring_v, partials, total;
   std::vector<int64_t> pages_cap, page_base;
   int max_splits, min_chunk_pages;
+  int32_t table_stride;
 };
 
-kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a) {
+// Arena of a contiguous cache (pool_blocks = 0: each sequence's pages at a
+// fixed place, sized by its capacity) or a paged one (pool_blocks > 0: a
+// shared pool of blocks and a block table row per sequence, as long as its
+// capacity in groups).
+kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int64_t pool_blocks = 0) {
   if (!cap) return fail(KVQ_EINVAL, "capacity_per_seq is NULL");
   const kvq::PageGeom geom = kvq::make_geom(c->group, c->head_dim, bits_of(c));
   a->pages_cap.assign(c->batch, 0);
@@ -119,10 +132,12 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a) {
     if (cap[b] < 1 || cap[b] >= (int64_t(1) << 31))
       return fail(KVQ_EINVAL, "capacity of sequence %d must be in [1, 2^31) (got %lld)", b, (long long)cap[b]);
     a->pages_cap[b] = cap[b] / c->group;
-    a->page_base[b] = off;
+    a->page_base[b] = pool_blocks > 0 ? 0 : off;
     off += (int64_t)c->n_kv_heads * a->pages_cap[b] * geom.page_bytes;
     pmax = std::max(pmax, a->pages_cap[b]);
   }
+  a->table_stride = (int32_t)std::max<int64_t>(1, pmax);
+  if (pool_blocks > 0) off = pool_blocks * c->n_kv_heads * geom.page_bytes;
   a->min_chunk_pages = (int)std::max<int64_t>(1, (kMinChunkTokens + c->group - 1) / c->group);
   a->max_splits = (int)((pmax + a->min_chunk_pages - 1) / a->min_chunk_pages) + 1;
   const int g = c->n_q_heads / c->n_kv_heads;
@@ -132,6 +147,8 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a) {
   o = align_up(o + sizeof(int32_t), kAlign);
   a->layout = o;
   o = align_up(o + (size_t)c->batch * sizeof(kvq::SeqLayout), kAlign);
+  a->table = o;
+  if (pool_blocks > 0) o = align_up(o + (size_t)c->batch * a->table_stride * sizeof(int32_t), kAlign);
   a->pages = o;
   o = align_up(o + (size_t)off, kAlign);
   const size_t ring = units * rcap_of(c) * c->head_dim * esize_of(c);
@@ -146,6 +163,15 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a) {
 }
 
 bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
+
+kvq::PageMap page_map(const kvq_cache* c) {
+  kvq::PageMap m;
+  m.layout = c->layout;
+  m.table = c->table;
+  m.table_stride = c->table_stride;
+  m.block_bytes = (int64_t)c->cfg.n_kv_heads * c->geom.page_bytes;
+  return m;
+}
 
 void fill_counters(const kvq_cache* c, int seq_begin, int n, SeqCounters* out) {
   for (int i = 0; i < n; ++i) {
@@ -191,7 +217,7 @@ void base_decode_params(const kvq_cache* c, kvq::DecodeParams* p) {
   p->qk_scale = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   p->geom = c->geom;
   p->pages = c->pages;
-  p->layout = c->layout;
+  p->map = page_map(c);
   p->ring_k = c->ring_k;
   p->ring_v = c->ring_v;
   p->partials = c->partials;
@@ -212,25 +238,30 @@ size_t kvq_page_bytes(const kvq_config* cfg) {
   return (size_t)kvq::make_geom(cfg->group, cfg->head_dim, bits_of(cfg)).page_bytes;
 }
 
-kvq_status kvq_required_bytes(const kvq_config* cfg, const int64_t* capacity_per_seq, size_t* out_bytes) {
+}  // extern "C"
+
+namespace {
+
+kvq_status required_bytes(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks,
+                          size_t* out_bytes) {
   if (!out_bytes) return fail(KVQ_EINVAL, "out_bytes is NULL");
   kvq_status st = check_config(cfg);
   if (st != KVQ_OK) return st;
   ArenaPlan a;
-  st = plan_arena(cfg, capacity_per_seq, &a);
+  st = plan_arena(cfg, capacity_per_seq, &a, pool_blocks);
   if (st != KVQ_OK) return st;
   *out_bytes = a.total;
   return KVQ_OK;
 }
 
-kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
-                      size_t device_bytes, kvq_cache** out) {
+kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks, void* device_mem,
+                  size_t device_bytes, kvq_cache** out) {
   if (!out) return fail(KVQ_EINVAL, "out is NULL");
   *out = nullptr;
   kvq_status st = check_config(cfg);
   if (st != KVQ_OK) return st;
   ArenaPlan a;
-  st = plan_arena(cfg, capacity_per_seq, &a);
+  st = plan_arena(cfg, capacity_per_seq, &a, pool_blocks);
   if (st != KVQ_OK) return st;
   if (!device_mem || ((uintptr_t)device_mem & (kAlign - 1)))
     return fail(KVQ_EINVAL, "device_mem must be a 256-byte aligned device pointer");
@@ -257,6 +288,11 @@ kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, vo
   c->last_flushed.assign(cfg->batch, 0);
   c->max_splits = a.max_splits;
   c->min_chunk_pages = a.min_chunk_pages;
+  c->paged = pool_blocks > 0;
+  c->pool_blocks = pool_blocks;
+  c->table_stride = a.table_stride;
+  c->blocks.assign(cfg->batch, {});
+  for (int64_t blk = pool_blocks - 1; blk >= 0; --blk) c->free_blocks.push_back((int32_t)blk);
   c->device = attr.device;
   int cur = 0;
   cudaGetDevice(&cur);
@@ -270,6 +306,7 @@ kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, vo
   c->arena_bytes = device_bytes;
   c->status = reinterpret_cast<int32_t*>(c->base + a.status);
   c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + a.layout);
+  c->table = c->paged ? reinterpret_cast<int32_t*>(c->base + a.table) : nullptr;
   c->pages = c->base + a.pages;
   c->ring_k = c->base + a.ring_k;
   c->ring_v = c->base + a.ring_v;
@@ -295,6 +332,33 @@ kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, vo
   return KVQ_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_required_bytes(const kvq_config* cfg, const int64_t* capacity_per_seq, size_t* out_bytes) {
+  return required_bytes(cfg, capacity_per_seq, 0, out_bytes);
+}
+
+kvq_status kvq_create(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
+                      size_t device_bytes, kvq_cache** out) {
+  return create(cfg, capacity_per_seq, 0, device_mem, device_bytes, out);
+}
+
+kvq_status kvq_required_bytes_paged(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks,
+                                    size_t* out_bytes) {
+  if (pool_blocks < 1 || pool_blocks >= (int64_t(1) << 31))
+    return fail(KVQ_EINVAL, "pool_blocks must be in [1, 2^31) (got %lld)", (long long)pool_blocks);
+  return required_bytes(cfg, capacity_per_seq, pool_blocks, out_bytes);
+}
+
+kvq_status kvq_create_paged(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks,
+                            void* device_mem, size_t device_bytes, kvq_cache** out) {
+  if (pool_blocks < 1 || pool_blocks >= (int64_t(1) << 31))
+    return fail(KVQ_EINVAL, "pool_blocks must be in [1, 2^31) (got %lld)", (long long)pool_blocks);
+  return create(cfg, capacity_per_seq, pool_blocks, device_mem, device_bytes, out);
+}
+
 void kvq_destroy(kvq_cache* cache) { delete cache; }
 
 kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens, int32_t seq_begin,
@@ -314,8 +378,45 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t R = c->cfg.residual_len, G = c->cfg.group;
   const int64_t per_seq_elems = (int64_t)c->cfg.n_kv_heads * n_tokens * c->cfg.head_dim;
-  for (int s0 = seq_begin; s0 < seq_begin + n_seqs; s0 += kvq::kMaxSeqsPerLaunch) {
-    const int n = std::min(kvq::kMaxSeqsPerLaunch, seq_begin + n_seqs - s0);
+  // groups each sequence flushes in this call
+  std::vector<int64_t> flushes(n_seqs);
+  int64_t new_blocks = 0;
+  for (int i = 0; i < n_seqs; ++i) {
+    const int b = seq_begin + i;
+    flushes[i] = kvq::flush_groups(c->total[b] - c->quantized[b], n_tokens, R, G);
+    new_blocks += flushes[i];
+  }
+  // launches: at most kMaxSeqsPerLaunch sequences and, for a paged cache, at
+  // most kMaxNewBlocks new blocks each
+  std::vector<std::pair<int, int>> launches;  // (first sequence, count)
+  for (int i = 0; i < n_seqs;) {
+    int n = 0;
+    int64_t blocks = 0;
+    while (i + n < n_seqs && n < kvq::kMaxSeqsPerLaunch &&
+           (!c->paged || blocks + flushes[i + n] <= kvq::kMaxNewBlocks)) {
+      blocks += flushes[i + n];
+      ++n;
+    }
+    if (n == 0)
+      return fail(KVQ_EUNSUPPORTED, "sequence %d would flush %lld groups in one append; a paged cache takes at most %d "
+                  "per call: split the append", seq_begin + i, (long long)flushes[i], kvq::kMaxNewBlocks);
+    launches.emplace_back(seq_begin + i, n);
+    i += n;
+  }
+  if (c->paged && new_blocks > (int64_t)c->free_blocks.size())
+    return fail(KVQ_ECAPACITY, "the append needs %lld new blocks; the pool has %zu free", (long long)new_blocks,
+                c->free_blocks.size());
+  // take the blocks now (no launch has happened, nothing else can fail before them)
+  std::vector<int32_t> taken;
+  if (c->paged) {
+    for (int64_t k = 0; k < new_blocks; ++k) {
+      taken.push_back(c->free_blocks.back());
+      c->free_blocks.pop_back();
+    }
+  }
+  size_t next_taken = 0;
+  for (const auto& ln : launches) {
+    const int s0 = ln.first, n = ln.second;
     kvq::AppendParams p;
     memset(&p, 0, sizeof p);
     p.D = c->cfg.head_dim;
@@ -328,7 +429,7 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
     p.eps = c->cfg.eps;
     p.geom = c->geom;
     p.pages = c->pages;
-    p.layout = c->layout;
+    p.map = page_map(c);
     p.ring_k = c->ring_k;
     p.ring_v = c->ring_v;
     const int64_t in_off = (int64_t)(s0 - seq_begin) * per_seq_elems * c->esize;
@@ -338,6 +439,17 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
     p.seq_begin = s0;
     p.n_seqs = n;
     fill_counters(c, s0, n, p.old);
+    if (c->paged) {
+      int32_t k = 0;
+      for (int i = 0; i < n; ++i) {
+        p.blk_first[i] = k;
+        for (int64_t j = 0; j < flushes[s0 - seq_begin + i]; ++j) {
+          const int32_t blk = taken[next_taken++];
+          p.blk_ids[k++] = blk;
+          c->blocks[s0 + i].push_back(blk);
+        }
+      }
+    }
     int64_t fmax = 0;
     bool overlap = false;
     for (int i = 0; i < n; ++i) {
@@ -621,10 +733,42 @@ kvq_status kvq_export_pages(const kvq_cache* c, int32_t seq, int32_t kv_head, vo
   if (!host_dst) return fail(KVQ_EINVAL, "host_dst is NULL");
   if (dst_bytes < bytes) return fail(KVQ_EINVAL, "host buffer of %zu bytes < %zu", dst_bytes, bytes);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const uint8_t* src = c->pages + c->page_base[seq] + (int64_t)kv_head * c->pages_cap[seq] * c->geom.page_bytes;
-  cudaError_t e = cudaMemcpyAsync(host_dst, src, bytes, cudaMemcpyDeviceToHost, s);
+  cudaError_t e = cudaSuccess;
+  if (c->paged) {
+    // one copy per block: the pages of a sequence lie wherever its blocks do
+    const int64_t pb = c->geom.page_bytes;
+    for (size_t j = 0; j < c->blocks[seq].size() && e == cudaSuccess; ++j) {
+      const uint8_t* src = c->pages + (int64_t)c->blocks[seq][j] * c->cfg.n_kv_heads * pb + (int64_t)kv_head * pb;
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(host_dst) + j * pb, src, pb, cudaMemcpyDeviceToHost, s);
+    }
+  } else {
+    const uint8_t* src = c->pages + c->page_base[seq] + (int64_t)kv_head * c->pages_cap[seq] * c->geom.page_bytes;
+    e = cudaMemcpyAsync(host_dst, src, bytes, cudaMemcpyDeviceToHost, s);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_export_pages");
+}
+
+kvq_status kvq_release(kvq_cache* c, int32_t seq_begin, int32_t n_seqs) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (n_seqs <= 0 || seq_begin < 0 || seq_begin + (int64_t)n_seqs > c->cfg.batch)
+    return fail(KVQ_EINVAL, "sequence range [%d, %d) is outside [0, %d)", seq_begin, seq_begin + n_seqs,
+                c->cfg.batch);
+  for (int b = seq_begin; b < seq_begin + n_seqs; ++b) {
+    // most recently taken first, so that a release followed by the same appends
+    // hands the blocks out in the same order again
+    for (auto it = c->blocks[b].rbegin(); it != c->blocks[b].rend(); ++it) c->free_blocks.push_back(*it);
+    c->blocks[b].clear();
+    c->total[b] = c->quantized[b] = c->last_flushed[b] = 0;
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_pool_state(const kvq_cache* c, int64_t* free_blocks, int64_t* pool_blocks) {
+  if (!c || !free_blocks || !pool_blocks) return fail(KVQ_EINVAL, "NULL argument");
+  *free_blocks = (int64_t)c->free_blocks.size();
+  *pool_blocks = c->pool_blocks;
+  return KVQ_OK;
 }
 
 kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, const kvq_unit_view* view,
@@ -757,7 +901,7 @@ kvq_status kvq_restore(const kvq_cache* c, int32_t seq_begin, int32_t n_seqs, vo
     p.eps = c->cfg.eps;
     p.geom = c->geom;
     p.pages = c->pages;
-    p.layout = c->layout;
+    p.map = page_map(c);
     p.ring_k = c->ring_k;
     p.ring_v = c->ring_v;
     p.in_dtype = c->cfg.dtype == KVQ_BF16 ? 0 : 1;

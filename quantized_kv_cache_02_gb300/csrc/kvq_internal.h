@@ -11,6 +11,9 @@ namespace kvq {
 constexpr int kMaxSeqsPerLaunch = 256;
 // Largest GQA group (query heads per KV head) the kernels handle.
 constexpr int kMaxGqa = 8;
+// New blocks one append launch of a paged cache may fill (their ids travel in
+// the parameter block).
+constexpr int kMaxNewBlocks = 4096;
 
 // Device status word codes (kvq_device_status).
 constexpr int32_t kStatusWaitTimeout = 0x101;  // a bounded mbarrier wait gave up
@@ -26,6 +29,24 @@ struct SeqLayout {
   int64_t page_base;    // byte offset of (seq, kv head 0, page 0) from the page region
   int64_t unit_stride;  // bytes between consecutive kv heads of the sequence
 };
+
+// Where the group pages live.  Contiguous cache: the pages of unit (b, h) lie
+// back to back from layout[b].page_base + h * layout[b].unit_stride.  Paged
+// cache ("KV Cache 与自回归视频生成" section 05, a block table per request):
+// a block holds one group of a sequence for every KV head (head h at
+// h * page_bytes, codes and scales together), and table[b * table_stride + j]
+// is the block of the sequence's group j.
+struct PageMap {
+  const SeqLayout* layout;
+  int32_t* table;              // null: contiguous
+  int32_t table_stride;        // table entries per sequence
+  int64_t block_bytes;         // n_kv_heads * page_bytes
+};
+
+__host__ __device__ inline int64_t page_offset(const PageMap& m, int64_t page_bytes, int b, int h, int64_t pg) {
+  if (m.table) return (int64_t)m.table[(int64_t)b * m.table_stride + pg] * m.block_bytes + (int64_t)h * page_bytes;
+  return m.layout[b].page_base + h * m.layout[b].unit_stride + pg * page_bytes;
+}
 
 // Geometry of a group page (see the layout comment in kvq.h).
 struct PageGeom {
@@ -59,8 +80,8 @@ struct AppendParams {
   int32_t D, Hkv, G, R, Rcap, qmax, bits;
   float eps;
   PageGeom geom;
-  uint8_t* pages;              // page region
-  const SeqLayout* layout;     // [batch]
+  uint8_t* pages;              // page region (contiguous) or block pool (paged)
+  PageMap map;
   void* ring_k;                // [batch][Hkv][Rcap][D] (dtype)
   void* ring_v;
   const void* new_k;           // [n_seqs][Hkv][n][D]
@@ -70,6 +91,10 @@ struct AppendParams {
   int32_t flush_blocks;        // grid.x slots for flush groups (0 if none in this launch)
   int32_t window_blocks;       // grid.x slots for window writes (0 or 1)
   SeqCounters old[kMaxSeqsPerLaunch];
+  // paged caches: the blocks of sequence i's new groups are
+  // blk_ids[blk_first[i] ..]; the flush writes them into the block table
+  int32_t blk_first[kMaxSeqsPerLaunch];
+  int32_t blk_ids[kMaxNewBlocks];
 };
 
 struct DecodeParams {
@@ -78,7 +103,7 @@ struct DecodeParams {
   float qk_scale;              // log2(e) / sqrt(D): scores are kept in base 2
   PageGeom geom;
   const uint8_t* pages;
-  const SeqLayout* layout;
+  PageMap map;
   const void* ring_k;
   const void* ring_v;
   const void* q;               // [batch][Hq][D]
@@ -136,14 +161,15 @@ struct RestoreParams {
   float eps;
   PageGeom geom;
   const uint8_t* pages;
-  const SeqLayout* layout;
+  PageMap map;
   const void* ring_k;          // cache dtype
   const void* ring_v;
   int32_t in_dtype, out_dtype; // 0 bf16, 1 fp32
   void* k_out;                 // [n_seqs][Hkv][t_stride][D] (out dtype)
   void* v_out;
   int64_t t_stride;
-  int32_t page_cols;           // grid columns for pages (the window column follows)
+  int32_t page_cols;           // pages of the longest unit (the launcher turns it into
+                               // columns of page runs; the window column follows)
   int32_t seq_begin, n_seqs;
   SeqCounters ctr[kMaxSeqsPerLaunch];
 };

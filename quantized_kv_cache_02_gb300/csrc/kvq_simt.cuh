@@ -142,11 +142,10 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
       simt_token<CPL>(s, qv, kv, vv, g);
     }
   } else {
-    const uint8_t* unit_pages = p.pages + p.layout[b].page_base + h * p.layout[b].unit_stride;
     const int64_t ntok = (int64_t)(pg1 - pg0) * G;
     for (int64_t tt = warp; tt < ntok; tt += kSimtWarps) {
       const int pg = pg0 + (int)(tt / G), tl = (int)(tt % G);
-      const uint8_t* page = unit_pages + (int64_t)pg * p.geom.page_bytes;
+      const uint8_t* page = p.pages + page_offset(p.map, p.geom.page_bytes, b, h, pg);
       const float* ks = reinterpret_cast<const float*>(page + p.geom.kscale_off);
       const float vs = reinterpret_cast<const float*>(page + p.geom.vscale_off)[tl];
 #pragma unroll

@@ -125,3 +125,18 @@ def test_restore_dense_and_compare_validate_before_any_launch():
     assert call(batch=70000) == kvq.binding.KVQ_EUNSUPPORTED
     assert lib.kvq_compare(None, ws, 1, 2, 32, 16, 0, 7, 1e-8, 0, ws, ctypes.byref(out), None) == kvq.binding.KVQ_EINVAL
     assert lib.kvq_compare(ws, ws, 1, 2, 32, 16, 0, 7, 1e-8, 0, ws, None, None) == kvq.binding.KVQ_EINVAL
+
+
+def test_paged_sizes_and_validation():
+    cfg = kvq.make_config(2, 8, 32, 128, 128, 32, 7)
+    small = kvq.binding.kvq_required_bytes_paged(cfg, [4096, 4096], 10)
+    big = kvq.binding.kvq_required_bytes_paged(cfg, [4096, 4096], 1000)
+    # the pool grows by whole blocks: n_kv_heads group pages each
+    assert big - small >= 990 * 8 * kvq.kvq_page_bytes(cfg) - 256
+    with pytest.raises(kvq.KVQError) as e:
+        kvq.binding.kvq_required_bytes_paged(cfg, [4096, 4096], 0)
+    assert e.value.status == kvq.binding.KVQ_EINVAL
+    lib = kvq.load_library()
+    assert lib.kvq_release(None, 0, 1) == kvq.binding.KVQ_EINVAL
+    free, total = ctypes.c_int64(), ctypes.c_int64()
+    assert lib.kvq_pool_state(None, ctypes.byref(free), ctypes.byref(total)) == kvq.binding.KVQ_EINVAL
