@@ -41,13 +41,13 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 # algorithmic bytes (what the step has to move by definition)
 # ---------------------------------------------------------------------------
 
-def split_bytes(quantized, window, w):
+def split_bytes(quantized, window, w, bits=4):
     """Bytes the split kernel of one layer reads: codes and fp32 scales of the
     quantized prefix, the bf16 window, and q; summed over sequences."""
     D, G, H, g = w["head_dim"], w["group"], w["n_kv_heads"], w["n_q_heads"] // w["n_kv_heads"]
     total = 0
     for Q, W in zip(quantized, window):
-        per_unit = Q * (D + 4 * D / G + 4) + W * 2 * D * 2 + g * D * 2
+        per_unit = Q * (2 * D * bits / 8 + 4 * D / G + 4) + W * 2 * D * 2 + g * D * 2
         total += H * per_unit
     return total
 
@@ -209,7 +209,54 @@ def load_traffic():
     return t.get("dram_bytes_per_launch_full_size")
 
 
-def foil_layer(torch, cache, q, w, B, H, D, stream, iters=20):
+def variants_layer(torch, kvq, w, dev, peak, steps=20):
+    """One layer of the benchmark shape in the cache's other forms, after the
+    same prefill as the main run: 2-bit codes (qmax 1) and a paged 4-bit cache
+    whose blocks interleave across sequences (prefilled in 8 rounds of chunks).
+    Each decode (split + combine) is timed; the split kernel alone with CUDA
+    events around it, as for the main roofline."""
+    B, H, Hq, D, R, G = w["batch"], w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["residual_len"], w["group"]
+    T0 = w["context"]
+    cap = T0 + 8
+    q = dev.q_block(0, 0, B, 0)
+    out = {}
+    for name, qmax, paged in (("two_bit", 1, False), ("paged_4bit", 7, True)):
+        pool = B * (cap // G) if paged else 0
+        cache = kvq.KVQCache(B, H, Hq, D, R, G, qmax, cap, pool_blocks=pool)
+        if paged:
+            chunk = T0 // 8
+            for r in range(8):
+                n = chunk if r < 7 else T0 - 7 * chunk
+                for b in range(B):
+                    K, V = dev.kv_block(0, b, 1, r * chunk, n)
+                    cache.append(K, V, b)
+        else:
+            K, V = dev.kv_block(0, 0, B, 0, T0)
+            cache.append(K, V, 0)
+            del K, V
+        o = torch.empty(B, Hq, D, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            cache.decode_attention(q, out=o)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:  # torch creates the CUDA event on first record
+            e0.record()
+            e1.record()
+        torch.cuda.synchronize()
+        for e0, e1 in evs:
+            cache.decode_attention(q, out=o, split_start=e0.cuda_event, split_stop=e1.cuda_event)
+        torch.cuda.synchronize()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) / steps
+        st = [cache.seq_state(b) for b in range(B)]
+        nbytes = split_bytes([x["quantized"] for x in st], [x["window"] for x in st], w,
+                             bits=2 if qmax <= 1 else 4)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"split_ms": round(ms, 5), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                     "algorithmic_bytes_per_launch": int(nbytes), "status": cache.device_status()}
+        del cache
+    return out
+
+
+def foil_layer(torch, cache, q, w, B, H, D, stream, peak, iters=20):
     """The read path the fused kernel replaces, on one layer's cache as it
     stands: kvq_restore to dense bf16 tensors, then the dense bf16 decode
     attention, against the fused decode (split + combine) of the same cache.
@@ -245,7 +292,10 @@ def foil_layer(torch, cache, q, w, B, H, D, stream, iters=20):
                     "attention (kvq_dense_decode_attention), vs the fused decode (split + combine) on the same cache",
             "restore_ms": round(r_ms, 5), "restore_gbs": round(restore_bytes / (r_ms / 1e3) / 1e9, 1),
             "dense_attention_ms": round(d_ms, 5), "dense_attention_gbs": round(dense_bytes / (d_ms / 1e3) / 1e9, 1),
-            "fused_ms": round(f_ms, 5), "foil_over_fused": round((r_ms + d_ms) / f_ms, 2)}
+            "fused_ms": round(f_ms, 5), "foil_over_fused": round((r_ms + d_ms) / f_ms, 2),
+            "foil_floor_over_fused": round((restore_bytes + dense_bytes) / (peak * 1e9) * 1e3 / f_ms, 2),
+            "note": "foil_floor = the foil's bytes at the measured HBM peak: what an ideal dequantize-to-HBM "
+                    "path would cost"}
 
 
 def run_ours(args):
@@ -443,8 +493,18 @@ def run_ours(args):
     d2h = int(d2h)
     assert np.isfinite(host_out[0].numpy()).all()
 
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     # ---- foil: dequantize to HBM, then standard attention (one layer) --------
-    foil = foil_layer(torch, caches[0], qs[0][0], w, B, H, D, stream) if not args.no_foil else None
+    foil = foil_layer(torch, caches[0], qs[0][0], w, B, H, D, stream, peak) if not args.no_foil else None
+    # ---- the 2-bit and paged forms of one layer -----------------------------
+    variants = variants_layer(torch, kvq, w, dev, peak) if not args.no_variants else None
 
     # ---- reduce over ranks: bytes summed, time of the slowest rank ----------
     pg = dist if world > 1 else None
@@ -455,14 +515,6 @@ def run_ours(args):
     e2e_value = e2e_total / (e2e_max / 1e3) / 1e9
     split_avg_ms = sum(split_ms) / len(split_ms)
     achieved = (sum(split_b) / len(split_b)) / (split_avg_ms / 1e3) / 1e9
-    peaks = {}
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            peaks = json.load(f)
-    except (OSError, ValueError):
-        pass
-    peak = peaks.get("hbm_gbs", 6800.0)
-    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -502,6 +554,7 @@ def run_ours(args):
                 "context_mean": T0 + W + K + (n_e2e - 1) / 2 + 1},
         "gpu_launches": int(launches),
         "foil": foil,
+        "variants": variants,
         "device_status": int(status),
     }
     if not args.no_cpu_baseline:
@@ -545,6 +598,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-foil", action="store_true", help="skip the dequantize-to-HBM foil measurement")
+    ap.add_argument("--no-variants", action="store_true", help="skip the 2-bit and paged one-layer measurements")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; 0 = all 32)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
