@@ -253,7 +253,61 @@ def variants_layer(torch, kvq, w, dev, peak, steps=20):
         out[name] = {"split_ms": round(ms, 5), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                      "algorithmic_bytes_per_launch": int(nbytes), "status": cache.device_status()}
         del cache
+    out["long_video"] = long_video_layer(torch, kvq, peak)
     return out
+
+
+LONG_VIDEO = dict(n_kv_heads=8, n_q_heads=32, head_dim=128, residual_len=256, group=128, qmax=7, chunk=14400,
+                  chunks=30, decode_steps=64, seed=4)
+
+
+def long_video_layer(torch, kvq, peak):
+    """The long-video workload on one layer: batch 1, 432000 tokens appended
+    as 30 chunks of 14400 (each append quantizes and packs its flushed groups),
+    then 64 decode steps of one token each with attention over the whole
+    cache.  Reports the flush throughput in bf16 bytes consumed per second and
+    the decode's split kernel against HBM."""
+    from kvq_inputs.device import DeviceInputs
+    from kvq_inputs.gen import InputSpec
+    v = LONG_VIDEO
+    H, Hq, D, R, G = v["n_kv_heads"], v["n_q_heads"], v["head_dim"], v["residual_len"], v["group"]
+    T = v["chunk"] * v["chunks"]
+    dev = DeviceInputs(InputSpec(seed=v["seed"], n_kv_heads=H, n_q_heads=Hq, head_dim=D))
+    cache = kvq.KVQCache(1, H, Hq, D, R, G, v["qmax"], T + v["decode_steps"] + 8)
+    chunks = [dev.kv_block(0, 0, 1, c * v["chunk"], v["chunk"]) for c in range(v["chunks"])]
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for K, V in chunks:
+        cache.append(K, V, 0)
+    e1.record()
+    torch.cuda.synchronize()
+    prefill_ms = e0.elapsed_time(e1)
+    consumed = T * H * D * 2 * 2
+    del chunks
+    steps = [dev.kv_block(0, 0, 1, T + s, 1) for s in range(v["decode_steps"])]
+    qs = [dev.q_block(0, 0, 1, s) for s in range(v["decode_steps"])]
+    o = torch.empty(1, Hq, D, dtype=torch.float32, device="cuda")
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in steps]
+    for a, b in evs:  # torch creates the CUDA event on first record
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    for s, ((K, V), q) in enumerate(zip(steps, qs)):
+        cache.append(K, V, 0)
+        a, b = evs[s]
+        cache.decode_attention(q, out=o, split_start=a.cuda_event, split_stop=b.cuda_event)
+    torch.cuda.synchronize()
+    split_ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+    st = cache.seq_state(0)
+    w = dict(head_dim=D, group=G, n_kv_heads=H, n_q_heads=Hq)
+    nbytes = split_bytes([st["quantized"]], [st["window"]], w)
+    return {"workload": "long video: 432000 tokens as 30 appends of 14400, R 256, G 128, 4-bit, 8 KV heads",
+            "prefill_ms": round(prefill_ms, 3), "prefill_consumed_gbs": round(consumed / (prefill_ms / 1e3) / 1e9, 1),
+            "decode_split_ms": round(split_ms, 5),
+            "decode_split_gbs": round(nbytes / (split_ms / 1e3) / 1e9, 1),
+            "decode_frac": round(nbytes / (split_ms / 1e3) / 1e9 / peak, 4),
+            "decode_bytes_per_launch": int(nbytes), "status": cache.device_status()}
 
 
 def foil_layer(torch, cache, q, w, B, H, D, stream, peak, iters=20):

@@ -22,7 +22,6 @@
 namespace kvq {
 namespace {
 
-constexpr int kAppendThreads = 256;
 
 __device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
   float r = rintf(__fmul_rn(x, scale));
@@ -49,20 +48,37 @@ __device__ __forceinline__ void store_f32(float* dst, const uint4& raw, __nv_bfl
 }
 
 // Stage the G x D tile of tokens [t_first, t_first + G) as fp32 in shared
-// memory, 16 bytes per load.  Tokens below T0 come from the ring: a group
-// starts at a multiple of G and the ring length is a multiple of G, so its
-// rows are contiguous there.  Later tokens come from the input.
+// memory, 16 bytes per load and four loads in flight per thread.  Tokens below
+// T0 come from the ring: a group starts at a multiple of G and the ring length
+// is a multiple of G, so its rows are contiguous there.  Later tokens come from
+// the input.  Each thread keeps one 16-byte column and steps over rows, so no
+// index is divided inside the loop.
 template <typename T>
 __device__ void load_group(float* tile, const T* ring, const T* input, int t_first, int T0, int G, int D,
                            int Rcap) {
   constexpr int kVec = 16 / sizeof(T);
+  constexpr int kBatch = 4;
   const int per_row = D / kVec;
+  const int rows_per_pass = blockDim.x / per_row;
+  if ((int)threadIdx.x >= rows_per_pass * per_row) return;
+  const int r0 = threadIdx.x / per_row, c = (threadIdx.x - r0 * per_row) * kVec;
   const int ring_row0 = t_first % Rcap;
-  for (int idx = threadIdx.x; idx < G * per_row; idx += blockDim.x) {
-    const int tl = idx / per_row, c = (idx - tl * per_row) * kVec;
-    const int t = t_first + tl;
-    const T* src = t < T0 ? ring + (size_t)(ring_row0 + tl) * D + c : input + (size_t)(t - T0) * D + c;
-    store_f32(tile + tl * D + c, *reinterpret_cast<const uint4*>(src), T());
+  for (int tl = r0; tl < G; tl += kBatch * rows_per_pass) {
+    uint4 v[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int r = tl + k * rows_per_pass;
+      if (r < G) {
+        const int t = t_first + r;
+        const T* src = t < T0 ? ring + (size_t)(ring_row0 + r) * D + c : input + (size_t)(t - T0) * D + c;
+        v[k] = *reinterpret_cast<const uint4*>(src);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int r = tl + k * rows_per_pass;
+      if (r < G) store_f32(tile + r * D + c, v[k], T());
+    }
   }
 }
 
@@ -90,18 +106,40 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 
   if ((int)blockIdx.x >= p.flush_blocks) {
     // Window block: the new tokens that stay in the residual window, copied
-    // 16 bytes at a time.
+    // 16 bytes at a time, four rows in flight per thread; each thread keeps
+    // one column and advances its ring row without a division.
     constexpr int kVec = 16 / sizeof(T);
+    constexpr int kBatch = 4;
     const int per_row = D / kVec;
+    const int rows_per_pass = blockDim.x / per_row;
+    if ((int)threadIdx.x >= rows_per_pass * per_row) return;
+    const int r0 = threadIdx.x / per_row, c = (threadIdx.x - r0 * per_row) * kVec;
     const int t_lo = Q1 > T0 ? Q1 : T0;
-    const int count = (T1 - t_lo) * per_row;
-    for (int idx = threadIdx.x; idx < count; idx += blockDim.x) {
-      const int r = idx / per_row, c = (idx - r * per_row) * kVec;
-      const int t = t_lo + r;
-      const size_t src = (size_t)(t - T0) * D + c;
-      const size_t dst = (size_t)(t % Rcap) * D + c;
-      *reinterpret_cast<uint4*>(ring_k + dst) = *reinterpret_cast<const uint4*>(in_k + src);
-      *reinterpret_cast<uint4*>(ring_v + dst) = *reinterpret_cast<const uint4*>(in_v + src);
+    const int rows = T1 - t_lo;
+    int ring_row = (t_lo + r0) % Rcap;
+    const int step = rows_per_pass % Rcap;
+    for (int r = r0; r < rows; r += kBatch * rows_per_pass) {
+      uint4 kv[kBatch], vv[kBatch];
+      int dst[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int rr = r + k * rows_per_pass;
+        dst[k] = ring_row;
+        ring_row += step;
+        if (ring_row >= Rcap) ring_row -= Rcap;
+        if (rr < rows) {
+          const size_t src = (size_t)(t_lo + rr - T0) * D + c;
+          kv[k] = *reinterpret_cast<const uint4*>(in_k + src);
+          vv[k] = *reinterpret_cast<const uint4*>(in_v + src);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        if (r + k * rows_per_pass < rows) {
+          *reinterpret_cast<uint4*>(ring_k + (size_t)dst[k] * D + c) = kv[k];
+          *reinterpret_cast<uint4*>(ring_v + (size_t)dst[k] * D + c) = vv[k];
+        }
+      }
     }
     return;
   }
@@ -129,34 +167,63 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   // ---- Key: per-channel absmax over the group's tokens --------------------
   load_group<T>(tile, ring_k, in_k, t_first, T0, G, D, Rcap);
   __syncthreads();
-  for (int c = threadIdx.x; c < D; c += blockDim.x) {
-    float a = 0.f;
-    for (int t = 0; t < G; ++t) a = fmaxf(a, fabsf(tile[t * D + c]));
-    sK[c] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+  {
+    // every thread takes one channel over a share of the tokens (four
+    // independent max chains), then the shares of a channel are merged
+    const int parts = blockDim.x / D > 0 ? blockDim.x / D : 1;
+    float* part_max = sV + G;  // [parts][D] (parts * D <= max(blockDim, D) floats)
+    for (int c0 = 0; c0 < D; c0 += blockDim.x) {
+      const int c = c0 + (int)threadIdx.x % D, part = (int)threadIdx.x / D;
+      if (c < D && part < parts) {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        int t = part;
+        for (; t + 3 * parts < G; t += 4 * parts) {
+          a0 = fmaxf(a0, fabsf(tile[t * D + c]));
+          a1 = fmaxf(a1, fabsf(tile[(t + parts) * D + c]));
+          a2 = fmaxf(a2, fabsf(tile[(t + 2 * parts) * D + c]));
+          a3 = fmaxf(a3, fabsf(tile[(t + 3 * parts) * D + c]));
+        }
+        for (; t < G; t += parts) a0 = fmaxf(a0, fabsf(tile[t * D + c]));
+        part_max[part * D + c] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      }
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+      float a = 0.f;
+      for (int k = 0; k < parts; ++k) a = fmaxf(a, part_max[k * D + c]);
+      sK[c] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+    }
   }
   __syncthreads();
   {
-    // rows of D*BITS/8 bytes, written as 32-bit words
+    // rows of D*BITS/8 bytes, written as 32-bit words; each thread keeps one
+    // word column and steps over the token rows
     constexpr int kPerWord = 32 / BITS;  // codes per 32-bit word
     const int words_per_row = D / kPerWord;
+    const int rows_per_pass = blockDim.x / words_per_row;
     uint32_t* kc = reinterpret_cast<uint32_t*>(page);
-    for (int idx = threadIdx.x; idx < G * words_per_row; idx += blockDim.x) {
-      const int t = idx / words_per_row, w = idx - t * words_per_row;
+    if ((int)threadIdx.x < rows_per_pass * words_per_row) {
+      const int t0 = threadIdx.x / words_per_row, w = threadIdx.x - t0 * words_per_row;
       // the word's channels as float4 reads (consecutive threads, consecutive addresses)
-      const float4* src = reinterpret_cast<const float4*>(tile + t * D + w * kPerWord);
       const float4* sc = reinterpret_cast<const float4*>(sK + w * kPerWord);
-      uint32_t word = 0;
+      float4 s4[kPerWord / 4];
 #pragma unroll
-      for (int k4 = 0; k4 < kPerWord / 4; ++k4) {
-        const float4 x = src[k4], s4 = sc[k4];
-        const int c0 = quantize_one(x.x, s4.x, qmax), c1 = quantize_one(x.y, s4.y, qmax);
-        const int c2 = quantize_one(x.z, s4.z, qmax), c3 = quantize_one(x.w, s4.w, qmax);
-        word |= ((uint32_t)(c0 + kBias)) << (BITS * (4 * k4 + 0));
-        word |= ((uint32_t)(c1 + kBias)) << (BITS * (4 * k4 + 1));
-        word |= ((uint32_t)(c2 + kBias)) << (BITS * (4 * k4 + 2));
-        word |= ((uint32_t)(c3 + kBias)) << (BITS * (4 * k4 + 3));
+      for (int k4 = 0; k4 < kPerWord / 4; ++k4) s4[k4] = sc[k4];
+      for (int t = t0; t < G; t += rows_per_pass) {
+        const float4* src = reinterpret_cast<const float4*>(tile + t * D + w * kPerWord);
+        uint32_t word = 0;
+#pragma unroll
+        for (int k4 = 0; k4 < kPerWord / 4; ++k4) {
+          const float4 x = src[k4];
+          const int c0 = quantize_one(x.x, s4[k4].x, qmax), c1 = quantize_one(x.y, s4[k4].y, qmax);
+          const int c2 = quantize_one(x.z, s4[k4].z, qmax), c3 = quantize_one(x.w, s4[k4].w, qmax);
+          word |= ((uint32_t)(c0 + kBias)) << (BITS * (4 * k4 + 0));
+          word |= ((uint32_t)(c1 + kBias)) << (BITS * (4 * k4 + 1));
+          word |= ((uint32_t)(c2 + kBias)) << (BITS * (4 * k4 + 2));
+          word |= ((uint32_t)(c3 + kBias)) << (BITS * (4 * k4 + 3));
+        }
+        kc[t * words_per_row + w] = word;
       }
-      kc[idx] = word;
     }
     float* ks = reinterpret_cast<float*>(page + geom.kscale_off);
     for (int c = threadIdx.x; c < D; c += blockDim.x) ks[c] = sK[c];
@@ -175,52 +242,57 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   }
   __syncthreads();
   {
+    // channel fastest across threads (each token row is read at consecutive
+    // addresses); each thread keeps one channel and steps over the words
     uint8_t* vbase = page + geom.code_bytes;
     const int n_sub = (G + 31) / 32;
+    const int per_pass = blockDim.x / D > 0 ? blockDim.x / D : 1;  // words of a channel per pass
+    const bool active = (int)threadIdx.x < per_pass * D;
+    const int c_me = (int)threadIdx.x % D, w_me = (int)threadIdx.x / D;
     for (int st = 0; st < n_sub; ++st) {
       const int n_st = min(32, G - 32 * st);
       uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
-      if (BITS == 2) {
-        // 16-bit pieces of 8 tokens: even tokens in the low byte, odd in the high
-        const int np = n_st / 8;  // pieces per channel row
-        uint16_t* vp = reinterpret_cast<uint16_t*>(vc);
-        for (int idx = threadIdx.x; idx < D * np; idx += blockDim.x) {
-          const int w = idx / D, c = idx - w * D;
-          uint32_t piece = 0;
+      for (int c0 = 0; c0 < D && active; c0 += blockDim.x) {
+        const int c = c0 + c_me;
+        if (c >= D) break;
+        if (BITS == 2) {
+          // 16-bit pieces of 8 tokens: even tokens in the low byte, odd in the high
+          const int np = n_st / 8;  // pieces per channel row
+          uint16_t* vp = reinterpret_cast<uint16_t*>(vc);
+          for (int w = w_me; w < np; w += per_pass) {
+            uint32_t piece = 0;
 #pragma unroll
-          for (int f = 0; f < 4; ++f) {
-            const int te = 32 * st + 8 * w + 2 * f;
-            piece |= ((uint32_t)(quantize_one(tile[te * D + c], sV[te], qmax) + kBias)) << (2 * f);
-            piece |= ((uint32_t)(quantize_one(tile[(te + 1) * D + c], sV[te + 1], qmax) + kBias)) << (8 + 2 * f);
+            for (int f = 0; f < 4; ++f) {
+              const int te = 32 * st + 8 * w + 2 * f;
+              piece |= ((uint32_t)(quantize_one(tile[te * D + c], sV[te], qmax) + kBias)) << (2 * f);
+              piece |= ((uint32_t)(quantize_one(tile[(te + 1) * D + c], sV[te + 1], qmax) + kBias)) << (8 + 2 * f);
+            }
+            vp[c * np + w] = (uint16_t)piece;
           }
-          vp[c * np + w] = (uint16_t)piece;
-        }
-      } else if (BITS == 4) {
-        const int nw = n_st / 8;  // words per channel row
-        // channel fastest across threads: each token row is read at consecutive addresses
-        for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
-          const int w = idx / D, c = idx - w * D;
-          uint32_t word = 0;
+        } else if (BITS == 4) {
+          const int nw = n_st / 8;  // words per channel row
+          for (int w = w_me; w < nw; w += per_pass) {
+            uint32_t word = 0;
 #pragma unroll
-          for (int jn = 0; jn < 8; ++jn) {
-            const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
-            const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
-            word |= ((uint32_t)(code + kBias)) << (4 * jn);
+            for (int jn = 0; jn < 8; ++jn) {
+              const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
+              const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
+              word |= ((uint32_t)(code + kBias)) << (4 * jn);
+            }
+            vc[c * nw + w] = word;
           }
-          vc[c * nw + w] = word;
-        }
-      } else {
-        const int nw = n_st / 4;
-        for (int idx = threadIdx.x; idx < D * nw; idx += blockDim.x) {
-          const int w = idx / D, c = idx - w * D;
-          uint32_t word = 0;
+        } else {
+          const int nw = n_st / 4;
+          for (int w = w_me; w < nw; w += per_pass) {
+            uint32_t word = 0;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int tok = 32 * st + 4 * w + k;
-            const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
-            word |= ((uint32_t)(code + kBias)) << (8 * k);
+            for (int k = 0; k < 4; ++k) {
+              const int tok = 32 * st + 4 * w + k;
+              const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
+              word |= ((uint32_t)(code + kBias)) << (8 * k);
+            }
+            vc[c * nw + w] = word;
           }
-          vc[c * nw + w] = word;
         }
       }
     }
@@ -304,7 +376,7 @@ __global__ void __launch_bounds__(kCompareThreads) compare_kernel(const CompareP
 template <typename T, int BITS>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
   const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
-  const size_t smem = p.flush_blocks ? ((size_t)p.G * p.D + p.D + p.G) * sizeof(float) : 0;
+  const size_t smem = p.flush_blocks ? flush_smem_bytes(p.G, p.D) : 0;
   return launch_pdl(append_kernel<T, BITS>, grid, dim3(kAppendThreads), smem, s, p);
 }
 

@@ -76,6 +76,14 @@ __host__ __device__ inline int64_t flush_groups(int64_t w, int64_t n, int64_t R,
   return tail < R + G ? 0 : (tail - R) / G;
 }
 
+// Shared memory of a flush CTA: the G x D fp32 tile, the Key and Value
+// scales, and the per-thread partial maxima of the Key absmax.
+constexpr int kAppendThreads = 256;
+inline size_t flush_smem_bytes(int G, int D) {
+  const int partials = D > kAppendThreads ? D : kAppendThreads;
+  return ((size_t)G * D + D + G + partials) * sizeof(float);
+}
+
 struct AppendParams {
   int32_t D, Hkv, G, R, Rcap, qmax, bits;
   float eps;
