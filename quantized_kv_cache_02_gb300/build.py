@@ -22,7 +22,8 @@ NVCC = os.path.join(CUDA_HOME, "bin", "nvcc") if os.path.exists(os.path.join(CUD
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", os.path.join(ROOT, "include")]
 LDFLAGS = ARCH + ["-shared", "-cudart", "shared", f"-Xlinker=-rpath={CUDA_HOME}/lib64"]
 
-SOURCES = ["kvq_host.cu", "kvq_append.cu", "kvq_decode_simt.cu", "kvq_decode_mma.cu", "kvq_restore.cu"]
+SOURCES = ["kvq_host.cu", "kvq_append.cu", "kvq_decode_simt.cu", "kvq_decode_mma.cu", "kvq_decode_mma_b2.cu",
+           "kvq_decode_mma_b4.cu", "kvq_decode_mma_b8.cu", "kvq_restore.cu"]
 
 
 def _run(cmd):

@@ -1,1085 +1,11 @@
-// Tensor-core split kernel of the decode attention over the quantized prefix.
-//
-// Work item: a run of group pages of one (sequence, KV head) unit; the CTA's
-// warps take pages round robin, each warp streaming its pages through its own
-// ring of shared-memory slots with cp.async.bulk (the TMA engine) and one
-// mbarrier per slot, so no warp ever waits on another.  All waits are bounded:
-// a wait that gives up sets the device status word and the warp stops.
-//
-// Per 32-token sub-tile the warp computes, for the g <= 8 query heads of the
-// KV head (GQA: they share every K/V tile):
-//   S[t][h] = sum_c code_K[t][c] * (q[h][c] / sK[c]) * log2(e)/sqrt(d)
-//   online softmax in base 2 (running max m, sum l)
-//   O^T[c][h] += sum_t code_V[t][c] * (p[h][t] / sV[t])
-// which is q.k/sqrt(d) and p.v over restored values k = code/sK, v = code/sV
-// ("KV Cache Quantization Strategies", restore; "KV Cache 与自回归视频生成"
-// 3.1 and attn_step) with both scales folded into the f16 MMA operand that
-// is not the code (q/sK as an f16 hi + lo pair, p/sV as one f16).  Codes
-// enter the MMA as f16 subnormals cut straight out of the stored word (see
-// "codes as f16 subnormals" below); the bias and the 2^-24 are undone once per
-// page for S and once per run for O.
-// Matrix shapes: S = A(K codes: 16 tokens x 16 channels) * B(q: 16 x 8 heads),
-// O^T = A(V codes^T: 16 channels x 16 tokens) * B(P^T: 16 tokens x 8 heads);
-// P goes from the S accumulator layout to the B layout with movmatrix.trans.
-// Token and channel orders inside a k-step are permuted to match the packed
-// byte layout; both operands of every MMA use the same permutation.
+// Tensor-core decode: the host-facing launchers.  The kernels live in
+// kvq_decode_mma.cuh; the split kernel's instantiations are compiled one code
+// width per translation unit (kvq_decode_mma_b2.cu, _b4.cu, _b8.cu) so that
+// they build in parallel.
 
-#include <cuda_bf16.h>
-#include <cuda_fp16.h>
-
-#include "kvq_simt.cuh"
+#include "kvq_decode_mma.cuh"
 
 namespace kvq {
-namespace {
-
-constexpr int kMmaWarps = 4;
-constexpr int kMmaThreads = kMmaWarps * 32;
-constexpr uint32_t kSpinLimit = 1u << 24;
-
-// ---- PTX helpers -----------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
-// Bounded wait on phase ``parity`` of an mbarrier; false if it gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t it = 0; it < kSpinLimit; ++it) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                         uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t transpose8x8(uint32_t x) {
-  uint32_t y;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// ---- codes as f16 subnormals --------------------------------------------
-// A stored code is offset binary: u = code + bias (bias 8 for 4-bit, 128 for
-// 8-bit), u in [1, 2*bias).  A 16-bit half whose bits are just u (exponent 0)
-// is the binary16 subnormal u * 2^-24, exactly; u << 4 is 16 * u * 2^-24.  So
-// masking the stored word yields MMA operands without any floating-point
-// conversion; the 2^-24, the x16 of the second nibble position (cancelled by a
-// 1/16 on the matching B rows) and the bias are undone after the MMA:
-// S = 2^24 * S' - bias * sum(B),  O = 2^24 * O' - bias * sum(p').
-
-// 4-bit: word of eight nibbles -> r[j] = (nibble j, nibble j + 4) as f16x2;
-// r[1] and r[3] carry an extra factor 16.
-__device__ __forceinline__ void nibble_regs(uint32_t w, uint32_t (&r)[4]) {
-  const uint32_t w2 = w >> 8;
-  r[0] = w & 0x000F000Fu;
-  r[1] = w & 0x00F000F0u;
-  r[2] = w2 & 0x000F000Fu;
-  r[3] = w2 & 0x00F000F0u;
-}
-
-// 2-bit: word of sixteen 2-bit fields (four per byte) -> r[j] = (field j of
-// byte 0, field j of byte 2), r[4 + j] = (field j of byte 1, of byte 3), each
-// carrying a factor 4^j.
-__device__ __forceinline__ void crumb_regs(uint32_t w, uint32_t (&r)[8]) {
-  const uint32_t w2 = w >> 8;
-  r[0] = w & 0x00030003u;
-  r[1] = w & 0x000C000Cu;
-  r[2] = w & 0x00300030u;
-  r[3] = w & 0x00C000C0u;
-  r[4] = w2 & 0x00030003u;
-  r[5] = w2 & 0x000C000Cu;
-  r[6] = w2 & 0x00300030u;
-  r[7] = w2 & 0x00C000C0u;
-}
-
-// 2-bit registers hold u * 4^j * 2^-24 with u = code + 2; subtracting
-// 2 * 4^j * 2^-24 (f16 subnormal arithmetic on small integers is exact) leaves
-// code * 4^j * 2^-24.  With codes of -1..1 and per-group absmax scales, a
-// channel holding one huge outlier adds 2 * q / sK to every token's biased
-// score, and the fp32 accumulation of that term would cost more precision
-// than the subtraction here.
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-__device__ __forceinline__ void unbias_crumbs(uint32_t (&r)[8]) {
-#pragma unroll
-  for (int m = 0; m < 8; ++m) r[m] = hsub2(r[m], 0x00020002u << (2 * (m & 3)));
-}
-
-// 2-bit Value piece (16 bits: even tokens of an 8-token span in the low byte,
-// odd tokens in the high byte) -> r[j] = (token 2j, token 2j + 1), factor 4^j.
-__device__ __forceinline__ void piece_regs(uint32_t piece, uint32_t (&r)[4]) {
-  const uint32_t x = __byte_perm(piece, 0u, 0x4140);  // bytes (b0, 0, b1, 0)
-  r[0] = x & 0x00030003u;
-  r[1] = x & 0x000C000Cu;
-  r[2] = x & 0x00300030u;
-  r[3] = x & 0x00C000C0u;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) r[j] = hsub2(r[j], 0x00020002u << (2 * j));
-}
-
-// 8-bit: word of four bytes -> r[0] = (byte 0, byte 2), r[1] = (byte 1, byte 3).
-__device__ __forceinline__ void byte_regs(uint32_t w, uint32_t (&r)[2]) {
-  r[0] = w & 0x00FF00FFu;
-  r[1] = (w >> 8) & 0x00FF00FFu;
-}
-
-__device__ __forceinline__ float fast_rcp(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t addr) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-
-// 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-template <int N>
-__device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[N]) {
-  static_assert(N == 1 || N % 2 == 0, "word count");
-  if constexpr (N == 1) {
-    w[0] = *reinterpret_cast<const uint32_t*>(p);
-  } else if constexpr (N % 4 == 0) {
-#pragma unroll
-    for (int i = 0; i < N / 4; ++i) {
-      const uint4 v = reinterpret_cast<const uint4*>(p)[i];
-      w[4 * i] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < N / 2; ++i) {
-      const uint2 v = reinterpret_cast<const uint2*>(p)[i];
-      w[2 * i] = v.x;
-      w[2 * i + 1] = v.y;
-    }
-  }
-}
-
-// GP = query heads per KV head rounded up to 2, 4 or 8.  The MMA's 8 columns
-// hold GP heads of each of PB = 8 / GP pages, so one B operand (q / sK) and one
-// softmax update serve PB pages ("streams"); column n belongs to stream n / GP.
-template <int D, int BITS, int GP>
-struct Shape {
-  static constexpr int PB = 8 / GP;
-  static constexpr int kSteps = D / 16;          // k-steps of the S MMA, m-tiles of the O MMA
-  static constexpr int kRowBytes = D * BITS / 8;
-  static constexpr int kWords = kRowBytes / 16;  // 32-bit words of a K row per thread
-  static constexpr int kChan = D / 4;            // channels of a K row per thread
-  static constexpr int kSubBytes = 32 * D * BITS / 8;
-  static constexpr int kChunks = D / 4;          // float4 chunks of a page's Key scales
-  static constexpr float kBias = BITS == 2 ? 2.f : BITS == 4 ? 8.f : 128.f;
-  // 2-bit: the B operand carries 16 * 4^-j for a code in field j, so that no
-  // q / sK term drops into the f16 subnormals; S is divided by it afterwards
-  static constexpr float kBScale = BITS == 2 ? 16.f : 1.f;
-};
-
-// Channel (in the thread's slice) of element e of k-step kk's B operand:
-// e = 0, 1 -> register 0 (k-slots 2tig, 2tig+1); e = 2, 3 -> register 1.
-// 2-bit: k-step kk = 4i + s takes registers R[2s] (a0) and R[2s + 1] (a2) of
-// word i, R as crumb_regs returns them.
-template <int BITS>
-__device__ __forceinline__ constexpr int kslot_channel(int kk, int e) {
-  if (BITS == 2) {
-    const int m = 2 * (kk & 3) + (e >> 1);
-    return 16 * (kk >> 2) + 4 * (m >> 2) + (m & 3) + 8 * (e & 1);
-  }
-  return BITS == 4 ? 8 * (kk >> 1) + 2 * (kk & 1) + (e == 0 ? 0 : e == 1 ? 4 : e == 2 ? 1 : 5)
-                   : 4 * kk + (e == 0 ? 0 : e == 1 ? 2 : e == 2 ? 1 : 3);
-}
-
-// Token row (inside a 32-token sub-tile) of S rows gid (r0) and gid + 8 (r1)
-// of m-block mb; these orders match how the conversions pair tokens.
-template <int BITS>
-__device__ __forceinline__ int token_row0(int gid, int mb) {
-  return BITS <= 4 ? 8 * (gid >> 1) + 4 * mb + (gid & 1) : 8 * (gid >> 1) + 4 * mb + 2 * (gid & 1);
-}
-template <int BITS>
-__device__ __forceinline__ constexpr int token_row_gap() {
-  return BITS <= 4 ? 2 : 1;
-}
-
-template <int D>
-struct WarpState {
-  float O[D / 16][4];  // O'^T accumulators (biased codes, scaled by 2^-24)
-  float C[4];          // 2^-24 * sum of the p / sV each column fed to O' (for the bias)
-  float m0, m1;        // running max of the thread's two columns (base 2)
-  float l0, l1;        // running sum of p (partial over this thread's rows)
-};
-
-// A group of PB pages (FULL) or of npages < PB pages (the tail of a warp's
-// run), already in shared memory.
-template <int D, int BITS, int GP, bool FULL>
-__device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BITS, GP>::PB], int npages_rt,
-                                          const PageGeom& geom, int G, const float4* q4, float* rsc, int lane,
-                                          int gid, int tig, WarpState<D>& st) {
-  using S = Shape<D, BITS, GP>;
-  constexpr float kTwo24 = 16777216.f;
-  const int npages = FULL ? S::PB : npages_rt;
-  // ---- reciprocal Key scales, cooperatively, in a bank-friendly order -------
-  // chunk i (channels tig*kChan + 4i .. +3) of slice tig goes to float4 slot
-  // i*4 + tig.  For 4-bit codes the odd channels meet the x16 registers, so
-  // their reciprocals carry the compensating 1/16.
-  static_assert((S::PB * S::kChunks) % 32 == 0 || S::PB * S::kChunks < 32, "chunk split");
-#pragma unroll
-  for (int it = 0; it < (S::PB * S::kChunks + 31) / 32; ++it) {
-    const int q = lane + 32 * it;
-    const int j = q / S::kChunks, cc = q - j * S::kChunks;
-    if (q < S::PB * S::kChunks && j < npages) {
-      const float4 s4 = reinterpret_cast<const float4*>(pg[j] + geom.kscale_off)[cc];
-      // the factor that undoes each channel's position in its code word
-      constexpr float f0 = BITS == 2 ? 16.f : 1.f, f1 = BITS == 2 ? 4.f : BITS == 4 ? 0.0625f : 1.f;
-      constexpr float f2 = 1.f, f3 = BITS == 2 ? 0.25f : BITS == 4 ? 0.0625f : 1.f;
-      const float4 r4 = make_float4(fast_rcp(s4.x) * f0, fast_rcp(s4.y) * f1, fast_rcp(s4.z) * f2,
-                                    fast_rcp(s4.w) * f3);
-      const int tg = cc / (S::kChan / 4), i = cc - tg * (S::kChan / 4);
-      reinterpret_cast<float4*>(rsc + j * D)[i * 4 + tg] = r4;
-    }
-  }
-  __syncwarp();
-  // ---- B operand of S: q / sK for (head gid % GP, page gid / GP), hi + lo ---
-  uint32_t bh[S::kSteps][2], bl[S::kSteps][2];
-  float beta0, beta1;
-  {
-    const int jb = FULL ? gid / GP : min(gid / GP, npages - 1);
-    const float4* rj = reinterpret_cast<const float4*>(rsc + jb * D);
-    float qk[S::kChan];
-    float bs[4] = {0.f, 0.f, 0.f, 0.f};  // sums over channels 4i + k
-    const int hq = gid % GP;
-#pragma unroll
-    for (int i = 0; i < S::kChan / 4; ++i) {
-      const float4 r = rj[i * 4 + tig];
-      const float4 qv = q4[(i * GP + hq) * 4 + tig];
-      qk[4 * i + 0] = qv.x * r.x;
-      qk[4 * i + 1] = qv.y * r.y;
-      qk[4 * i + 2] = qv.z * r.z;
-      qk[4 * i + 3] = qv.w * r.w;
-      bs[0] += qk[4 * i + 0];
-      bs[1] += qk[4 * i + 1];
-      bs[2] += qk[4 * i + 2];
-      bs[3] += qk[4 * i + 3];
-    }
-    // sum of q / sK with the position factors taken back out
-    if constexpr (BITS == 2) {
-      // 2-bit codes enter the MMA already signed: no bias to take out
-      beta0 = beta1 = 0.f;
-    } else {
-      float beta = BITS == 4 ? (bs[0] + bs[2]) + 16.f * (bs[1] + bs[3]) : (bs[0] + bs[2]) + (bs[1] + bs[3]);
-      beta += __shfl_xor_sync(0xffffffffu, beta, 1);
-      beta += __shfl_xor_sync(0xffffffffu, beta, 2);
-      beta0 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig));
-      beta1 = S::kBias * __shfl_sync(0xffffffffu, beta, 4 * (2 * tig + 1));
-    }
-#pragma unroll
-    for (int kk = 0; kk < S::kSteps; ++kk) {
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)], x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)];
-        const __half2 hi = __floats2half2_rn(x0, x1);
-        const float2 back = __half22float2(hi);
-        const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
-        bh[kk][r] = *reinterpret_cast<const uint32_t*>(&hi);
-        bl[kk][r] = *reinterpret_cast<const uint32_t*>(&lo);
-      }
-    }
-  }
-  const int sj = (2 * tig) / GP;                  // this thread's stream (both columns)
-  const int vpage = FULL ? sj : min(sj, npages - 1);  // a valid page for its Value scales
-  const uint8_t* vpg = pg[0];
-#pragma unroll
-  for (int j = 1; j < S::PB; ++j)
-    if (j == vpage) vpg = pg[j];
-  constexpr int kGap = token_row_gap<BITS>();
-  // A operand of the p/sV counter: the value 1 (or 16 on the x16 k-slots) in
-  // every element, as 2^-24-scaled subnormals like the codes
-  constexpr uint32_t kOneLo = 0x00010001u;
-  constexpr uint32_t kOneHi = BITS == 4 ? 0x00100010u : 0x00010001u;
-
-  for (int sub = 0; sub < G / 32; ++sub) {
-    // ---- scores of every page; keep each column's own page ------------------
-    float ss[2][4];
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb) ss[mb][0] = ss[mb][1] = ss[mb][2] = ss[mb][3] = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < S::PB; ++j) {
-      if (!FULL && j >= npages) break;
-      const uint8_t* kc = pg[j] + sub * 32 * S::kRowBytes;
-      uint32_t wa[2][S::kWords], wb[2][S::kWords];
-      // hi and lo halves of q accumulate separately: two dependent MMA chains
-      // of half the length, summed once per sub-tile
-      float s[2][4], s2[2][4];
-#pragma unroll
-      for (int mb = 0; mb < 2; ++mb) {
-        const int r0 = token_row0<BITS>(gid, mb);
-        lds_words<S::kWords>(kc + r0 * S::kRowBytes + tig * (S::kRowBytes / 4), wa[mb]);
-        lds_words<S::kWords>(kc + (r0 + kGap) * S::kRowBytes + tig * (S::kRowBytes / 4), wb[mb]);
-        s[mb][0] = s[mb][1] = s[mb][2] = s[mb][3] = 0.f;
-        s2[mb][0] = s2[mb][1] = s2[mb][2] = s2[mb][3] = 0.f;
-      }
-      if (BITS == 2) {
-#pragma unroll
-        for (int i = 0; i < S::kWords; ++i) {
-#pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            uint32_t ra[8], rb[8];
-            crumb_regs(wa[mb][i], ra);
-            crumb_regs(wb[mb][i], rb);
-            unbias_crumbs(ra);
-            unbias_crumbs(rb);
-#pragma unroll
-            for (int st2 = 0; st2 < 4; ++st2) {
-              const int kk = 4 * i + st2;
-              mma16816(s[mb], ra[2 * st2], rb[2 * st2], ra[2 * st2 + 1], rb[2 * st2 + 1], bh[kk][0], bh[kk][1]);
-              mma16816(s2[mb], ra[2 * st2], rb[2 * st2], ra[2 * st2 + 1], rb[2 * st2 + 1], bl[kk][0], bl[kk][1]);
-            }
-          }
-        }
-#pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[mb][e] += s2[mb][e];
-      } else if (BITS == 4) {
-#pragma unroll
-        for (int i = 0; i < S::kWords; ++i) {
-#pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            uint32_t ra[4], rb[4];
-            nibble_regs(wa[mb][i], ra);
-            nibble_regs(wb[mb][i], rb);
-            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bh[2 * i][0], bh[2 * i][1]);
-            mma16816(s2[mb], ra[0], rb[0], ra[1], rb[1], bl[2 * i][0], bl[2 * i][1]);
-            mma16816(s[mb], ra[2], rb[2], ra[3], rb[3], bh[2 * i + 1][0], bh[2 * i + 1][1]);
-            mma16816(s2[mb], ra[2], rb[2], ra[3], rb[3], bl[2 * i + 1][0], bl[2 * i + 1][1]);
-          }
-        }
-#pragma unroll
-        for (int mb = 0; mb < 2; ++mb)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[mb][e] += s2[mb][e];
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < S::kWords; ++kk) {
-#pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            uint32_t ra[2], rb[2];
-            byte_regs(wa[mb][kk], ra);
-            byte_regs(wb[mb][kk], rb);
-            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bh[kk][0], bh[kk][1]);
-            mma16816(s[mb], ra[0], rb[0], ra[1], rb[1], bl[kk][0], bl[kk][1]);
-          }
-        }
-      }
-      const bool mine = sj == j;
-#pragma unroll
-      for (int mb = 0; mb < 2; ++mb) {
-        constexpr float kUnscale = kTwo24 / S::kBScale;
-        ss[mb][0] = mine ? fmaf(s[mb][0], kUnscale, -beta0) : ss[mb][0];
-        ss[mb][1] = mine ? fmaf(s[mb][1], kUnscale, -beta1) : ss[mb][1];
-        ss[mb][2] = mine ? fmaf(s[mb][2], kUnscale, -beta0) : ss[mb][2];
-        ss[mb][3] = mine ? fmaf(s[mb][3], kUnscale, -beta1) : ss[mb][3];
-      }
-    }
-    // ---- online softmax (base 2) over the 32 tokens of each column ----------
-    // Lazy rescaling: the reference max m moves only when a score exceeds it
-    // by more than kSlack (weights then stay below 2^kSlack, well inside f16);
-    // l and O always share the same m, so the final o = O / l is exact.  Each
-    // lane tests its own scores; the column maxima are reduced across the
-    // warp only when some lane asks for a move.
-    constexpr float kSlack = 8.f;
-    float mx0 = fmaxf(fmaxf(ss[0][0], ss[0][2]), fmaxf(ss[1][0], ss[1][2]));
-    float mx1 = fmaxf(fmaxf(ss[0][1], ss[0][3]), fmaxf(ss[1][1], ss[1][3]));
-    if (__any_sync(0xffffffffu, mx0 > st.m0 + kSlack || mx1 > st.m1 + kSlack)) {
-#pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-      }
-      const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-      const float a0 = st.m0 == -INFINITY ? 0.f : fast_exp2(st.m0 - mn0);
-      const float a1 = st.m1 == -INFINITY ? 0.f : fast_exp2(st.m1 - mn1);
-      st.m0 = mn0;
-      st.m1 = mn1;
-      st.l0 *= a0;
-      st.l1 *= a1;
-#pragma unroll
-      for (int mt = 0; mt < S::kSteps; ++mt) {
-        st.O[mt][0] *= a0;
-        st.O[mt][1] *= a1;
-        st.O[mt][2] *= a0;
-        st.O[mt][3] *= a1;
-      }
-      st.C[0] *= a0;
-      st.C[1] *= a1;
-      st.C[2] *= a0;
-      st.C[3] *= a1;
-    }
-    const float ms0 = st.m0 == -INFINITY ? 0.f : st.m0, ms1 = st.m1 == -INFINITY ? 0.f : st.m1;
-    float pr[2][4];
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb) {
-      pr[mb][0] = fast_exp2(ss[mb][0] - ms0);
-      pr[mb][1] = fast_exp2(ss[mb][1] - ms1);
-      pr[mb][2] = fast_exp2(ss[mb][2] - ms0);
-      pr[mb][3] = fast_exp2(ss[mb][3] - ms1);
-    }
-    st.l0 += (pr[0][0] + pr[0][2]) + (pr[1][0] + pr[1][2]);
-    st.l1 += (pr[0][1] + pr[0][3]) + (pr[1][1] + pr[1][3]);
-    // ---- p / sV (Value scale of this thread's stream page), f16 -------------
-    const float* vscale = reinterpret_cast<const float*>(vpg + geom.vscale_off) + sub * 32;
-    uint32_t pk[2][2];
-#pragma unroll
-    for (int mb = 0; mb < 2; ++mb) {
-      const int r0 = token_row0<BITS>(gid, mb);
-      // undo the code's position factor: 4-bit x16 on the second row of each
-      // pair; 2-bit x1, x4 (m-block 0) and x16, x64 (m-block 1)
-      const float f0 = BITS == 2 ? (mb == 0 ? 1.f : 0.0625f) : 1.f;
-      const float f1 = BITS == 2 ? (mb == 0 ? 0.25f : 0.015625f) : BITS == 4 ? 0.0625f : 1.f;
-      const float i0 = fast_rcp(vscale[r0]) * f0;
-      const float i1 = fast_rcp(vscale[r0 + kGap]) * f1;
-      pk[mb][0] = pack_f16x2(pr[mb][0] * i0, pr[mb][1] * i0);
-      pk[mb][1] = pack_f16x2(pr[mb][2] * i1, pr[mb][3] * i1);
-    }
-    // ---- O'^T += V'^T P' for every page, P' masked to the page's columns ------
-#pragma unroll
-    for (int j = 0; j < S::PB; ++j) {
-      if (!FULL && j >= npages) break;
-      const bool mine = sj == j;
-      uint32_t bp[2][2];
-#pragma unroll
-      for (int mb = 0; mb < 2; ++mb) {
-        bp[mb][0] = transpose8x8(mine ? pk[mb][0] : 0u);
-        bp[mb][1] = transpose8x8(mine ? pk[mb][1] : 0u);
-        // the p / sV sum for the Value bias (2-bit codes enter signed: none)
-        if (BITS != 2) mma16816(st.C, kOneLo, kOneLo, kOneHi, kOneHi, bp[mb][0], bp[mb][1]);
-      }
-      const uint8_t* vc = pg[j] + geom.code_bytes + sub * S::kSubBytes;
-#pragma unroll
-      for (int mt = 0; mt < S::kSteps; ++mt) {
-        const int c_lo = 16 * mt + gid, c_hi = c_lo + 8;
-        if (BITS == 2) {
-          const uint32_t pl = *reinterpret_cast<const uint16_t*>(vc + c_lo * 8 + 2 * tig);
-          const uint32_t ph = *reinterpret_cast<const uint16_t*>(vc + c_hi * 8 + 2 * tig);
-          uint32_t rl[4], rh[4];
-          piece_regs(pl, rl);
-          piece_regs(ph, rh);
-          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
-          mma16816(st.O[mt], rl[2], rh[2], rl[3], rh[3], bp[1][0], bp[1][1]);
-        } else if (BITS == 4) {
-          const uint32_t wl = *reinterpret_cast<const uint32_t*>(vc + c_lo * 16 + 4 * tig);
-          const uint32_t wh = *reinterpret_cast<const uint32_t*>(vc + c_hi * 16 + 4 * tig);
-          uint32_t rl[4], rh[4];
-          nibble_regs(wl, rl);
-          nibble_regs(wh, rh);
-          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
-          mma16816(st.O[mt], rl[2], rh[2], rl[3], rh[3], bp[1][0], bp[1][1]);
-        } else {
-          const uint2 vl = *reinterpret_cast<const uint2*>(vc + c_lo * 32 + 8 * tig);
-          const uint2 vh = *reinterpret_cast<const uint2*>(vc + c_hi * 32 + 8 * tig);
-          uint32_t rl[2], rh[2];
-          byte_regs(vl.x, rl);
-          byte_regs(vh.x, rh);
-          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[0][0], bp[0][1]);
-          byte_regs(vl.y, rl);
-          byte_regs(vh.y, rh);
-          mma16816(st.O[mt], rl[0], rh[0], rl[1], rh[1], bp[1][0], bp[1][1]);
-        }
-      }
-    }
-  }
-}
-
-// A run of bf16 Key/Value rows on the tensor cores: the residual window of a
-// unit (rows in its ring) or a range of a dense restored cache.  Steps of 16
-// tokens: the rows are copied into a per-warp shared buffer with cp.async
-// (16-byte chunks XOR-swizzled by row so ldmatrix is conflict free; rows past
-// the run are zero-filled), double-buffered so the next step's copy overlaps
-// this step's math when NBUF = 2; then S = K q with bf16 MMAs (q is the bf16 input, so every
-// product is exact), the same online softmax as the pages, and O^T += V^T P
-// with V^T read by ldmatrix.trans and P as a bf16 hi + lo pair.  Row t of the
-// run is row (row0 + t) mod ring of kbase / vbase (RING), else row0 + t.
-// Column n holds head (n % GP) % g of the unit; only n < g is kept.
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-
-template <int D, int GP, int NBUF, bool RING>
-__device__ __forceinline__ void rows_mma(const DecodeParams& p, const __nv_bfloat16* kbase,
-                                         const __nv_bfloat16* vbase, int64_t row0, int ring, int n,
-                                         const __nv_bfloat16* qunit, int lane, int warp, int gid, int tig,
-                                         uint8_t* wbuf, WarpState<D>& st) {
-  constexpr int kRow = D * 2;             // bytes of one bf16 row
-  constexpr int kChunks = kRow / 16;      // 16-byte chunks per row
-  constexpr int kBuf = 32 * kRow;         // one step: 16 K rows + 16 V rows
-  uint32_t bq[D / 16][2];
-  {
-    const __nv_bfloat16* q = qunit + (int64_t)((gid % GP) % p.g) * D;
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      bq[kk][0] = *reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig);
-      bq[kk][1] = *reinterpret_cast<const uint32_t*>(q + 16 * kk + 2 * tig + 8);
-    }
-  }
-  const uint32_t buf_s = smem_addr(wbuf);
-  const int nsteps = (n + 15) / 16;
-  // copies of step stp into buffer half ``half``
-  auto issue = [&](int stp, int half) {
-    const int t0 = stp * 16;
-    const uint32_t kb = buf_s + half * kBuf, vb = kb + 16 * kRow;
-    for (int idx = lane; idx < 16 * kChunks; idx += 32) {
-      const int r = idx / kChunks, c = idx - r * kChunks;
-      const bool valid = t0 + r < n;
-      const int64_t t = row0 + t0 + (valid ? r : 0);
-      const int64_t row = RING ? t % ring : t;
-      const uint32_t off = r * kRow + ((c ^ (r & 7)) * 16);
-      cp_async16(kb + off, kbase + row * D + c * 8, valid ? 16u : 0u);
-      cp_async16(vb + off, vbase + row * D + c * 8, valid ? 16u : 0u);
-    }
-    cp_async_commit();
-  };
-  if (NBUF == 2 && warp < nsteps) issue(warp, 0);
-  int half = 0;
-  for (int stp = warp; stp < nsteps; stp += kMmaWarps, half ^= (NBUF - 1)) {
-    if (NBUF == 1) {
-      issue(stp, 0);
-      cp_async_wait_group<0>();
-    } else if (stp + kMmaWarps < nsteps) {
-      issue(stp + kMmaWarps, half ^ 1);
-      cp_async_wait_group<1>();
-    } else {
-      cp_async_wait_group<0>();
-    }
-    __syncwarp();
-    const int t0 = stp * 16;
-    const uint32_t kb_s = buf_s + half * kBuf, vb_s = kb_s + 16 * kRow;
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
-    {
-      const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        uint32_t a[4];
-        ldmatrix_x4(a, kb_s + r * kRow + (((2 * kk + (lane >> 4)) ^ (r & 7)) * 16));
-        mma16816_bf16(s, a[0], a[1], a[2], a[3], bq[kk][0], bq[kk][1]);
-      }
-    }
-    const bool v0 = t0 + gid < n, v1 = t0 + gid + 8 < n;
-    s[0] = v0 ? s[0] * p.qk_scale : -INFINITY;
-    s[1] = v0 ? s[1] * p.qk_scale : -INFINITY;
-    s[2] = v1 ? s[2] * p.qk_scale : -INFINITY;
-    s[3] = v1 ? s[3] * p.qk_scale : -INFINITY;
-    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(st.m0, mx0), mn1 = fmaxf(st.m1, mx1);
-    const float a0 = fast_exp2(st.m0 - mn0), a1 = fast_exp2(st.m1 - mn1);  // mn is finite: row 0 is valid
-    st.m0 = mn0;
-    st.m1 = mn1;
-    const float p0 = fast_exp2(s[0] - mn0), p1 = fast_exp2(s[1] - mn1);
-    const float p2 = fast_exp2(s[2] - mn0), p3 = fast_exp2(s[3] - mn1);
-    st.l0 = fmaf(st.l0, a0, p0 + p2);
-    st.l1 = fmaf(st.l1, a1, p1 + p3);
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      st.O[mt][0] *= a0;
-      st.O[mt][1] *= a1;
-      st.O[mt][2] *= a0;
-      st.O[mt][3] *= a1;
-    }
-    uint32_t bh[2], bl[2];
-    {
-      const uint32_t h0 = pack_bf16x2(p0, p1), h1 = pack_bf16x2(p2, p3);
-      const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h0));
-      const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&h1));
-      bh[0] = transpose8x8(h0);
-      bh[1] = transpose8x8(h1);
-      bl[0] = transpose8x8(pack_bf16x2(p0 - f0.x, p1 - f0.y));
-      bl[1] = transpose8x8(pack_bf16x2(p2 - f1.x, p3 - f1.y));
-    }
-    {
-      const int r = (lane & 7) + 8 * (lane >> 4);
-#pragma unroll
-      for (int mt = 0; mt < D / 16; ++mt) {
-        uint32_t a[4];
-        ldmatrix_x4_trans(a, vb_s + r * kRow + (((2 * mt + ((lane >> 3) & 1)) ^ (r & 7)) * 16));
-        mma16816_bf16(st.O[mt], a[0], a[1], a[2], a[3], bh[0], bh[1]);
-        mma16816_bf16(st.O[mt], a[0], a[1], a[2], a[3], bl[0], bl[1]);
-      }
-    }
-    __syncwarp();  // the buffer is refilled by a later step
-  }
-  // sums over the thread's rows -> over the warp's rows
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
-    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
-  }
-}
-
-// Merge the thread's (m, l, O) of its two columns with lane ^ off (same heads,
-// another stream of pages).
-template <int D>
-__device__ __forceinline__ void merge_streams(WarpState<D>& st, int off) {
-  const float m0o = __shfl_xor_sync(0xffffffffu, st.m0, off), m1o = __shfl_xor_sync(0xffffffffu, st.m1, off);
-  const float l0o = __shfl_xor_sync(0xffffffffu, st.l0, off), l1o = __shfl_xor_sync(0xffffffffu, st.l1, off);
-  const float M0 = fmaxf(st.m0, m0o), M1 = fmaxf(st.m1, m1o);
-  const float s0 = M0 == -INFINITY ? 0.f : M0, s1 = M1 == -INFINITY ? 0.f : M1;
-  const float fa0 = fast_exp2(st.m0 - s0), fb0 = fast_exp2(m0o - s0);
-  const float fa1 = fast_exp2(st.m1 - s1), fb1 = fast_exp2(m1o - s1);
-  st.l0 = st.l0 * fa0 + l0o * fb0;
-  st.l1 = st.l1 * fa1 + l1o * fb1;
-  st.m0 = M0;
-  st.m1 = M1;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    const float o0 = __shfl_xor_sync(0xffffffffu, st.O[mt][0], off);
-    const float o1 = __shfl_xor_sync(0xffffffffu, st.O[mt][1], off);
-    const float o2 = __shfl_xor_sync(0xffffffffu, st.O[mt][2], off);
-    const float o3 = __shfl_xor_sync(0xffffffffu, st.O[mt][3], off);
-    st.O[mt][0] = st.O[mt][0] * fa0 + o0 * fb0;
-    st.O[mt][1] = st.O[mt][1] * fa1 + o1 * fb1;
-    st.O[mt][2] = st.O[mt][2] * fa0 + o2 * fb0;
-    st.O[mt][3] = st.O[mt][3] * fa1 + o3 * fb1;
-  }
-}
-
-// Fold the four warps' (m, l, O) of the stream-0 columns into one partial
-// (o = sum O, m, l per query head) of slot ``slot`` of ``unit``.  ``buf`` is
-// shared memory no warp still reads (kMmaWarps * kMaxGqa * (D + 2) floats).
-template <int D, int GP>
-__device__ __forceinline__ void write_partial(const DecodeParams& p, int64_t unit, int slot, int warp,
-                                              int gid, int tig, const WarpState<D>& st, uint8_t* buf) {
-  const int g = p.g;
-
-  float* mrg = reinterpret_cast<float*>(buf);  // [kMmaWarps][kMaxGqa][D + 2]
-  const int hd0 = 2 * tig, hd1 = 2 * tig + 1;  // heads of the stream-0 columns
-  float* mw = mrg + (size_t)warp * kMaxGqa * (D + 2);
-  const bool stream0 = 2 * tig < GP;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) {
-    const int c_lo = 16 * mt + gid;
-    if (stream0 && hd0 < g) {
-      mw[hd0 * (D + 2) + c_lo] = st.O[mt][0];
-      mw[hd0 * (D + 2) + c_lo + 8] = st.O[mt][2];
-    }
-    if (stream0 && hd1 < g) {
-      mw[hd1 * (D + 2) + c_lo] = st.O[mt][1];
-      mw[hd1 * (D + 2) + c_lo + 8] = st.O[mt][3];
-    }
-  }
-  if (gid == 0 && stream0) {
-    if (hd0 < g) {
-      mw[hd0 * (D + 2) + D] = st.m0;
-      mw[hd0 * (D + 2) + D + 1] = st.l0;
-    }
-    if (hd1 < g) {
-      mw[hd1 * (D + 2) + D] = st.m1;
-      mw[hd1 * (D + 2) + D + 1] = st.l1;
-    }
-  }
-  __syncthreads();
-  float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * (D + 2);
-  for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
-    const int j = idx / D, c = idx - j * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, mrg[((size_t)w * kMaxGqa + j) * (D + 2) + D]);
-    float L = 0.f, O = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kMmaWarps; ++w) {
-        const float* r = mrg + ((size_t)w * kMaxGqa + j) * (D + 2);
-        if (r[D] == -INFINITY) continue;
-        const float f = exp2f(r[D] - M);
-        L = fmaf(r[D + 1], f, L);
-        O = fmaf(r[c], f, O);
-      }
-    }
-    part[(int64_t)j * (D + 2) + c] = O;
-    if (c == 0) {
-      part[(int64_t)j * (D + 2) + D] = M;
-      part[(int64_t)j * (D + 2) + D + 1] = L;
-    }
-  }
-}
-
-// Per-warp shared bytes of rows_mma: NBUF steps of 16 Key + 16 Value bf16 rows.
-template <int D, int NBUF>
-constexpr int kRowsBuf = NBUF * 32 * D * 2;
-
-template <int D, int BITS, int GP, bool PAGED>
-__global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const DecodeParams p, int slots) {
-  using S = Shape<D, BITS, GP>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  pdl_wait();
-  pdl_release();
-  // column-major over (split column, unit): every unit's first chunk, then
-  // every unit's second, ..., the windows last, so the last wave holds the
-  // shortest items
-  const int n_units = p.n_seqs * p.Hkv;
-  const int col = blockIdx.x / n_units;
-  const int u = blockIdx.x - col * n_units;
-  const int i = u / p.Hkv, h = u - i * p.Hkv;
-  bool win;
-  int pg0, pg1, slot;
-  if (!split_item(p, col, i, &win, &pg0, &pg1, &slot)) return;
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int b = p.seq_begin + i;
-  const int g = p.g;
-  const PageGeom geom = p.geom;
-  const uint32_t page_bytes = (uint32_t)geom.page_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-  float* scratch = reinterpret_cast<float*>(smem + 128 * ((kMmaWarps * slots * 8 + 127) / 128));
-  float* my_rsc = scratch + warp * S::PB * D;
-  float4* q4 = reinterpret_cast<float4*>(scratch + kMmaWarps * S::PB * D);  // GP * D floats
-  uint8_t* buf = reinterpret_cast<uint8_t*>(scratch + kMmaWarps * S::PB * D + GP * D);
-  uint8_t* my_buf = buf + (size_t)warp * slots * page_bytes;
-  const uint32_t my_bar = smem_addr(bars + warp * slots);
-
-  WarpState<D> st;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
-  st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
-  st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = 0.f;
-  bool ok = true;
-
-  if (win) {
-    const int64_t unit = (int64_t)b * p.Hkv + h;
-    const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-    rows_mma<D, GP, 1, true>(p, reinterpret_cast<const __nv_bfloat16*>(p.ring_k) + unit * p.Rcap * D,
-                    reinterpret_cast<const __nv_bfloat16*>(p.ring_v) + unit * p.Rcap * D, Q0, p.Rcap,
-                    (int)(T0 - Q0), reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * g) * D,
-                    lane, warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st);
-  } else {
-  // queries of the GP column heads (head n % g for the padding columns, so every
-  // value stays finite), pre-scaled, in shared memory: channel c of head n goes
-  // to float4 ((i * GP + n) * 4 + tig) with tig = c / (D/4), i = (c % (D/4)) / 4,
-  // so the lanes that read together hit distinct banks
-  for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) {
-    const int n = idx / D, c = idx - n * D;
-    const __nv_bfloat16* qrow =
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D;
-    const int tg = c / S::kChan, i4 = (c - tg * S::kChan) >> 2;
-    reinterpret_cast<float*>(q4)[((i4 * GP + n) * 4 + tg) * 4 + (c & 3)] = __bfloat162float(qrow[c]) * p.qk_scale;
-  }
-  __syncthreads();
-
-  // source of this warp's pos-th page (pages pg0 + warp, + 4, ...), through
-  // the block table for a paged cache
-  const uint8_t* unit_pages = PAGED ? p.pages : p.pages + page_offset(p.map, page_bytes, b, h, 0);
-  auto src_of = [&](int pos) {
-    const int pg = pg0 + warp + pos * kMmaWarps;
-    return PAGED ? p.pages + page_offset(p.map, page_bytes, b, h, pg) : unit_pages + (int64_t)pg * page_bytes;
-  };
-  const int npg = pg1 - pg0;
-  const int my_n = warp < npg ? (npg - warp + kMmaWarps - 1) / kMmaWarps : 0;
-  if (lane == 0) {
-    for (int s = 0; s < slots; ++s) mbar_init(my_bar + 8 * s, 1);
-    fence_mbar_init();
-    fence_proxy_async();
-    for (int s = 0; s < slots && s < my_n; ++s) {
-      mbar_expect_tx(my_bar + 8 * s, page_bytes);
-      bulk_load(smem_addr(my_buf + (size_t)s * page_bytes), src_of(s), page_bytes, my_bar + 8 * s);
-    }
-  }
-  __syncwarp();
-
-  // Pages are consumed in issue order; page k sits in slot k mod slots, and
-  // bit t of ``phases`` is the parity slot t's barrier completes next.  Every
-  // lane keeps the same counters; lane 0 issues the copies.
-  int k = 0, sidx = 0, consumed = 0, issued = slots < my_n ? slots : my_n;
-  uint32_t phases = 0;
-  const uint8_t* next_src = PAGED ? nullptr : src_of(issued);  // contiguous: advanced by whole runs
-  for (; k < my_n; k += S::PB) {
-    const int np = min(S::PB, my_n - k);
-    int sl[S::PB];
-    const uint8_t* pgs[S::PB];
-#pragma unroll
-    for (int j = 0; j < S::PB; ++j) {
-      int t = sidx + (j < np ? j : np - 1);
-      if (t >= slots) t -= slots;
-      sl[j] = t;
-      pgs[j] = my_buf + (size_t)t * page_bytes;
-    }
-#pragma unroll
-    for (int j = 0; j < S::PB; ++j) {
-      if (j < np && ok) {
-        ok = mbar_wait(my_bar + 8 * sl[j], (phases >> sl[j]) & 1u);
-        if (ok) {
-          phases ^= 1u << sl[j];
-          ++consumed;
-        }
-      }
-    }
-    if (!ok) break;
-    if (np == S::PB)
-      mma_group<D, BITS, GP, true>(pgs, np, geom, p.G, q4, my_rsc, lane, gid, tig, st);
-    else
-      mma_group<D, BITS, GP, false>(pgs, np, geom, p.G, q4, my_rsc, lane, gid, tig, st);
-    __syncwarp();
-    // refill the freed slots with the next pages of this warp's run
-    const int refill = min(np, my_n - issued);
-    if (lane == 0 && refill > 0) {
-      fence_proxy_async();
-#pragma unroll
-      for (int j = 0; j < S::PB; ++j) {
-        if (j < refill) {
-          mbar_expect_tx(my_bar + 8 * sl[j], page_bytes);
-          const uint8_t* src = PAGED ? src_of(issued + j) : next_src + (int64_t)j * kMmaWarps * page_bytes;
-          bulk_load(smem_addr(my_buf + (size_t)sl[j] * page_bytes), src, page_bytes, my_bar + 8 * sl[j]);
-        }
-      }
-    }
-    if (!PAGED) next_src += (int64_t)refill * kMmaWarps * page_bytes;
-    issued += refill;
-    sidx += np;
-    if (sidx >= slots) sidx -= slots;
-  }
-  if (!ok) {
-    // drain the copies still in flight (bounded), report, and contribute nothing
-    for (int kk = consumed; kk < issued; ++kk) {
-      const int t = kk % slots;
-      mbar_wait(my_bar + 8 * t, (phases >> t) & 1u);
-      phases ^= 1u << t;
-    }
-    if (lane == 0) atomicOr(p.status, kStatusWaitTimeout);
-    st.m0 = st.m1 = -INFINITY;
-    st.l0 = st.l1 = 0.f;
-    st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
-  }
-  // sums over the thread's rows -> over the warp's rows; undo the code bias
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    st.l0 += __shfl_xor_sync(0xffffffffu, st.l0, off);
-    st.l1 += __shfl_xor_sync(0xffffffffu, st.l1, off);
-  }
-  {
-    // C holds 2^-24 * sum of p/sV per column (every row of the counter MMA
-    // carries the full sum), so the bias term is bias * 2^24 * C
-    constexpr float kTwo24 = 16777216.f;
-    const float c0 = S::kBias * kTwo24 * st.C[0], c1 = S::kBias * kTwo24 * st.C[1];
-#pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt) {
-      st.O[mt][0] = fmaf(st.O[mt][0], kTwo24, -c0);
-      st.O[mt][1] = fmaf(st.O[mt][1], kTwo24, -c1);
-      st.O[mt][2] = fmaf(st.O[mt][2], kTwo24, -c0);
-      st.O[mt][3] = fmaf(st.O[mt][3], kTwo24, -c1);
-    }
-  }
-  // fold the page streams onto stream 0 (columns 0 .. GP-1)
-#pragma unroll
-  for (int off = GP / 2; off < 4; off <<= 1) merge_streams<D>(st, off);
-  }  // page path
-  __syncthreads();  // every warp is done with its slots: reuse them for the merge
-  write_partial<D, GP>(p, (int64_t)b * p.Hkv + h, slot, warp, gid, tig, st, buf);
-}
-
-// Decode attention over a dense bf16 Key/Value cache ([batch][Hkv][t_stride][D],
-// as kvq_restore writes it): the second half of the dequantize-to-HBM read
-// path, kept as the measured foil of the fused kernel.  One CTA per
-// (token chunk, unit), column-major like the fused kernel; its four warps take
-// 16-token steps round robin through rows_mma (double-buffered) and the CTA
-// writes the chunk's partial to slot ``chunk``.
-template <int D, int GP>
-__global__ void __launch_bounds__(kMmaThreads) decode_dense_kernel(const DecodeParams p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  pdl_wait();
-  pdl_release();
-  const int n_units = p.n_seqs * p.Hkv;
-  const int col = blockIdx.x / n_units;
-  const int u = blockIdx.x - col * n_units;
-  const int i = u / p.Hkv, h = u - i * p.Hkv;
-  const int64_t T0 = p.ctr[i].total;
-  const int64_t t_begin = (int64_t)col * p.dense_chunk;
-  if (t_begin >= T0) return;
-  const int n = T0 - t_begin < p.dense_chunk ? (int)(T0 - t_begin) : p.dense_chunk;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int gid = lane >> 2, tig = lane & 3;
-  const int b = p.seq_begin + i;
-  const int64_t unit = (int64_t)b * p.Hkv + h;
-  WarpState<D> st;
-#pragma unroll
-  for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
-  st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
-  st.m0 = st.m1 = -INFINITY;
-  st.l0 = st.l1 = 0.f;
-  rows_mma<D, GP, 2, false>(p, reinterpret_cast<const __nv_bfloat16*>(p.dense_k) + unit * p.t_stride * D,
-                            reinterpret_cast<const __nv_bfloat16*>(p.dense_v) + unit * p.t_stride * D, t_begin, 0,
-                            n, reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * p.g) * D, lane,
-                            warp, gid, tig, smem + (size_t)warp * kRowsBuf<D, 2>, st);
-  __syncthreads();  // every warp is done with its buffers: reuse them for the merge
-  write_partial<D, GP>(p, unit, col, warp, gid, tig, st, smem);
-}
-
-template <int D>
-size_t dense_smem() {
-  const size_t rows = (size_t)kMmaWarps * kRowsBuf<D, 2>;
-  const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
-  return rows > merge ? rows : merge;
-}
-
-template <int D, int GP>
-cudaError_t launch_dense_t(const DecodeParams& p, int cols, cudaStream_t s) {
-  const size_t smem = dense_smem<D>();
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static size_t configured[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (smem > configured[dev]) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(decode_dense_kernel<D, GP>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = smem;
-  }
-  return launch_pdl(decode_dense_kernel<D, GP>, dim3(cols * p.n_seqs * p.Hkv), dim3(kMmaThreads), smem, s, p);
-}
-
-int gqa_pad(int g) { return g <= 2 ? 2 : g <= 4 ? 4 : 8; }
-
-template <int D>
-cudaError_t launch_dense_g(const DecodeParams& p, int cols, cudaStream_t s) {
-  switch (gqa_pad(p.g)) {
-    case 2: return launch_dense_t<D, 2>(p, cols, s);
-    case 4: return launch_dense_t<D, 4>(p, cols, s);
-    default: return launch_dense_t<D, 8>(p, cols, s);
-  }
-}
-
-// Shared-memory page slots per warp: about 60 KB of pages per CTA, at least
-// one group (8 / padded g pages) and at most 8.
-int mma_slots(int64_t page_bytes, int g) {
-  const int pb = 8 / gqa_pad(g);
-  int slots = (int)(60 * 1024 / (kMmaWarps * page_bytes));
-  if (slots < pb) slots = pb;
-  if (slots > 8) slots = 8;
-  return slots;
-}
-
-constexpr size_t kMaxSmem = 227 * 1024;
-
-template <int D>
-size_t smem_for(const DecodeParams& p) {
-  const int slots = mma_slots(p.geom.page_bytes, p.g);
-  size_t pages = (size_t)kMmaWarps * slots * p.geom.page_bytes;
-  const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
-  const size_t window = (size_t)kMmaWarps * kRowsBuf<D, 1>;
-  if (pages < merge) pages = merge;
-  if (pages < window) pages = window;
-  const size_t scratch = ((size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D + (size_t)gqa_pad(p.g) * D) * sizeof(float);
-  return 128 * ((kMmaWarps * slots * 8 + 127) / 128) + scratch + pages;
-}
-
-template <int D, int BITS, int GP, bool PAGED>
-cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
-  const size_t smem = smem_for<D>(p);
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static size_t configured[64] = {};
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (smem > configured[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BITS, GP, PAGED>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[dev] = smem;
-  }
-  const dim3 grid((p.grid_splits + 1) * p.n_seqs * p.Hkv);
-  return launch_pdl(decode_mma_kernel<D, BITS, GP, PAGED>, grid, dim3(kMmaThreads), smem, s, p,
-                    mma_slots(p.geom.page_bytes, p.g));
-}
-
-template <int D, int BITS>
-cudaError_t launch_g(const DecodeParams& p, cudaStream_t s) {
-  switch (gqa_pad(p.g)) {
-    case 2: return p.map.table ? launch_t<D, BITS, 2, true>(p, s) : launch_t<D, BITS, 2, false>(p, s);
-    case 4: return p.map.table ? launch_t<D, BITS, 4, true>(p, s) : launch_t<D, BITS, 4, false>(p, s);
-    default: return p.map.table ? launch_t<D, BITS, 8, true>(p, s) : launch_t<D, BITS, 8, false>(p, s);
-  }
-}
-
-}  // namespace
 
 size_t decode_mma_smem_bytes(const DecodeParams& p) {
   return p.D == 64 ? smem_for<64>(p) : smem_for<128>(p);
@@ -1099,8 +25,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* suppor
   *supported = (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g >= 2 && p.g <= kMaxGqa &&
                decode_mma_smem_bytes(p) <= kMaxSmem;
   if (!*supported) return cudaSuccess;
-  if (p.D == 64) return p.bits == 2 ? launch_g<64, 2>(p, s) : p.bits == 4 ? launch_g<64, 4>(p, s) : launch_g<64, 8>(p, s);
-  return p.bits == 2 ? launch_g<128, 2>(p, s) : p.bits == 4 ? launch_g<128, 4>(p, s) : launch_g<128, 8>(p, s);
+  return p.bits == 2 ? launch_mma_bits2(p, s) : p.bits == 4 ? launch_mma_bits4(p, s) : launch_mma_bits8(p, s);
 }
 
 }  // namespace kvq

@@ -1,0 +1,12 @@
+// Instantiations of the tensor-core split kernel for 2-bit codes (head_dim
+// 64 and 128, every GQA padding and page mode); see kvq_decode_mma.cuh.
+
+#include "kvq_decode_mma.cuh"
+
+namespace kvq {
+
+cudaError_t launch_mma_bits2(const DecodeParams& p, cudaStream_t s) {
+  return p.D == 64 ? launch_g<64, 2>(p, s) : launch_g<128, 2>(p, s);
+}
+
+}  // namespace kvq

@@ -199,6 +199,10 @@ cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s);
 cudaError_t configure_append(int dtype, int bits, size_t smem_bytes);
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported);
+// the split kernel for one code width (one translation unit each)
+cudaError_t launch_mma_bits2(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_mma_bits4(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_mma_bits8(const DecodeParams& p, cudaStream_t s);
 size_t decode_mma_smem_bytes(const DecodeParams& p);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supported);
