@@ -200,6 +200,23 @@ kvq_status kvq_required_bytes_paged(const kvq_config* cfg, const int64_t* capaci
 kvq_status kvq_create_paged(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks,
                             void* device_mem, size_t device_bytes, kvq_cache** out);
 
+/* Segmented cache: the flush rule of "54. KV Cache Quantization Strategies"
+ * (append_and_partition) verbatim.  An append of n tokens to a window of L
+ * flushes its whole overflow, max(L + n - R, 0) tokens, as ONE segment: Key
+ * codes with one scale per channel over the segment's tokens, Value codes
+ * with one scale per token; the newest min(L + n, R) tokens stay at input
+ * precision.  cfg->group is not used (any valid value).  Storage: per unit,
+ * token-major code rows (each row packed like a group page's Key row, for
+ * Keys and Values alike), each token's copy of its segment's Key scales
+ * (head_dim fp32), its Value scale, and a window ring of R rows.  Decode
+ * attention runs on the CUDA-core kernel; kvq_export_unit returns one Key
+ * scale row per segment; kvq_export_pages returns KVQ_EUNSUPPORTED; the other
+ * calls work as on a grouped cache.  Arguments as kvq_required_bytes /
+ * kvq_create. */
+kvq_status kvq_required_bytes_segmented(const kvq_config* cfg, const int64_t* capacity_per_seq, size_t* out_bytes);
+kvq_status kvq_create_segmented(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
+                                size_t device_bytes, kvq_cache** out);
+
 /* Empty sequences [seq_begin, seq_begin + n_seqs) (counters to zero); a paged
  * cache returns their blocks to the pool.  Host bookkeeping only: work already
  * queued on a stream still sees the old contents, and a later append may
@@ -264,7 +281,10 @@ kvq_status kvq_ledger(const kvq_config* cfg, const int64_t* tokens_per_seq, kvq_
 kvq_status kvq_seq_state(const kvq_cache* cache, int32_t seq, kvq_seq_info* out);
 
 /* Copy one unit's codes, scales and window to host buffers, decoded from the
- * layout above (synchronizes ``stream``). */
+ * layout above (synchronizes ``stream``): k_codes, v_codes [quantized][head_dim]
+ * int8; k_scales [n_groups][head_dim] (one row per flushed group, or per
+ * segment of a segmented cache); v_scales [quantized]; window_k, window_v
+ * [window][head_dim] fp32.  Any pointer may be NULL to skip that part. */
 kvq_status kvq_export_unit(const kvq_cache* cache, int32_t seq, int32_t kv_head,
                            const kvq_unit_view* view, void* stream);
 

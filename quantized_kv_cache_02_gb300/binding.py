@@ -23,7 +23,8 @@ EXPORTED = ("kvq_required_bytes", "kvq_create", "kvq_append", "kvq_decode_attent
             "kvq_decode_attention_ex", "kvq_bytes", "kvq_ledger", "kvq_seq_state", "kvq_export_unit",
             "kvq_export_pages", "kvq_device_status", "kvq_page_bytes", "kvq_kernel_launches", "kvq_destroy",
             "kvq_last_error", "kvq_decode_attention_noalloc", "kvq_restore", "kvq_dense_decode_attention",
-            "kvq_compare", "kvq_required_bytes_paged", "kvq_create_paged", "kvq_release", "kvq_pool_state")
+            "kvq_compare", "kvq_required_bytes_paged", "kvq_create_paged", "kvq_release", "kvq_pool_state",
+            "kvq_required_bytes_segmented", "kvq_create_segmented")
 
 
 class kvq_config(ctypes.Structure):
@@ -97,6 +98,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                         ctypes.c_int),
         "kvq_required_bytes_paged": ([P(kvq_config), P(I64), I64, P(SZ)], ctypes.c_int),
         "kvq_create_paged": ([P(kvq_config), P(I64), I64, V, SZ, P(V)], ctypes.c_int),
+        "kvq_required_bytes_segmented": ([P(kvq_config), P(I64), P(SZ)], ctypes.c_int),
+        "kvq_create_segmented": ([P(kvq_config), P(I64), V, SZ, P(V)], ctypes.c_int),
         "kvq_release": ([V, I32, I32], ctypes.c_int),
         "kvq_pool_state": ([V, P(I64), P(I64)], ctypes.c_int),
         "kvq_destroy": ([V], None),
@@ -153,6 +156,19 @@ def kvq_create_paged(cfg: kvq_config, capacity, pool_blocks: int, device_ptr: in
     handle = ctypes.c_void_p()
     _check(load_library().kvq_create_paged(ctypes.byref(cfg), _i64_array(capacity), pool_blocks,
                                            ctypes.c_void_p(device_ptr), device_bytes, ctypes.byref(handle)))
+    return handle.value
+
+
+def kvq_required_bytes_segmented(cfg: kvq_config, capacity) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load_library().kvq_required_bytes_segmented(ctypes.byref(cfg), _i64_array(capacity), ctypes.byref(out)))
+    return out.value
+
+
+def kvq_create_segmented(cfg: kvq_config, capacity, device_ptr: int, device_bytes: int) -> int:
+    handle = ctypes.c_void_p()
+    _check(load_library().kvq_create_segmented(ctypes.byref(cfg), _i64_array(capacity), ctypes.c_void_p(device_ptr),
+                                               device_bytes, ctypes.byref(handle)))
     return handle.value
 
 
@@ -267,9 +283,11 @@ class KVQCache:
     current stream."""
 
     def __init__(self, batch, n_kv_heads, n_q_heads, head_dim, residual_len, group, qmax, capacity,
-                 dtype="bf16", eps=1e-8, device=None, pool_blocks=0):
+                 dtype="bf16", eps=1e-8, device=None, pool_blocks=0, segmented=False):
         """pool_blocks > 0 makes a paged cache: ``capacity`` then bounds each
-        sequence's length and the pool of blocks is shared."""
+        sequence's length and the pool of blocks is shared.  segmented=True
+        makes a cache that flushes each append's whole overflow as one segment
+        (``group`` is then unused)."""
         import torch
         self.torch = torch
         self.device = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
@@ -280,13 +298,20 @@ class KVQCache:
             capacity = [capacity] * batch
         self.capacity = list(capacity)
         self.pool_blocks = pool_blocks
-        self.nbytes = (kvq_required_bytes_paged(self.cfg, self.capacity, pool_blocks) if pool_blocks
-                       else kvq_required_bytes(self.cfg, self.capacity))
+        self.segmented = segmented
+        if segmented:
+            self.nbytes = kvq_required_bytes_segmented(self.cfg, self.capacity)
+        elif pool_blocks:
+            self.nbytes = kvq_required_bytes_paged(self.cfg, self.capacity, pool_blocks)
+        else:
+            self.nbytes = kvq_required_bytes(self.cfg, self.capacity)
         self.arena = torch.empty(self.nbytes + 256, dtype=torch.uint8, device=self.device)
         base = self.arena.data_ptr()
         self._base = (base + 255) // 256 * 256
         with torch.cuda.device(self.device):
-            if pool_blocks:
+            if segmented:
+                self.handle = kvq_create_segmented(self.cfg, self.capacity, self._base, self.nbytes)
+            elif pool_blocks:
                 self.handle = kvq_create_paged(self.cfg, self.capacity, pool_blocks, self._base, self.nbytes)
             else:
                 self.handle = kvq_create(self.cfg, self.capacity, self._base, self.nbytes)
@@ -369,9 +394,9 @@ class KVQCache:
         v_scales, window_k, window_v (token order)."""
         import numpy as np
         st = self.seq_state(seq)
-        Q, W, D, G = st["quantized"], st["window"], self.cfg.head_dim, self.cfg.group
+        Q, W, D = st["quantized"], st["window"], self.cfg.head_dim
         arrs = {"k_codes": np.zeros((Q, D), np.int8), "v_codes": np.zeros((Q, D), np.int8),
-                "k_scales": np.zeros((Q // G, D), np.float32), "v_scales": np.zeros((Q,), np.float32),
+                "k_scales": np.zeros((st["n_groups"], D), np.float32), "v_scales": np.zeros((Q,), np.float32),
                 "window_k": np.zeros((W, D), np.float32), "window_v": np.zeros((W, D), np.float32)}
         view = kvq_unit_view(*[a.ctypes.data for a in arrs.values()])
         kvq_export_unit(self.handle, seq, kv_head, view, self._stream())

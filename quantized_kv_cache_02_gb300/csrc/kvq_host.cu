@@ -42,6 +42,12 @@ struct kvq_cache {
   int32_t* table;                            // device [batch][table_stride]
   std::vector<int32_t> free_blocks;
   std::vector<std::vector<int32_t>> blocks;  // host copy of each sequence's table
+  // segmented mode (the whole overflow of an append is one segment): token-major
+  // codes and scales; cfg.group is 1 inside (a "page" is one token)
+  bool segmented;
+  kvq::SegArrays seg;
+  uint32_t* kmax;                            // device [batch][Hkv][D]
+  std::vector<std::vector<int32_t>> seg_starts;  // first token of each segment
   int max_splits;
   int min_chunk_pages;
   int n_sm;
@@ -162,6 +168,54 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int
   return KVQ_OK;
 }
 
+// Arena of a segmented cache: token-major Key and Value code rows and scales
+// for capacity_max tokens per unit, the segment maxima, rings of R rows and
+// the split partials.
+struct SegPlan {
+  size_t status, layout, kcodes, vcodes, kscales, vscales, kmax, ring_k, ring_v, partials, total;
+  int64_t cap;
+  int max_splits;
+};
+
+kvq_status plan_arena_seg(const kvq_config* c, const int64_t* cap, SegPlan* a) {
+  if (!cap) return fail(KVQ_EINVAL, "capacity_per_seq is NULL");
+  int64_t cmax = 1;
+  for (int b = 0; b < c->batch; ++b) {
+    if (cap[b] < 1 || cap[b] >= (int64_t(1) << 31))
+      return fail(KVQ_EINVAL, "capacity of sequence %d must be in [1, 2^31) (got %lld)", b, (long long)cap[b]);
+    cmax = std::max(cmax, cap[b]);
+  }
+  a->cap = cmax;
+  a->max_splits = (int)((cmax + kMinChunkTokens - 1) / kMinChunkTokens) + 1;
+  const size_t units = (size_t)c->batch * c->n_kv_heads, D = c->head_dim;
+  const size_t rows = units * (size_t)cmax;
+  const int g = c->n_q_heads / c->n_kv_heads;
+  size_t o = 0;
+  a->status = o;
+  o = align_up(o + sizeof(int32_t), kAlign);
+  a->layout = o;
+  o = align_up(o + (size_t)c->batch * sizeof(kvq::SeqLayout), kAlign);
+  a->kcodes = o;
+  o = align_up(o + rows * D * bits_of(c) / 8, kAlign);
+  a->vcodes = o;
+  o = align_up(o + rows * D * bits_of(c) / 8, kAlign);
+  a->kscales = o;
+  o = align_up(o + rows * D * sizeof(float), kAlign);
+  a->vscales = o;
+  o = align_up(o + rows * sizeof(float), kAlign);
+  a->kmax = o;
+  o = align_up(o + units * D * sizeof(uint32_t), kAlign);
+  const size_t ring = units * (size_t)c->residual_len * D * esize_of(c);
+  a->ring_k = o;
+  o = align_up(o + ring, kAlign);
+  a->ring_v = o;
+  o = align_up(o + ring, kAlign);
+  a->partials = o;
+  o = align_up(o + units * a->max_splits * g * (D + 2) * sizeof(float), kAlign);
+  a->total = o;
+  return KVQ_OK;
+}
+
 bool aligned16(const void* p) { return p && ((uintptr_t)p & 15u) == 0; }
 
 kvq::PageMap page_map(const kvq_cache* c) {
@@ -218,6 +272,7 @@ void base_decode_params(const kvq_cache* c, kvq::DecodeParams* p) {
   p->geom = c->geom;
   p->pages = c->pages;
   p->map = page_map(c);
+  p->seg = c->seg;
   p->ring_k = c->ring_k;
   p->ring_v = c->ring_v;
   p->partials = c->partials;
@@ -255,7 +310,7 @@ kvq_status required_bytes(const kvq_config* cfg, const int64_t* capacity_per_seq
 }
 
 kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_t pool_blocks, void* device_mem,
-                  size_t device_bytes, kvq_cache** out) {
+                  size_t device_bytes, kvq_cache** out, bool segmented = false) {
   if (!out) return fail(KVQ_EINVAL, "out is NULL");
   *out = nullptr;
   kvq_status st = check_config(cfg);
@@ -263,10 +318,13 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   ArenaPlan a;
   st = plan_arena(cfg, capacity_per_seq, &a, pool_blocks);
   if (st != KVQ_OK) return st;
+  SegPlan sp{};
+  if (segmented && (st = plan_arena_seg(cfg, capacity_per_seq, &sp)) != KVQ_OK) return st;
+  const size_t need = segmented ? sp.total : a.total;
   if (!device_mem || ((uintptr_t)device_mem & (kAlign - 1)))
     return fail(KVQ_EINVAL, "device_mem must be a 256-byte aligned device pointer");
-  if (device_bytes < a.total)
-    return fail(KVQ_ENOMEM, "arena of %zu bytes is smaller than the %zu bytes required", device_bytes, a.total);
+  if (device_bytes < need)
+    return fail(KVQ_ENOMEM, "arena of %zu bytes is smaller than the %zu bytes required", device_bytes, need);
   cudaPointerAttributes attr;
   cudaError_t e = cudaPointerGetAttributes(&attr, device_mem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
@@ -311,6 +369,29 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   c->ring_k = c->base + a.ring_k;
   c->ring_v = c->base + a.ring_v;
   c->partials = reinterpret_cast<float*>(c->base + a.partials);
+  if (segmented) {
+    // a "page" is one token: group 1 inside, rings of R rows
+    c->segmented = true;
+    c->cfg.group = 1;
+    c->rcap = cfg->residual_len;
+    c->geom = kvq::make_geom(1, cfg->head_dim, c->bits);
+    c->max_splits = sp.max_splits;
+    c->min_chunk_pages = (int)kMinChunkTokens;
+    c->seg.kcodes = c->base + sp.kcodes;
+    c->seg.vcodes = c->base + sp.vcodes;
+    c->seg.kscales = reinterpret_cast<float*>(c->base + sp.kscales);
+    c->seg.vscales = reinterpret_cast<float*>(c->base + sp.vscales);
+    c->seg.cap = sp.cap;
+    c->seg.row_bytes = cfg->head_dim * c->bits / 8;
+    c->kmax = reinterpret_cast<uint32_t*>(c->base + sp.kmax);
+    c->status = reinterpret_cast<int32_t*>(c->base + sp.status);
+    c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + sp.layout);
+    c->pages = nullptr;
+    c->ring_k = c->base + sp.ring_k;
+    c->ring_v = c->base + sp.ring_v;
+    c->partials = reinterpret_cast<float*>(c->base + sp.partials);
+    c->seg_starts.assign(cfg->batch, {});
+  }
 
   std::vector<kvq::SeqLayout> table(cfg->batch);
   for (int b = 0; b < cfg->batch; ++b) {
@@ -329,6 +410,56 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
     return cuda_fail(e, "kvq_create set-up");
   }
   *out = c;
+  return KVQ_OK;
+}
+
+// Append to a segmented cache: zero the segment maxima of the sequences, run
+// the two flush passes over the overflow of each sequence, then copy the new
+// tokens that stay into the rings.
+kvq_status append_segmented(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens, int32_t seq_begin,
+                            int32_t n_seqs, cudaStream_t s) {
+  const int64_t R = c->cfg.residual_len, H = c->cfg.n_kv_heads, D = c->cfg.head_dim;
+  const int64_t per_seq_elems = H * n_tokens * D;
+  for (int s0 = seq_begin; s0 < seq_begin + n_seqs; s0 += kvq::kMaxSeqsPerLaunch) {
+    const int n = std::min(kvq::kMaxSeqsPerLaunch, seq_begin + n_seqs - s0);
+    kvq::SegFlushParams p;
+    memset(&p, 0, sizeof p);
+    p.D = (int)D;
+    p.Hkv = (int)H;
+    p.R = (int)R;
+    p.qmax = c->cfg.qmax;
+    p.bits = c->bits;
+    p.eps = c->cfg.eps;
+    p.seg = c->seg;
+    p.kmax = c->kmax;
+    p.ring_k = p.ring_k_out = c->ring_k;
+    p.ring_v = p.ring_v_out = c->ring_v;
+    const int64_t in_off = (int64_t)(s0 - seq_begin) * per_seq_elems * c->esize;
+    p.new_k = static_cast<const uint8_t*>(new_k) + in_off;
+    p.new_v = static_cast<const uint8_t*>(new_v) + in_off;
+    p.n = n_tokens;
+    p.seq_begin = s0;
+    p.n_seqs = n;
+    fill_counters(c, s0, n, p.old);
+    int64_t fmax = 0;
+    for (int i = 0; i < n; ++i) fmax = std::max<int64_t>(fmax, p.old[i].total - p.old[i].quantized + n_tokens - R);
+    cudaError_t e = cudaSuccess;
+    if (fmax > 0) {
+      e = cudaMemsetAsync(c->kmax + (int64_t)s0 * H * D, 0, (size_t)n * H * D * sizeof(uint32_t), s);
+      if (e == cudaSuccess) e = kvq::launch_seg_flush(p, c->cfg.dtype == KVQ_BF16 ? 0 : 1, fmax, s);
+      if (e == cudaSuccess) g_launches += 2;
+    }
+    if (e == cudaSuccess) e = kvq::launch_seg_window(p, c->cfg.dtype == KVQ_BF16 ? 0 : 1, s);
+    if (e != cudaSuccess) return cuda_fail(e, "segmented append launch");
+    g_launches += 1;
+  }
+  for (int b = seq_begin; b < seq_begin + n_seqs; ++b) {
+    const int64_t F = std::max<int64_t>(0, c->total[b] - c->quantized[b] + n_tokens - R);
+    if (F > 0) c->seg_starts[b].push_back(c->quantized[b]);
+    c->quantized[b] += (int32_t)F;
+    c->total[b] += (int32_t)n_tokens;
+    c->last_flushed[b] = (int32_t)F;
+  }
   return KVQ_OK;
 }
 
@@ -359,6 +490,22 @@ kvq_status kvq_create_paged(const kvq_config* cfg, const int64_t* capacity_per_s
   return create(cfg, capacity_per_seq, pool_blocks, device_mem, device_bytes, out);
 }
 
+kvq_status kvq_required_bytes_segmented(const kvq_config* cfg, const int64_t* capacity_per_seq, size_t* out_bytes) {
+  if (!out_bytes) return fail(KVQ_EINVAL, "out_bytes is NULL");
+  kvq_status st = check_config(cfg);
+  if (st != KVQ_OK) return st;
+  SegPlan sp{};
+  st = plan_arena_seg(cfg, capacity_per_seq, &sp);
+  if (st != KVQ_OK) return st;
+  *out_bytes = sp.total;
+  return KVQ_OK;
+}
+
+kvq_status kvq_create_segmented(const kvq_config* cfg, const int64_t* capacity_per_seq, void* device_mem,
+                                size_t device_bytes, kvq_cache** out) {
+  return create(cfg, capacity_per_seq, 0, device_mem, device_bytes, out, true);
+}
+
 void kvq_destroy(kvq_cache* cache) { delete cache; }
 
 kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens, int32_t seq_begin,
@@ -376,6 +523,7 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
                   (long long)c->total[b], (long long)n_tokens, (long long)c->cap[b]);
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (c->segmented) return append_segmented(c, new_k, new_v, n_tokens, seq_begin, n_seqs, s);
   const int64_t R = c->cfg.residual_len, G = c->cfg.group;
   const int64_t per_seq_elems = (int64_t)c->cfg.n_kv_heads * n_tokens * c->cfg.head_dim;
   // groups each sequence flushes in this call
@@ -705,6 +853,24 @@ kvq_status kvq_ledger(const kvq_config* cfg, const int64_t* tokens_per_seq, kvq_
 
 kvq_status kvq_bytes(const kvq_cache* c, kvq_bytes_t* out) {
   if (!c || !out) return fail(KVQ_EINVAL, "NULL argument");
+  if (c->segmented) {
+    // one Key scale per channel per segment, one Value scale per token
+    const int64_t H = c->cfg.n_kv_heads, D = c->cfg.head_dim;
+    int64_t code = 0, n_scales = 0, window = 0;
+    for (int b = 0; b < c->cfg.batch; ++b) {
+      code += 2 * H * (int64_t)c->quantized[b] * D * c->bits / 8;
+      n_scales += H * ((int64_t)c->seg_starts[b].size() * D + c->quantized[b]);
+      window += 2 * H * (int64_t)(c->total[b] - c->quantized[b]) * D;
+    }
+    out->code_bytes = code;
+    out->n_scales = n_scales;
+    out->scale_bytes = 4 * n_scales;
+    out->window_elems = window;
+    out->window_bytes = window * c->esize;
+    out->total = code + 4 * n_scales + window * c->esize;
+    out->allocated = (int64_t)c->arena_bytes;
+    return KVQ_OK;
+  }
   std::vector<int64_t> t(c->total.begin(), c->total.end());
   const kvq_status st = kvq_ledger(&c->cfg, t.data(), out);
   if (st == KVQ_OK) out->allocated = (int64_t)c->arena_bytes;
@@ -718,7 +884,7 @@ kvq_status kvq_seq_state(const kvq_cache* c, int32_t seq, kvq_seq_info* out) {
   out->quantized = c->quantized[seq];
   out->window = c->total[seq] - c->quantized[seq];
   out->last_flushed = c->last_flushed[seq];
-  out->n_groups = c->quantized[seq] / c->cfg.group;
+  out->n_groups = c->segmented ? (int64_t)c->seg_starts[seq].size() : c->quantized[seq] / c->cfg.group;
   out->capacity = c->cap[seq];
   return KVQ_OK;
 }
@@ -728,6 +894,7 @@ kvq_status kvq_export_pages(const kvq_cache* c, int32_t seq, int32_t kv_head, vo
   if (!c) return fail(KVQ_EINVAL, "NULL argument");
   if (seq < 0 || seq >= c->cfg.batch || kv_head < 0 || kv_head >= c->cfg.n_kv_heads)
     return fail(KVQ_EINVAL, "unit (%d, %d) out of range", seq, kv_head);
+  if (c->segmented) return fail(KVQ_EUNSUPPORTED, "a segmented cache has no group pages (use kvq_export_unit)");
   const size_t bytes = (size_t)(c->quantized[seq] / c->cfg.group) * c->geom.page_bytes;
   if (bytes == 0) return KVQ_OK;
   if (!host_dst) return fail(KVQ_EINVAL, "host_dst is NULL");
@@ -759,6 +926,7 @@ kvq_status kvq_release(kvq_cache* c, int32_t seq_begin, int32_t n_seqs) {
     // hands the blocks out in the same order again
     for (auto it = c->blocks[b].rbegin(); it != c->blocks[b].rend(); ++it) c->free_blocks.push_back(*it);
     c->blocks[b].clear();
+    if (c->segmented) c->seg_starts[b].clear();
     c->total[b] = c->quantized[b] = c->last_flushed[b] = 0;
   }
   return KVQ_OK;
@@ -777,11 +945,39 @@ kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, con
   if (seq < 0 || seq >= c->cfg.batch || kv_head < 0 || kv_head >= c->cfg.n_kv_heads)
     return fail(KVQ_EINVAL, "unit (%d, %d) out of range", seq, kv_head);
   const int D = c->cfg.head_dim, G = c->cfg.group, bits = c->bits;
-  const int64_t Q = c->quantized[seq], T = c->total[seq], P = Q / G;
+  const int64_t Q = c->quantized[seq], T = c->total[seq], P = c->segmented ? 0 : Q / G;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   std::vector<uint8_t> pages((size_t)P * c->geom.page_bytes);
-  kvq_status st = kvq_export_pages(c, seq, kv_head, pages.data(), pages.size(), stream);
+  kvq_status st = c->segmented ? KVQ_OK : kvq_export_pages(c, seq, kv_head, pages.data(), pages.size(), stream);
   if (st != KVQ_OK) return st;
+  if (c->segmented && Q > 0) {
+    // token-major rows: codes, the segment's Key scale row per token, Value scales
+    const int64_t row0 = ((int64_t)seq * c->cfg.n_kv_heads + kv_head) * c->seg.cap;
+    const int rb = c->seg.row_bytes;
+    std::vector<uint8_t> kc((size_t)Q * rb), vc((size_t)Q * rb);
+    std::vector<float> ks((size_t)Q * D), vs((size_t)Q);
+    cudaError_t e = cudaMemcpyAsync(kc.data(), c->seg.kcodes + row0 * rb, kc.size(), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(vc.data(), c->seg.vcodes + row0 * rb, vc.size(), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(ks.data(), c->seg.kscales + row0 * D, ks.size() * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(vs.data(), c->seg.vscales + row0, vs.size() * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "kvq_export_unit");
+    auto code_at = [&](const uint8_t* row, int ch) -> int8_t {
+      if (bits == 2) return (int8_t)((int)((row[ch / 4] >> (2 * (ch % 4))) & 0x3) - 2);
+      if (bits == 4) return (int8_t)((int)((row[ch / 2] >> (4 * (ch % 2))) & 0xF) - 8);
+      return (int8_t)((int)row[ch] - 128);
+    };
+    for (int64_t t = 0; t < Q; ++t)
+      for (int ch = 0; ch < D; ++ch) {
+        if (view->k_codes) view->k_codes[t * D + ch] = code_at(kc.data() + t * rb, ch);
+        if (view->v_codes) view->v_codes[t * D + ch] = code_at(vc.data() + t * rb, ch);
+      }
+    if (view->v_scales) memcpy(view->v_scales, vs.data(), vs.size() * 4);
+    if (view->k_scales)
+      for (size_t j = 0; j < c->seg_starts[seq].size(); ++j)
+        memcpy(view->k_scales + j * D, ks.data() + (size_t)c->seg_starts[seq][j] * D, (size_t)D * 4);
+  }
   // ring rows of the window, read whole and reordered on the host
   const size_t ring_bytes = (size_t)c->rcap * D * c->esize;
   std::vector<uint8_t> rk(ring_bytes), rv(ring_bytes);
@@ -889,6 +1085,35 @@ kvq_status kvq_restore(const kvq_cache* c, int32_t seq_begin, int32_t n_seqs, vo
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int64_t unit_elems = t_stride * c->cfg.head_dim;
   const int osz = out_dtype == KVQ_BF16 ? 2 : 4;
+  if (c->segmented) {
+    for (int s0 = seq_begin; s0 < seq_begin + n_seqs; s0 += kvq::kMaxSeqsPerLaunch) {
+      const int n = std::min(kvq::kMaxSeqsPerLaunch, seq_begin + n_seqs - s0);
+      kvq::RestoreParams p;
+      memset(&p, 0, sizeof p);
+      p.D = c->cfg.head_dim;
+      p.Hkv = c->cfg.n_kv_heads;
+      p.G = 1;
+      p.Rcap = c->rcap;
+      p.bits = c->bits;
+      p.eps = c->cfg.eps;
+      p.seg = c->seg;
+      p.ring_k = c->ring_k;
+      p.ring_v = c->ring_v;
+      p.in_dtype = c->cfg.dtype == KVQ_BF16 ? 0 : 1;
+      p.out_dtype = out_dtype == KVQ_BF16 ? 0 : 1;
+      const int64_t off = (int64_t)(s0 - seq_begin) * c->cfg.n_kv_heads * unit_elems * osz;
+      p.k_out = static_cast<uint8_t*>(k_out) + off;
+      p.v_out = static_cast<uint8_t*>(v_out) + off;
+      p.t_stride = t_stride;
+      p.seq_begin = s0;
+      p.n_seqs = n;
+      fill_counters(c, s0, n, p.ctr);
+      const cudaError_t e = kvq::launch_seg_restore(p, tmax, s);
+      if (e != cudaSuccess) return cuda_fail(e, "restore launch");
+      g_launches += 1;
+    }
+    return KVQ_OK;
+  }
   for (int s0 = seq_begin; s0 < seq_begin + n_seqs; s0 += kvq::kMaxSeqsPerLaunch) {
     const int n = std::min(kvq::kMaxSeqsPerLaunch, seq_begin + n_seqs - s0);
     kvq::RestoreParams p;

@@ -76,6 +76,36 @@ __host__ __device__ inline int64_t flush_groups(int64_t w, int64_t n, int64_t R,
   return tail < R + G ? 0 : (tail - R) / G;
 }
 
+// Segmented cache ("54. KV Cache Quantization Strategies", append_and_partition
+// verbatim): every append flushes its whole overflow as one segment with one
+// Key scale per channel over the segment's tokens.  Codes are token-major rows
+// (the Key row packing of a group page, for Keys and Values alike); each
+// token keeps its segment's Key scale row and its own Value scale.
+struct SegArrays {
+  uint8_t* kcodes;             // [batch][Hkv][cap][row_bytes]; null: not segmented
+  uint8_t* vcodes;
+  float* kscales;              // [batch][Hkv][cap][D]
+  float* vscales;              // [batch][Hkv][cap]
+  int64_t cap;                 // token rows per unit
+  int32_t row_bytes;           // D * bits / 8
+};
+
+struct SegFlushParams {
+  int32_t D, Hkv, R, qmax, bits;
+  float eps;
+  SegArrays seg;
+  uint32_t* kmax;              // [batch][Hkv][D] bits of the segment's Key absmax (zeroed first)
+  const void* ring_k;          // [batch][Hkv][R][D] (the window before the append)
+  const void* ring_v;
+  void* ring_k_out;            // the same rings (written by the window pass only)
+  void* ring_v_out;
+  const void* new_k;           // [n_seqs][Hkv][n][D]
+  const void* new_v;
+  int64_t n;
+  int32_t seq_begin, n_seqs;
+  SeqCounters old[kMaxSeqsPerLaunch];
+};
+
 // Shared memory of a flush CTA: the G x D fp32 tile, the Key and Value
 // scales, and the per-thread partial maxima of the Key absmax.
 constexpr int kAppendThreads = 256;
@@ -121,6 +151,7 @@ struct DecodeParams {
   int32_t grid_splits;         // quantized split columns in this launch (window column after)
   int32_t seq_begin, n_seqs;
   int32_t* status;
+  SegArrays seg;                // segmented caches (pages are then single tokens, G = 1)
   // dense restored cache (decode_dense_kernel only): [batch][Hkv][t_stride][D]
   const void* dense_k;
   const void* dense_v;
@@ -176,6 +207,7 @@ struct RestoreParams {
   void* k_out;                 // [n_seqs][Hkv][t_stride][D] (out dtype)
   void* v_out;
   int64_t t_stride;
+  SegArrays seg;               // segmented caches
   int32_t page_cols;           // pages of the longest unit (the launcher turns it into
                                // columns of page runs; the window column follows)
   int32_t seq_begin, n_seqs;
@@ -207,6 +239,10 @@ size_t decode_mma_smem_bytes(const DecodeParams& p);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supported);
 cudaError_t launch_restore(const RestoreParams& p, cudaStream_t s);
+// segmented caches: pass 1 (Key absmax, Value codes), pass 2 (Key codes), window copy
+cudaError_t launch_seg_flush(const SegFlushParams& p, int dtype, int64_t max_tokens, cudaStream_t s);
+cudaError_t launch_seg_window(const SegFlushParams& p, int dtype, cudaStream_t s);
+cudaError_t launch_seg_restore(const RestoreParams& p, int64_t max_tokens, cudaStream_t s);
 cudaError_t launch_compare(const CompareParams& p, int64_t rows, cudaStream_t s);
 
 }  // namespace kvq

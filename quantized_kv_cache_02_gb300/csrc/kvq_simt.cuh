@@ -141,6 +141,28 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
       }
       simt_token<CPL>(s, qv, kv, vv, g);
     }
+  } else if (p.seg.kcodes) {
+    // segmented cache: a "page" is one token of the token-major code rows,
+    // with its segment's Key scale row and its own Value scale
+    for (int64_t t = pg0 + warp; t < pg1; t += kSimtWarps) {
+      const int64_t row = unit * p.seg.cap + t;
+      const uint8_t* kr = p.seg.kcodes + row * p.seg.row_bytes;
+      const uint8_t* vr = p.seg.vcodes + row * p.seg.row_bytes;
+      const float* ks = p.seg.kscales + row * D;
+      const float vs = p.seg.vscales[row];
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        const int c = lane + 32 * k;
+        if (c < D) {
+          kv[k] = __fdiv_rn((float)key_code<BITS>(kr, 0, c, D), fmaxf(ks[c], p.eps));
+          vv[k] = __fdiv_rn((float)key_code<BITS>(vr, 0, c, D), fmaxf(vs, p.eps));
+        } else {
+          kv[k] = 0.f;
+          vv[k] = 0.f;
+        }
+      }
+      simt_token<CPL>(s, qv, kv, vv, g);
+    }
   } else {
     const int64_t ntok = (int64_t)(pg1 - pg0) * G;
     for (int64_t tt = warp; tt < ntok; tt += kSimtWarps) {

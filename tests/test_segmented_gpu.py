@@ -1,0 +1,188 @@
+"""The segmented cache on the GPU: the datawhale page's flush rule
+(append_and_partition, the whole overflow of an append as one segment)
+against the oracle's page rule (``group=None``), and the page's mechanism
+checks run on the GPU path.  The cache needs head_dim >= 16, so the page's
+tiny shapes use head_dim 16 with the page's token schedules.
+
+Codes, scales and counters bit-exact; restore bit-exact (fp32); attention
+within |d| <= 1e-3 + 1e-2 |ref|.
+"""
+
+import numpy as np
+import pytest
+
+from kvq_inputs import gen
+from oracle import kvq_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-3, 1e-2
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch
+
+
+@pytest.fixture(scope="module")
+def kvq(torch):
+    import quantized_kv_cache_02_gb300 as kvq
+    kvq.load_library()
+    return kvq
+
+
+def _r(*shape, seed=0):
+    return np.random.default_rng(seed).standard_normal(shape).astype(np.float32)
+
+
+class SegPair:
+    """A segmented GPU cache (batch 1) and the oracle's page-rule state."""
+
+    def __init__(self, kvq, torch, Hkv, Hq, D, R, qmax=7, capacity=512, dtype="fp32"):
+        self.torch = torch
+        self.tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+        self.cache = kvq.KVQCache(1, Hkv, Hq, D, R, 8, qmax, capacity, dtype=dtype, segmented=True)
+        self.state = None
+        self.R, self.qmax = R, qmax
+
+    def append(self, k, v):
+        """k, v: [Hkv, n, D] fp32 (values representable in the cache dtype)."""
+        dev = lambda a: self.torch.from_numpy(np.ascontiguousarray(a[None])).to("cuda").to(self.tdt).contiguous()
+        self.cache.append(dev(k), dev(v), 0)
+        self.state = O.append_and_partition(self.state, k[None], v[None], self.R, self.qmax, group=None)
+
+    def check_unit(self, h):
+        st = self.cache.seq_state(0)
+        assert (st["total"], st["quantized"]) == (self.state["total_tokens"], self.state["quantized_tokens"])
+        assert st["n_groups"] == len(self.state["key_q_segments"])
+        got = self.cache.export_unit(0, h)
+        if st["quantized"]:
+            kq = np.concatenate([s[0, h] for s in self.state["key_q_segments"]], axis=0)
+            vq = np.concatenate([s[0, h] for s in self.state["value_q_segments"]], axis=0)
+            ks = np.stack([s[0, h, 0] for s in self.state["key_scale_segments"]])
+            vs = np.concatenate([s[0, h, :, 0] for s in self.state["value_scale_segments"]])
+            np.testing.assert_array_equal(got["k_codes"], kq)
+            np.testing.assert_array_equal(got["v_codes"], vq)
+            np.testing.assert_array_equal(got["k_scales"].view(np.uint32), ks.view(np.uint32))
+            np.testing.assert_array_equal(got["v_scales"].view(np.uint32), vs.view(np.uint32))
+        np.testing.assert_array_equal(got["window_k"], self.state["key_residual"][0, h])
+        np.testing.assert_array_equal(got["window_v"], self.state["value_residual"][0, h])
+        return got
+
+    def attend(self, q):
+        qd = self.torch.from_numpy(np.ascontiguousarray(q[None])).to("cuda").to(self.tdt).contiguous()
+        got = self.cache.decode_attention(qd).cpu().numpy()[0].astype(np.float64)
+        ref = O.decode_attention(self.state, q[None])[0]
+        excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
+        assert excess.max() <= 0, f"|d| {np.abs(got - ref).max():.3e}"
+
+
+# ---- the page's mechanism checks, on the GPU path --------------------------
+
+def test_segment_scale_axes(kvq, torch):
+    """Key: one scale per channel over the segment; Value: one per token."""
+    pair = SegPair(kvq, torch, 2, 2, 16, 2)
+    pair.append(_r(2, 5, 16), _r(2, 5, 16, seed=1))   # 3 tokens flush as one segment
+    for h in range(2):
+        got = pair.check_unit(h)
+        assert got["k_scales"].shape == (1, 16) and got["v_scales"].shape == (3,)
+
+
+def test_segment_token_conservation(kvq, torch):
+    pair = SegPair(kvq, torch, 2, 2, 16, 4)
+    pair.append(_r(2, 3, 16), _r(2, 3, 16, seed=1))
+    pair.append(_r(2, 2, 16, seed=2), _r(2, 2, 16, seed=3))
+    st = pair.cache.seq_state(0)
+    assert st["total"] == 5 and st["quantized"] + st["window"] == 5
+    for h in range(2):
+        pair.check_unit(h)
+
+
+def test_segment_partition_residual_two(kvq, torch):
+    pair = SegPair(kvq, torch, 2, 2, 16, 2)
+    pair.append(_r(2, 3, 16), _r(2, 3, 16, seed=1))
+    pair.append(_r(2, 2, 16, seed=2), _r(2, 2, 16, seed=3))
+    st = pair.cache.seq_state(0)
+    assert (st["quantized"], st["window"], st["n_groups"]) == (3, 2, 2)
+    for h in range(2):
+        pair.check_unit(h)
+
+
+def test_segment_prefix_not_rewritten(kvq, torch):
+    pair = SegPair(kvq, torch, 1, 1, 16, 2)
+    pair.append(_r(1, 3, 16), _r(1, 3, 16, seed=1))
+    first = pair.check_unit(0)
+    pair.append(_r(1, 2, 16, seed=2) * 100, _r(1, 2, 16, seed=3))
+    after = pair.check_unit(0)
+    np.testing.assert_array_equal(after["k_codes"][:1], first["k_codes"])
+    np.testing.assert_array_equal(after["k_scales"][:1], first["k_scales"])
+    assert pair.cache.seq_state(0)["last_flushed"] == 2
+
+
+def test_segment_no_overflow(kvq, torch):
+    pair = SegPair(kvq, torch, 1, 1, 16, 4)
+    pair.append(_r(1, 1, 16), _r(1, 1, 16, seed=1))
+    pair.append(_r(1, 1, 16, seed=2), _r(1, 1, 16, seed=3))
+    st = pair.cache.seq_state(0)
+    assert (st["quantized"], st["last_flushed"], st["window"]) == (0, 0, 2)
+    pair.check_unit(0)
+    pair.attend(_r(1, 16, seed=4))
+
+
+def test_segment_zero_range(kvq, torch):
+    pair = SegPair(kvq, torch, 2, 2, 16, 2)
+    z = np.zeros((2, 6, 16), np.float32)
+    pair.append(z, z)
+    got = pair.check_unit(0)
+    assert np.isfinite(got["k_scales"]).all() and not got["k_codes"].any()
+    pair.attend(_r(2, 16, seed=5))
+
+
+def test_segment_ledger(kvq, torch):
+    pair = SegPair(kvq, torch, 2, 2, 16, 4, qmax=7)
+    pair.append(_r(2, 10, 16), _r(2, 10, 16, seed=1))       # segment of 6
+    pair.append(_r(2, 3, 16, seed=2), _r(2, 3, 16, seed=3))  # segment of 3
+    led = pair.cache.bytes()
+    Q, W = 9, 4
+    assert led["code_bytes"] == 2 * 2 * Q * 16 // 2
+    assert led["n_scales"] == 2 * (2 * 16 + Q)
+    assert led["window_elems"] == 2 * 2 * W * 16
+
+
+def test_segment_validation(kvq, torch):
+    with pytest.raises(kvq.KVQError) as e:
+        kvq.KVQCache(1, 1, 1, 16, 0, 8, 7, 64, dtype="fp32", segmented=True)   # R <= 0
+    assert e.value.status == kvq.binding.KVQ_EINVAL
+    pair = SegPair(kvq, torch, 1, 1, 16, 2)
+    with pytest.raises(kvq.KVQError) as e:
+        kvq.kvq_append(pair.cache.handle, 0, 0, 1, 0, 1, 0)                       # NULL inputs
+    assert e.value.status == kvq.binding.KVQ_EINVAL
+    with pytest.raises(kvq.KVQError) as e:
+        kvq.kvq_export_pages(pair.cache.handle, 0, 0, 0, 0, 0)
+    assert e.value.status == kvq.binding.KVQ_EUNSUPPORTED
+
+
+# ---- longer schedules: codes, restore and attention -----------------------
+
+@pytest.mark.parametrize("dtype,qmax,D", [("fp32", 7, 64), ("bf16", 7, 128), ("bf16", 127, 64), ("fp32", 1, 32)])
+def test_segment_schedule_matches_oracle(kvq, torch, dtype, qmax, D):
+    Hkv, Hq, R = 4, 8, 32
+    spec = gen.InputSpec(seed=41, n_kv_heads=Hkv, n_q_heads=Hq, head_dim=D, bf16=dtype == "bf16", spikes=True)
+    pair = SegPair(kvq, torch, Hkv, Hq, D, R, qmax=qmax, capacity=400, dtype=dtype)
+    t = 0
+    for n in [100] + [1] * 12 + [50, 7, 1, 1, 70]:
+        k, v = spec.kv_block(0, [0], t, n)
+        t += n
+        pair.append(k[0], v[0])
+        if n != 1 or t % 5 == 0:
+            pair.attend(spec.q_block(0, [0], t)[0])
+    for h in range(Hkv):
+        pair.check_unit(h)
+    k_out, v_out = pair.cache.restore(out_dtype="fp32")
+    K, V = O.restored_kv(pair.state)
+    np.testing.assert_array_equal(k_out.cpu().numpy()[0].view(np.uint32), K[0].view(np.uint32))
+    np.testing.assert_array_equal(v_out.cpu().numpy()[0].view(np.uint32), V[0].view(np.uint32))
+    assert pair.cache.device_status() == 0
