@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn µs/step & achieved HBM GB/s vs 8 TB/s (4-bit KV, Llama-3-8B shape)"
 WORKLOAD = dict(name="llama3_8b_decode_b32_ctx8192_4bit", layers=32, batch=32, n_kv_heads=8, n_q_heads=32,
                 head_dim=128, context=8192, residual_len=128, group=32, qmax=7, seed=2)
-SPLIT_KERNEL_SOURCE = os.path.join(ROOT, "quantized_kv_cache_02_gb300", "csrc", "kvq_decode_mma.cu")
+SPLIT_KERNEL_SOURCE = os.path.join(ROOT, "quantized_kv_cache_02_gb300", "csrc", "kvq_decode_mma.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 
 
@@ -254,7 +254,46 @@ def variants_layer(torch, kvq, w, dev, peak, steps=20):
                      "algorithmic_bytes_per_launch": int(nbytes), "status": cache.device_status()}
         del cache
     out["long_video"] = long_video_layer(torch, kvq, peak)
+    out["segmented_4bit"] = segmented_layer(torch, kvq, w, dev, peak)
     return out
+
+
+def segmented_layer(torch, kvq, w, dev, peak, batch=8, steps=10):
+    """The segmented cache (the page's flush rule: each append's overflow is
+    one segment) at the benchmark's head shape, 8 sequences of 8192 tokens:
+    one prefill segment, then one-token segments.  Its decode runs on the
+    CUDA-core kernel; each token also carries its segment's Key scale row."""
+    H, Hq, D, R = w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["residual_len"]
+    T0 = w["context"]
+    cache = kvq.KVQCache(batch, H, Hq, D, R, w["group"], w["qmax"], T0 + 3 + steps + 8, segmented=True)
+    K, V = dev.kv_block(0, 0, batch, 0, T0)
+    cache.append(K, V, 0)
+    del K, V
+    q = dev.q_block(0, 0, batch, 0)
+    o = torch.empty(batch, Hq, D, dtype=torch.float32, device="cuda")
+    for s in range(3):
+        Kn, Vn = dev.kv_block(0, 0, batch, T0 + s, 1)
+        cache.append(Kn, Vn, 0)
+        cache.decode_attention(q, out=o)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:  # torch creates the CUDA event on first record
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    for a, b in evs:
+        cache.decode_attention(q, out=o, split_start=a.cuda_event, split_stop=b.cuda_event)
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / steps
+    st = [cache.seq_state(b) for b in range(batch)]
+    Q = sum(x["quantized"] for x in st)
+    W = sum(x["window"] for x in st)
+    g = Hq // H
+    # codes (K and V), the per-token Key scale row and Value scale, window, q
+    nbytes = H * (Q * (D + 4 * D + 4) + W * 2 * D * 2 + batch * g * D * 2)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": f"segmented cache, {batch} x 8192 tokens, Llama head shape, 4-bit",
+            "split_ms": round(ms, 5), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "algorithmic_bytes_per_launch": int(nbytes), "status": cache.device_status()}
 
 
 LONG_VIDEO = dict(n_kv_heads=8, n_q_heads=32, head_dim=128, residual_len=256, group=128, qmax=7, chunk=14400,
