@@ -248,6 +248,18 @@ kvq_status kvq_decode_attention(kvq_cache* cache, const void* q, float* out, voi
 kvq_status kvq_decode_attention_ex(kvq_cache* cache, const void* q, float* out, void* stream,
                                    const kvq_decode_opts* opts);
 
+/* One decode step: append one new token to every sequence, then the decode
+ * attention -- kvq_append(n_tokens = 1, all sequences) followed by
+ * kvq_decode_attention_ex, with the same results.  new_k, new_v: device
+ * [batch][n_kv_heads][1][head_dim] of the cache dtype; q, out as in
+ * kvq_decode_attention; opts may be NULL.  On the tensor-core path the
+ * append's window copy is folded into the split kernel: each window item
+ * attends the step's token straight from new_k / new_v and stores it in its
+ * ring row, so a step without a flush is two launches instead of three.
+ * Errors as kvq_append and kvq_decode_attention, before any launch. */
+kvq_status kvq_decode_step(kvq_cache* cache, const void* new_k, const void* new_v, const void* q, float* out,
+                           void* stream, const kvq_decode_opts* opts);
+
 /* No counterpart in the source pages: an addition for callers that cannot
  * allocate device memory when they decode (a plugin whose host framework owns
  * every device allocation, a deployment that reserves all memory once at

@@ -24,7 +24,7 @@ EXPORTED = ("kvq_required_bytes", "kvq_create", "kvq_append", "kvq_decode_attent
             "kvq_export_pages", "kvq_device_status", "kvq_page_bytes", "kvq_kernel_launches", "kvq_destroy",
             "kvq_last_error", "kvq_decode_attention_noalloc", "kvq_restore", "kvq_dense_decode_attention",
             "kvq_compare", "kvq_required_bytes_paged", "kvq_create_paged", "kvq_release", "kvq_pool_state",
-            "kvq_required_bytes_segmented", "kvq_create_segmented")
+            "kvq_required_bytes_segmented", "kvq_create_segmented", "kvq_decode_step")
 
 
 class kvq_config(ctypes.Structure):
@@ -92,6 +92,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "kvq_page_bytes": ([P(kvq_config)], SZ),
         "kvq_kernel_launches": ([], ctypes.c_uint64),
         "kvq_decode_attention_noalloc": ([V, V, V, V], ctypes.c_int),
+        "kvq_decode_step": ([V, V, V, V, V, V, P(kvq_decode_opts)], ctypes.c_int),
         "kvq_restore": ([V, I32, I32, V, V, I64, ctypes.c_int, V], ctypes.c_int),
         "kvq_dense_decode_attention": ([V, V, V, I64, V, V, V], ctypes.c_int),
         "kvq_compare": ([V, V, I64, I32, I64, I32, ctypes.c_int, I32, ctypes.c_float, I32, V, P(kvq_compare_t), V],
@@ -201,6 +202,11 @@ def kvq_decode_attention_ex(handle, q_ptr, out_ptr, stream, kernel=0, chunk_page
                             split_stop=None) -> None:
     opts = kvq_decode_opts(kernel, chunk_pages, split_start, split_stop)
     _check(load_library().kvq_decode_attention_ex(handle, q_ptr, out_ptr, stream, ctypes.byref(opts)))
+
+
+def kvq_decode_step(handle, k_ptr, v_ptr, q_ptr, out_ptr, stream, kernel=0, split_start=None, split_stop=None):
+    opts = kvq_decode_opts(kernel, 0, split_start, split_stop)
+    _check(load_library().kvq_decode_step(handle, k_ptr, v_ptr, q_ptr, out_ptr, stream, ctypes.byref(opts)))
 
 
 def kvq_decode_attention_noalloc(handle, q_ptr, out_ptr, stream) -> None:
@@ -374,6 +380,20 @@ class KVQCache:
             out = self.torch.empty(shape, dtype=self.torch.float32, device=self.device)
         kvq_dense_decode_attention(self.handle, k.data_ptr(), v.data_ptr(), k.shape[2], q.data_ptr(), out.data_ptr(),
                                    self._stream())
+        return out
+
+    def decode_step(self, new_k, new_v, q, out=None, kernel=0, split_start=None, split_stop=None):
+        """Append one token per sequence (new_k, new_v: [batch, n_kv_heads, 1,
+        head_dim]) and attend with q [batch, n_q_heads, head_dim]."""
+        shape = (self.cfg.batch, self.cfg.n_kv_heads, 1, self.cfg.head_dim)
+        self._check_input(new_k, shape)
+        self._check_input(new_v, shape)
+        qshape = (self.cfg.batch, self.cfg.n_q_heads, self.cfg.head_dim)
+        self._check_input(q, qshape)
+        if out is None:
+            out = self.torch.empty(qshape, dtype=self.torch.float32, device=self.device)
+        kvq_decode_step(self.handle, new_k.data_ptr(), new_v.data_ptr(), q.data_ptr(), out.data_ptr(), self._stream(),
+                        kernel, split_start, split_stop)
         return out
 
     def bytes(self):

@@ -21,9 +21,13 @@ cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supp
   return p.D == 64 ? launch_dense_g<64>(p, cols, s) : launch_dense_g<128>(p, cols, s);
 }
 
+bool decode_mma_supported(const DecodeParams& p) {
+  return (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g >= 2 && p.g <= kMaxGqa &&
+         decode_mma_smem_bytes(p) <= kMaxSmem;
+}
+
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported) {
-  *supported = (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g >= 2 && p.g <= kMaxGqa &&
-               decode_mma_smem_bytes(p) <= kMaxSmem;
+  *supported = decode_mma_supported(p);
   if (!*supported) return cudaSuccess;
   return p.bits == 2 ? launch_mma_bits2(p, s) : p.bits == 4 ? launch_mma_bits4(p, s) : launch_mma_bits8(p, s);
 }

@@ -585,7 +585,8 @@ template <int D, int GP, int NBUF, bool RING>
 __device__ __forceinline__ void rows_mma(const DecodeParams& p, const __nv_bfloat16* kbase,
                                          const __nv_bfloat16* vbase, int64_t row0, int ring, int n,
                                          const __nv_bfloat16* qunit, int lane, int warp, int gid, int tig,
-                                         uint8_t* wbuf, WarpState<D>& st) {
+                                         uint8_t* wbuf, WarpState<D>& st, const __nv_bfloat16* last_k = nullptr,
+                                         const __nv_bfloat16* last_v = nullptr) {
   constexpr int kRow = D * 2;             // bytes of one bf16 row
   constexpr int kChunks = kRow / 16;      // 16-byte chunks per row
   constexpr int kBuf = 32 * kRow;         // one step: 16 K rows + 16 V rows
@@ -610,8 +611,10 @@ __device__ __forceinline__ void rows_mma(const DecodeParams& p, const __nv_bfloa
       const int64_t t = row0 + t0 + (valid ? r : 0);
       const int64_t row = RING ? t % ring : t;
       const uint32_t off = r * kRow + ((c ^ (r & 7)) * 16);
-      cp_async16(kb + off, kbase + row * D + c * 8, valid ? 16u : 0u);
-      cp_async16(vb + off, vbase + row * D + c * 8, valid ? 16u : 0u);
+      // the run's last row may come from elsewhere (this step's input token)
+      const bool last = last_k != nullptr && valid && t0 + r == n - 1;
+      cp_async16(kb + off, last ? last_k + c * 8 : kbase + row * D + c * 8, valid ? 16u : 0u);
+      cp_async16(vb + off, last ? last_v + c * 8 : vbase + row * D + c * 8, valid ? 16u : 0u);
     }
     cp_async_commit();
   };
@@ -839,10 +842,25 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   if (win) {
     const int64_t unit = (int64_t)b * p.Hkv + h;
     const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-    rows_mma<D, GP, 1, true>(p, reinterpret_cast<const __nv_bfloat16*>(p.ring_k) + unit * p.Rcap * D,
-                    reinterpret_cast<const __nv_bfloat16*>(p.ring_v) + unit * p.Rcap * D, Q0, p.Rcap,
-                    (int)(T0 - Q0), reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * g) * D,
-                    lane, warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st);
+    __nv_bfloat16* rk = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.ring_k)) + unit * p.Rcap * D;
+    __nv_bfloat16* rv = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.ring_v)) + unit * p.Rcap * D;
+    const __nv_bfloat16* lk = nullptr;
+    const __nv_bfloat16* lv = nullptr;
+    if (p.step_k) {
+      // this step's token: attended from the input and stored in its ring row
+      // (row (T0 - 1) mod Rcap holds no other token of the window, so no copy
+      // of this launch reads it)
+      lk = reinterpret_cast<const __nv_bfloat16*>(p.step_k) + ((int64_t)i * p.Hkv + h) * D;
+      lv = reinterpret_cast<const __nv_bfloat16*>(p.step_v) + ((int64_t)i * p.Hkv + h) * D;
+      const int64_t row = ((T0 - 1) % p.Rcap) * D;
+      for (int c = threadIdx.x; c < D / 8; c += blockDim.x) {
+        reinterpret_cast<uint4*>(rk + row)[c] = reinterpret_cast<const uint4*>(lk)[c];
+        reinterpret_cast<uint4*>(rv + row)[c] = reinterpret_cast<const uint4*>(lv)[c];
+      }
+    }
+    rows_mma<D, GP, 1, true>(p, rk, rv, Q0, p.Rcap, (int)(T0 - Q0),
+                             reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * g) * D, lane,
+                             warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st, lk, lv);
   } else {
   // queries of the GP column heads (head n % g for the padding columns, so every
   // value stays finite), pre-scaled, in shared memory: channel c of head n goes

@@ -508,8 +508,10 @@ kvq_status kvq_create_segmented(const kvq_config* cfg, const int64_t* capacity_p
 
 void kvq_destroy(kvq_cache* cache) { delete cache; }
 
-kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens, int32_t seq_begin,
-                      int32_t n_seqs, void* stream) {
+// The append; window_copy = false leaves the new tokens out of the rings
+// (kvq_decode_step's split kernel stores them) and launches the flushes only.
+static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens,
+                              int32_t seq_begin, int32_t n_seqs, void* stream, bool window_copy) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
   if (n_tokens <= 0) return fail(KVQ_EINVAL, "n_tokens must be positive (got %lld)", (long long)n_tokens);
   if (n_seqs <= 0 || seq_begin < 0 || seq_begin + (int64_t)n_seqs > c->cfg.batch)
@@ -608,8 +610,15 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
       // when the old window plus the new tokens exceed the ring
       if (F > 0 && w + n_tokens > c->rcap) overlap = true;
     }
-    cudaError_t e;
-    if (!overlap) {
+    cudaError_t e = cudaSuccess;
+    if (!window_copy) {
+      p.flush_blocks = (int)fmax;
+      p.window_blocks = 0;
+      if (fmax > 0) {
+        e = kvq::launch_append(p, c->cfg.dtype, s);
+        g_launches += 1;
+      }
+    } else if (!overlap) {
       p.flush_blocks = (int)fmax;
       p.window_blocks = 1;
       e = kvq::launch_append(p, c->cfg.dtype, s);
@@ -638,8 +647,15 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
   return KVQ_OK;
 }
 
-kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void* stream,
-                                   const kvq_decode_opts* opts) {
+kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens, int32_t seq_begin,
+                      int32_t n_seqs, void* stream) {
+  return append_impl(c, new_k, new_v, n_tokens, seq_begin, n_seqs, stream, true);
+}
+
+// The decode; step_k / step_v (kvq_decode_step) hand the split kernel's window
+// items this step's tokens, which are then not in the rings yet.
+static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* stream, const kvq_decode_opts* opts,
+                              const void* step_k, const void* step_v) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
   const int kernel = opts ? opts->kernel : 0;
@@ -671,6 +687,11 @@ kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void
     p.grid_splits = bt.grid;
     p.seq_begin = bt.s0;
     p.n_seqs = bt.n;
+    if (step_k) {
+      const int64_t off = (int64_t)bt.s0 * c->cfg.n_kv_heads * c->cfg.head_dim * c->esize;
+      p.step_k = static_cast<const uint8_t*>(step_k) + off;
+      p.step_v = static_cast<const uint8_t*>(step_v) + off;
+    }
     fill_counters(c, bt.s0, bt.n, p.ctr);
     cudaError_t e = cudaSuccess;
     int supported = 0;
@@ -710,8 +731,36 @@ kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void
   return KVQ_OK;
 }
 
+kvq_status kvq_decode_attention_ex(kvq_cache* c, const void* q, float* out, void* stream,
+                                   const kvq_decode_opts* opts) {
+  return decode_impl(c, q, out, stream, opts, nullptr, nullptr);
+}
+
 kvq_status kvq_decode_attention(kvq_cache* c, const void* q, float* out, void* stream) {
   return kvq_decode_attention_ex(c, q, out, stream, nullptr);
+}
+
+kvq_status kvq_decode_step(kvq_cache* c, const void* new_k, const void* new_v, const void* q, float* out,
+                           void* stream, const kvq_decode_opts* opts) {
+  if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (!aligned16(new_k) || !aligned16(new_v) || !aligned16(q) || !aligned16(out))
+    return fail(KVQ_EINVAL, "new_k / new_v / q / out must be non-NULL 16-byte aligned device pointers");
+  const int kernel = opts ? opts->kernel : 0;
+  // the tensor-core kernel takes the step's tokens from the input; any other
+  // path runs the plain append and decode
+  bool fuse = kernel != 1 && !c->segmented && c->cfg.dtype == KVQ_BF16 &&
+              (c->cfg.head_dim == 64 || c->cfg.head_dim == 128) && c->cfg.group % 32 == 0 && c->g >= 2;
+  if (fuse) {
+    kvq::DecodeParams p;
+    base_decode_params(c, &p);
+    fuse = kvq::decode_mma_supported(p);
+  }
+  if (!fuse) {
+    const kvq_status st = kvq_append(c, new_k, new_v, 1, 0, c->cfg.batch, stream);
+    return st != KVQ_OK ? st : decode_impl(c, q, out, stream, opts, nullptr, nullptr);
+  }
+  const kvq_status st = append_impl(c, new_k, new_v, 1, 0, c->cfg.batch, stream, false);
+  return st != KVQ_OK ? st : decode_impl(c, q, out, stream, opts, new_k, new_v);
 }
 
 }  // extern "C"

@@ -152,6 +152,10 @@ struct DecodeParams {
   int32_t seq_begin, n_seqs;
   int32_t* status;
   SegArrays seg;                // segmented caches (pages are then single tokens, G = 1)
+  // kvq_decode_step: this step's token per (sequence, KV head), [n_seqs][Hkv][D];
+  // the window item reads it from here and writes it into its ring row
+  const void* step_k;
+  const void* step_v;
   // dense restored cache (decode_dense_kernel only): [batch][Hkv][t_stride][D]
   const void* dense_k;
   const void* dense_v;
@@ -236,6 +240,7 @@ cudaError_t launch_mma_bits2(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_mma_bits4(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_mma_bits8(const DecodeParams& p, cudaStream_t s);
 size_t decode_mma_smem_bytes(const DecodeParams& p);
+bool decode_mma_supported(const DecodeParams& p);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supported);
 cudaError_t launch_restore(const RestoreParams& p, cudaStream_t s);
