@@ -29,6 +29,54 @@ __device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
   return (int)r;
 }
 
+// code = clamp(rint(x * scale), -qmax, qmax) with one rounding conversion:
+// |x| <= absmax makes |x * scale| <= qmax, so the conversion cannot overflow,
+// and round-to-nearest-even conversion is rint.
+__device__ __forceinline__ int quantize_int(float x, float scale, int qmax) {
+  const int r = __float2int_rn(__fmul_rn(x, scale));
+  return min(max(r, -qmax), qmax);
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// 16 bytes of elements -> fp32 values
+__device__ __forceinline__ void unpack16(const uint4& raw, float (&x)[4]) {
+  const float* f = reinterpret_cast<const float*>(&raw);
+  x[0] = f[0];
+  x[1] = f[1];
+  x[2] = f[2];
+  x[3] = f[3];
+}
+__device__ __forceinline__ void unpack16(const uint4& raw, float (&x)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 f = __bfloat1622float2(h[e]);
+    x[2 * e] = f.x;
+    x[2 * e + 1] = f.y;
+  }
+}
+
+// N consecutive elements of shared memory as fp32 (vector loads)
+template <typename T, int N>
+__device__ __forceinline__ void load_elems(const T* src, float (&x)[N]) {
+  constexpr int kBytes = N * (int)sizeof(T);
+  if constexpr (kBytes % 16 == 0) {
+    constexpr int kPer = 16 / (int)sizeof(T);
+#pragma unroll
+    for (int i = 0; i < kBytes / 16; ++i) {
+      float y[kPer];
+      unpack16(reinterpret_cast<const uint4*>(src)[i], y);
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) x[i * kPer + e] = y[e];
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < N; ++e) x[e] = to_f32(src[e]);
+  }
+}
+
 // 16 bytes of elements -> fp32 into shared memory.
 __device__ __forceinline__ void store_f32(float* dst, const uint4& raw, float) {
   const float* f = reinterpret_cast<const float*>(&raw);
@@ -82,15 +130,16 @@ __device__ void load_group(float* tile, const T* ring, const T* input, int t_fir
   }
 }
 
-template <typename T, int BITS>
-__global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendParams p) {
+// DC: head_dim as a compile-time constant (64, 128), or 0 for any other.
+template <typename T, int BITS, int DC>
+__global__ void __launch_bounds__(kAppendThreads, 3) append_kernel(const AppendParams p) {
   extern __shared__ float smem[];
   pdl_wait();
   pdl_release();
   const int i = blockIdx.y;
   const int h = blockIdx.z;
   const int b = p.seq_begin + i;
-  const int D = p.D, G = p.G, Rcap = p.Rcap;
+  const int D = DC ? DC : p.D, G = p.G, Rcap = p.Rcap;
   // token counts fit in 32 bits (capacities are below 2^31)
   const int T0 = p.old[i].total;
   const int Q0 = p.old[i].quantized;
@@ -157,102 +206,137 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
   } else {
     page = p.pages + page_offset(p.map, geom.page_bytes, b, h, t_first / G);
   }
-  float* tile = smem;
-  float* sK = tile + G * D;
-  float* sV = sK + D;
+  // The group's rows are staged in shared memory in the input dtype.  Each
+  // thread loads one 16-byte column of kVec channels, stepping over rows with
+  // four loads in flight, and keeps the column's Key absmax in registers; the
+  // Value absmax of a row is reduced over the threads of the row with shuffles.
+  constexpr int kVec = 16 / sizeof(T);
+  constexpr int kBatch = 8;
+  T* tileT = reinterpret_cast<T*>(smem);                         // [G][D]
+  float* sK = reinterpret_cast<float*>(tileT + (size_t)G * D);   // [D] Key scales
+  float* sV = sK + D;                                            // [G] Value scales
+  float* part = sV + G;                                          // [rows_per_pass][D] partial Key maxima
+  const int qmax_i = p.qmax;
   const float qmax = (float)p.qmax;
   constexpr int kBias = BITS == 2 ? 2 : BITS == 4 ? 8 : 128;  // stored offset binary: code + bias
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int per_row = D / kVec;
+  const int rows_per_pass = blockDim.x / per_row;
+  const bool act = (int)threadIdx.x < rows_per_pass * per_row;
+  const int r0 = act ? threadIdx.x / per_row : 0, col = act ? (threadIdx.x - r0 * per_row) * kVec : 0;
+  const int ring_row0 = t_first % Rcap;
+  // rows of a thread in one pass of the batch loop: the same count for every
+  // lane of a warp, so the shuffles below see the whole warp
+  auto load_rows = [&](const T* ring, const T* input, auto&& per_row_fn) {
+    for (int base = 0; base < G; base += kBatch * rows_per_pass) {
+      uint4 v[kBatch];
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int r = base + r0 + k * rows_per_pass;
+        if (act && r < G) {
+          const int t = t_first + r;
+          const T* src = t < T0 ? ring + (size_t)(ring_row0 + r) * D + col : input + (size_t)(t - T0) * D + col;
+          v[k] = *reinterpret_cast<const uint4*>(src);
+        } else {
+          v[k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) {
+        const int r = base + r0 + k * rows_per_pass;
+        if (act && r < G) *reinterpret_cast<uint4*>(tileT + (size_t)r * D + col) = v[k];
+        float x[kVec];
+        unpack16(v[k], x);
+        per_row_fn(r, x);
+      }
+    }
+  };
 
   // ---- Key: per-channel absmax over the group's tokens --------------------
-  load_group<T>(tile, ring_k, in_k, t_first, T0, G, D, Rcap);
-  __syncthreads();
   {
-    // every thread takes one channel over a share of the tokens (four
-    // independent max chains), then the shares of a channel are merged
-    const int parts = blockDim.x / D > 0 ? blockDim.x / D : 1;
-    float* part_max = sV + G;  // [parts][D] (parts * D <= max(blockDim, D) floats)
-    for (int c0 = 0; c0 < D; c0 += blockDim.x) {
-      const int c = c0 + (int)threadIdx.x % D, part = (int)threadIdx.x / D;
-      if (c < D && part < parts) {
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        int t = part;
-        for (; t + 3 * parts < G; t += 4 * parts) {
-          a0 = fmaxf(a0, fabsf(tile[t * D + c]));
-          a1 = fmaxf(a1, fabsf(tile[(t + parts) * D + c]));
-          a2 = fmaxf(a2, fabsf(tile[(t + 2 * parts) * D + c]));
-          a3 = fmaxf(a3, fabsf(tile[(t + 3 * parts) * D + c]));
-        }
-        for (; t < G; t += parts) a0 = fmaxf(a0, fabsf(tile[t * D + c]));
-        part_max[part * D + c] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-      }
+    float amax[kVec];
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) amax[e] = 0.f;
+    load_rows(ring_k, in_k, [&](int, const float (&x)[kVec]) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) amax[e] = fmaxf(amax[e], fabsf(x[e]));
+    });
+    if (act) {
+#pragma unroll
+      for (int e = 0; e < kVec; ++e) part[r0 * D + col + e] = amax[e];
     }
     __syncthreads();
     for (int c = threadIdx.x; c < D; c += blockDim.x) {
       float a = 0.f;
-      for (int k = 0; k < parts; ++k) a = fmaxf(a, part_max[k * D + c]);
+      for (int r = 0; r < rows_per_pass; ++r) a = fmaxf(a, part[r * D + c]);
       sK[c] = __fdiv_rn(qmax, fmaxf(a, p.eps));
     }
+    __syncthreads();
   }
-  __syncthreads();
   {
     // rows of D*BITS/8 bytes, written as 32-bit words; each thread keeps one
-    // word column and steps over the token rows
+    // word column (and its scales) and steps over the token rows
     constexpr int kPerWord = 32 / BITS;  // codes per 32-bit word
     const int words_per_row = D / kPerWord;
-    const int rows_per_pass = blockDim.x / words_per_row;
+    const int rows_pp = blockDim.x / words_per_row;
     uint32_t* kc = reinterpret_cast<uint32_t*>(page);
-    if ((int)threadIdx.x < rows_per_pass * words_per_row) {
+    if ((int)threadIdx.x < rows_pp * words_per_row) {
       const int t0 = threadIdx.x / words_per_row, w = threadIdx.x - t0 * words_per_row;
-      // the word's channels as float4 reads (consecutive threads, consecutive addresses)
-      const float4* sc = reinterpret_cast<const float4*>(sK + w * kPerWord);
-      float4 s4[kPerWord / 4];
+      float sc[kPerWord];
 #pragma unroll
-      for (int k4 = 0; k4 < kPerWord / 4; ++k4) s4[k4] = sc[k4];
-      for (int t = t0; t < G; t += rows_per_pass) {
-        const float4* src = reinterpret_cast<const float4*>(tile + t * D + w * kPerWord);
+      for (int k = 0; k < kPerWord; ++k) sc[k] = sK[w * kPerWord + k];
+      for (int t = t0; t < G; t += rows_pp) {
+        float x[kPerWord];
+        load_elems<T, kPerWord>(tileT + (size_t)t * D + w * kPerWord, x);
         uint32_t word = 0;
 #pragma unroll
-        for (int k4 = 0; k4 < kPerWord / 4; ++k4) {
-          const float4 x = src[k4];
-          const int c0 = quantize_one(x.x, s4[k4].x, qmax), c1 = quantize_one(x.y, s4[k4].y, qmax);
-          const int c2 = quantize_one(x.z, s4[k4].z, qmax), c3 = quantize_one(x.w, s4[k4].w, qmax);
-          word |= ((uint32_t)(c0 + kBias)) << (BITS * (4 * k4 + 0));
-          word |= ((uint32_t)(c1 + kBias)) << (BITS * (4 * k4 + 1));
-          word |= ((uint32_t)(c2 + kBias)) << (BITS * (4 * k4 + 2));
-          word |= ((uint32_t)(c3 + kBias)) << (BITS * (4 * k4 + 3));
-        }
+        for (int k = 0; k < kPerWord; ++k)
+          word |= (uint32_t)(quantize_int(x[k], sc[k], qmax_i) + kBias) << (BITS * k);
         kc[t * words_per_row + w] = word;
       }
     }
     float* ks = reinterpret_cast<float*>(page + geom.kscale_off);
     for (int c = threadIdx.x; c < D; c += blockDim.x) ks[c] = sK[c];
   }
-  __syncthreads();
+  __syncthreads();  // the tile is rewritten with the Values
 
   // ---- Value: per-token absmax over head_dim -----------------------------
-  load_group<T>(tile, ring_v, in_v, t_first, T0, G, D, Rcap);
-  __syncthreads();
-  for (int t = warp; t < G; t += nwarps) {
-    float a = 0.f;
-    for (int c = lane; c < D; c += 32) a = fmaxf(a, fabsf(tile[t * D + c]));
+  {
+    const bool shuffle_rows = (per_row & (per_row - 1)) == 0 && per_row <= 32;
+    uint32_t* rmax = reinterpret_cast<uint32_t*>(part);  // [G] bits of row maxima (other widths)
+    if (!shuffle_rows) {
+      for (int t = threadIdx.x; t < G; t += blockDim.x) rmax[t] = 0u;
+      __syncthreads();
+    }
+    load_rows(ring_v, in_v, [&](int r, const float (&x)[kVec]) {
+      float a = 0.f;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    if (lane == 0) sV[t] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+      for (int e = 0; e < kVec; ++e) a = fmaxf(a, fabsf(x[e]));
+      if (shuffle_rows) {
+        for (int o = 1; o < per_row; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (act && r < G && col == 0) sV[r] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+      } else if (act && r < G) {
+        atomicMax(rmax + r, __float_as_uint(a));
+      }
+    });
+    __syncthreads();
+    if (!shuffle_rows) {
+      for (int t = threadIdx.x; t < G; t += blockDim.x) sV[t] = __fdiv_rn(qmax, fmaxf(__uint_as_float(rmax[t]), p.eps));
+      __syncthreads();
+    }
   }
-  __syncthreads();
   {
     // channel fastest across threads (each token row is read at consecutive
     // addresses); each thread keeps one channel and steps over the words
     uint8_t* vbase = page + geom.code_bytes;
     const int n_sub = (G + 31) / 32;
     const int per_pass = blockDim.x / D > 0 ? blockDim.x / D : 1;  // words of a channel per pass
-    const bool active = (int)threadIdx.x < per_pass * D;
+    const bool vact = (int)threadIdx.x < per_pass * D;
     const int c_me = (int)threadIdx.x % D, w_me = (int)threadIdx.x / D;
-    for (int st = 0; st < n_sub; ++st) {
+    auto x_at = [&](int tok, int c) { return to_f32(tileT[(size_t)tok * D + c]); };
+    for (int st = 0; st < n_sub && vact; ++st) {
       const int n_st = min(32, G - 32 * st);
       uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
-      for (int c0 = 0; c0 < D && active; c0 += blockDim.x) {
+      for (int c0 = 0; c0 < D; c0 += blockDim.x) {
         const int c = c0 + c_me;
         if (c >= D) break;
         if (BITS == 2) {
@@ -264,8 +348,8 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 #pragma unroll
             for (int f = 0; f < 4; ++f) {
               const int te = 32 * st + 8 * w + 2 * f;
-              piece |= ((uint32_t)(quantize_one(tile[te * D + c], sV[te], qmax) + kBias)) << (2 * f);
-              piece |= ((uint32_t)(quantize_one(tile[(te + 1) * D + c], sV[te + 1], qmax) + kBias)) << (8 + 2 * f);
+              piece |= (uint32_t)(quantize_int(x_at(te, c), sV[te], qmax_i) + kBias) << (2 * f);
+              piece |= (uint32_t)(quantize_int(x_at(te + 1, c), sV[te + 1], qmax_i) + kBias) << (8 + 2 * f);
             }
             vp[c * np + w] = (uint16_t)piece;
           }
@@ -276,8 +360,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 #pragma unroll
             for (int jn = 0; jn < 8; ++jn) {
               const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
-              const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
-              word |= ((uint32_t)(code + kBias)) << (4 * jn);
+              word |= (uint32_t)(quantize_int(x_at(tok, c), sV[tok], qmax_i) + kBias) << (4 * jn);
             }
             vc[c * nw + w] = word;
           }
@@ -288,8 +371,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kernel(const AppendPara
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int tok = 32 * st + 4 * w + k;
-              const int code = quantize_one(tile[tok * D + c], sV[tok], qmax);
-              word |= ((uint32_t)(code + kBias)) << (8 * k);
+              word |= (uint32_t)(quantize_int(x_at(tok, c), sV[tok], qmax_i) + kBias) << (8 * k);
             }
             vc[c * nw + w] = word;
           }
@@ -376,14 +458,21 @@ __global__ void __launch_bounds__(kCompareThreads) compare_kernel(const CompareP
 template <typename T, int BITS>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
   const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
-  const size_t smem = p.flush_blocks ? flush_smem_bytes(p.G, p.D) : 0;
-  return launch_pdl(append_kernel<T, BITS>, grid, dim3(kAppendThreads), smem, s, p);
+  const size_t smem = p.flush_blocks ? flush_smem_bytes(p.G, p.D, (int)sizeof(T)) : 0;
+  if (p.D == 128) return launch_pdl(append_kernel<T, BITS, 128>, grid, dim3(kAppendThreads), smem, s, p);
+  if (p.D == 64) return launch_pdl(append_kernel<T, BITS, 64>, grid, dim3(kAppendThreads), smem, s, p);
+  return launch_pdl(append_kernel<T, BITS, 0>, grid, dim3(kAppendThreads), smem, s, p);
 }
 
 template <typename T, int BITS>
 cudaError_t configure_t(size_t smem) {
-  return cudaFuncSetAttribute(append_kernel<T, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(append_kernel<T, BITS, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_kernel<T, BITS, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(append_kernel<T, BITS, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return e;
 }
 
 }  // namespace

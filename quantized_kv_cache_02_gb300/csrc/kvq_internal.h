@@ -106,12 +106,15 @@ struct SegFlushParams {
   SeqCounters old[kMaxSeqsPerLaunch];
 };
 
-// Shared memory of a flush CTA: the G x D fp32 tile, the Key and Value
-// scales, and the per-thread partial maxima of the Key absmax.
+// Shared memory of a flush CTA: the G x D tile in the input dtype (esize
+// bytes an element), the Key and Value scales, and the partial Key maxima of
+// the threads' 16-byte columns (rows per pass x D floats; 16 / esize channels
+// a column, kAppendThreads threads).
 constexpr int kAppendThreads = 256;
-inline size_t flush_smem_bytes(int G, int D) {
-  const int partials = D > kAppendThreads ? D : kAppendThreads;
-  return ((size_t)G * D + D + G + partials) * sizeof(float);
+inline size_t flush_smem_bytes(int G, int D, int esize) {
+  const size_t partials = (size_t)kAppendThreads * (16 / esize) > (size_t)D ? (size_t)kAppendThreads * (16 / esize)
+                                                                            : (size_t)D;
+  return (size_t)G * D * esize + ((size_t)D + G + partials + G) * sizeof(float);
 }
 
 struct AppendParams {
