@@ -269,7 +269,7 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* new_k, const void* new_
  * cudaMalloc, cudaFree or allocating library call.
  *  - The array holds 2^21 floats (8 MiB); every GPU that loads the library
  *    holds it until the process exits.  A cache whose batch * n_kv_heads *
- *    (n_q_heads / n_kv_heads) * (head_dim + 2) floats times 2 split columns
+ *    (n_q_heads / n_kv_heads) * (head_dim + 4) floats times 2 split columns
  *    (1 without any flushed group) exceed it is rejected with KVQ_ECAPACITY
  *    before any launch; otherwise the split count is lowered to fit.
  *  - The first call on each device looks up the array's device address

@@ -35,52 +35,105 @@ cudaError_t launch_bits(const DecodeParams& p, cudaStream_t s) {
   return launch_pdl(decode_simt_kernel<T, BITS, 8>, grid, block, 0, s, p);
 }
 
-constexpr int kCombineThreads = 128;
+constexpr int kCombineWarps = 4;
+constexpr int kCombineChunk = 8;  // slots whose loads are in flight together
 
 // Merge of the split partials (o[D], m, l) of one (sequence, query head):
 // M = max m_s, L = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M) / L
-// ("KV Cache 与自回归视频生成" section 05, FlashDecoding).  One CTA per
-// (sequence, query head), one thread per channel; the slot loops are unrolled
-// so their loads overlap.  A sequence without tokens gets zeros.
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const CombineParams p) {
+// ("KV Cache 与自回归视频生成" section 05, FlashDecoding).  One warp per
+// (sequence, query head).  The slots are taken eight at a time: lane s reads
+// slot s's (m, l) while every lane reads its 16-byte pieces of the eight o
+// rows, so one round trip serves the whole chunk; the chunk is then folded
+// into the running (M, L, o) with the usual rescale.  VPL = 16-byte pieces of
+// o per lane (1 for head_dim <= 128, 2 up to 256).  A sequence without tokens
+// gets zeros.
+template <int VPL>
+__global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
   pdl_wait();
   pdl_release();
-  const int i = blockIdx.x / p.Hq;
-  const int hq = blockIdx.x - i * p.Hq;
+  const int lane = threadIdx.x & 31;
+  const int item = blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+  if (item >= p.n_seqs * p.Hq) return;
+  const int i = item / p.Hq;
+  const int hq = item - i * p.Hq;
   const int b = p.seq_begin + i;
   const int h = hq / p.g, j = hq - h * p.g;
   const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
   const int nsplit = p.dense_chunk > 0 ? (T0 + p.dense_chunk - 1) / p.dense_chunk
                                       : (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
   const int nslots = nsplit + (p.dense_chunk == 0 && T0 > Q0 ? 1 : 0);
-  const int D = p.D;
+  const int D = p.D, nvec = D >> 2;
   const int64_t unit = (int64_t)b * p.Hkv + h;
-  const float* base = p.partials + unit * p.max_splits * (int64_t)p.g * (D + 2) + (int64_t)j * (D + 2);
-  const int64_t stride = (int64_t)p.g * (D + 2);
+  const int64_t stride = (int64_t)p.g * part_row(D);
+  const float* base = p.partials + unit * p.max_splits * stride + (int64_t)j * part_row(D);
+  // slot k < nsplit is split column k; the window's partial sits in the last column
   auto row = [&](int k) { return base + (k < nsplit ? k : p.max_splits - 1) * stride; };
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int k = 0; k < nslots; ++k) M = fmaxf(M, row(k)[D]);
-  const float Ms = M == -INFINITY ? 0.f : M;
-  float L = 0.f;
-  float o[2] = {0.f, 0.f};
-#pragma unroll 4
-  for (int k = 0; k < nslots; ++k) {
-    const float* r = row(k);
-    const float f = exp2f(r[D] - Ms);
-    L = fmaf(r[D + 1], f, L);
+
+  float M = -INFINITY, L = 0.f;
+  float4 o[VPL];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int c = threadIdx.x + e * kCombineThreads;
-      if (c < D) o[e] = fmaf(r[c], f, o[e]);
+  for (int e = 0; e < VPL; ++e) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nslots; k0 += kCombineChunk) {
+    const int n = min(kCombineChunk, nslots - k0);
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < n) ml = __ldg(reinterpret_cast<const float2*>(row(k0 + lane) + D));
+    float4 v[kCombineChunk][VPL];
+#pragma unroll
+    for (int s = 0; s < kCombineChunk; ++s)
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) {
+        const int c4 = lane + 32 * e;
+        v[s][e] = (s < n && c4 < nvec) ? __ldg(reinterpret_cast<const float4*>(row(k0 + s)) + c4)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    float cm = ml.x;
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    cm = __shfl_sync(0xffffffffu, cm, 0);
+    const float Mn = fmaxf(M, cm);
+    const float Ms = Mn == -INFINITY ? 0.f : Mn;
+    const float corr = exp2f(M - Ms);
+    const float f = exp2f(ml.x - Ms);  // lanes >= n: 0
+    float ls = ml.y * f;
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    L = fmaf(L, corr, __shfl_sync(0xffffffffu, ls, 0));
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) {
+      o[e].x *= corr;
+      o[e].y *= corr;
+      o[e].z *= corr;
+      o[e].w *= corr;
     }
+#pragma unroll
+    for (int s = 0; s < kCombineChunk; ++s) {
+      const float fs = __shfl_sync(0xffffffffu, f, s);
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) {
+        o[e].x = fmaf(v[s][e].x, fs, o[e].x);
+        o[e].y = fmaf(v[s][e].y, fs, o[e].y);
+        o[e].z = fmaf(v[s][e].z, fs, o[e].z);
+        o[e].w = fmaf(v[s][e].w, fs, o[e].w);
+      }
+    }
+    M = Mn;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
   float* out = p.out + ((int64_t)b * p.Hq + hq) * D;
+  const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;  // caller's buffer
 #pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int c = threadIdx.x + e * kCombineThreads;
-    if (c < D) out[c] = o[e] * inv;
+  for (int e = 0; e < VPL; ++e) {
+    const int c4 = lane + 32 * e;
+    if (c4 >= nvec) continue;
+    const float4 r = make_float4(o[e].x * inv, o[e].y * inv, o[e].z * inv, o[e].w * inv);
+    if (vec) {
+      reinterpret_cast<float4*>(out)[c4] = r;
+    } else {
+      out[4 * c4] = r.x;
+      out[4 * c4 + 1] = r.y;
+      out[4 * c4 + 2] = r.z;
+      out[4 * c4 + 3] = r.w;
+    }
   }
 }
 
@@ -96,7 +149,9 @@ cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s)
 }
 
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s) {
-  return launch_pdl(combine_kernel, dim3(p.n_seqs * p.Hq), dim3(kCombineThreads), 0, s, p);
+  const dim3 grid((p.n_seqs * p.Hq + kCombineWarps - 1) / kCombineWarps);
+  return p.D <= 128 ? launch_pdl(combine_kernel<1>, grid, dim3(kCombineWarps * 32), 0, s, p)
+                    : launch_pdl(combine_kernel<2>, grid, dim3(kCombineWarps * 32), 0, s, p);
 }
 
 }  // namespace kvq

@@ -163,7 +163,7 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int
   a->ring_v = o;
   o = align_up(o + ring, kAlign);
   a->partials = o;
-  o = align_up(o + units * a->max_splits * g * (c->head_dim + 2) * sizeof(float), kAlign);
+  o = align_up(o + units * a->max_splits * g * kvq::part_row(c->head_dim) * sizeof(float), kAlign);
   a->total = o;
   return KVQ_OK;
 }
@@ -211,7 +211,7 @@ kvq_status plan_arena_seg(const kvq_config* c, const int64_t* cap, SegPlan* a) {
   a->ring_v = o;
   o = align_up(o + ring, kAlign);
   a->partials = o;
-  o = align_up(o + units * a->max_splits * g * (D + 2) * sizeof(float), kAlign);
+  o = align_up(o + units * a->max_splits * g * kvq::part_row((int)D) * sizeof(float), kAlign);
   a->total = o;
   return KVQ_OK;
 }
@@ -817,7 +817,7 @@ kvq_status kvq_decode_attention_noalloc(kvq_cache* c, const void* q, float* out,
   // one split plan for every sequence, then as many split slots as the array holds
   int64_t pmax = 0;
   for (int b = 0; b < B; ++b) pmax = std::max<int64_t>(pmax, c->quantized[b] / c->cfg.group);
-  const size_t per_slot = (size_t)B * H * c->g * (D + 2);  // floats of one split column
+  const size_t per_slot = (size_t)B * H * c->g * kvq::part_row(D);  // floats of one split column
   const size_t min_slots = pmax > 0 ? 2 : 1;              // one quantized split plus the window
   if (per_slot * min_slots > kNoAllocScratchFloats)
     return fail(KVQ_ECAPACITY,

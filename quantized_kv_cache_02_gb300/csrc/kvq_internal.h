@@ -15,6 +15,10 @@ constexpr int kMaxGqa = 8;
 // the parameter block).
 constexpr int kMaxNewBlocks = 4096;
 
+// Floats of one split partial row (o[D], m, l): padded to a multiple of 16
+// bytes so that the combine reads it with 16-byte loads.
+__host__ __device__ constexpr int part_row(int D) { return D + 4; }
+
 // Device status word codes (kvq_device_status).
 constexpr int32_t kStatusWaitTimeout = 0x101;  // a bounded mbarrier wait gave up
 
@@ -148,7 +152,7 @@ struct DecodeParams {
   const void* ring_k;
   const void* ring_v;
   const void* q;               // [batch][Hq][D]
-  float* partials;             // [batch*Hkv][max_splits][g][D + 2]
+  float* partials;             // [batch*Hkv][max_splits][g][part_row(D)]
   int32_t max_splits;          // slots per unit; the window uses slot max_splits - 1
   int32_t chunk_pages;         // pages per quantized split
   int32_t grid_splits;         // quantized split columns in this launch (window column after)

@@ -198,7 +198,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
 #pragma unroll
     for (int k = 0; k < CPL; ++k) wo[warp][j][lane + 32 * k] = s.o[j][k];
   __syncthreads();
-  float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * (D + 2);
+  float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * part_row(D);
   for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
     const int j = idx / D, c = idx - j * D;
     float M = -INFINITY;
@@ -212,10 +212,10 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
         O = fmaf(wo[w][j][c], f, O);
       }
     }
-    part[(int64_t)j * (D + 2) + c] = O;
+    part[(int64_t)j * part_row(D) + c] = O;
     if (c == 0) {
-      part[(int64_t)j * (D + 2) + D] = M;
-      part[(int64_t)j * (D + 2) + D + 1] = L;
+      part[(int64_t)j * part_row(D) + D] = M;
+      part[(int64_t)j * part_row(D) + D + 1] = L;
     }
   }
 }
