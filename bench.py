@@ -35,6 +35,9 @@ WORKLOAD = dict(name="llama3_8b_decode_b32_ctx8192_4bit", layers=32, batch=32, n
                 head_dim=128, context=8192, residual_len=128, group=32, qmax=7, seed=2)
 SPLIT_KERNEL_SOURCE = os.path.join(ROOT, "quantized_kv_cache_02_gb300", "csrc", "kvq_decode_mma.cuh")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
+SPLIT_KERNEL_NAMES = {0: "decode_mma_kernel<128,4> (split, one layer per launch)",
+                      2: "decode_mma_kernel<128,4> (split, one layer per launch)",
+                      3: "decode_tc_kernel<4> (tcgen05 split, one layer per launch)"}
 
 
 # ---------------------------------------------------------------------------
@@ -196,9 +199,11 @@ def kernel_source_hash():
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def load_traffic():
+def load_traffic(kernel=0):
     """ncu DRAM bytes per split launch, if the capture matches the current
-    kernel source (else None)."""
+    kernel source (else None).  The capture is of the mma.sync split kernel."""
+    if kernel == 3:
+        return None
     try:
         with open(TRAFFIC_FILE) as f:
             t = json.load(f)
@@ -458,10 +463,11 @@ def run_ours(args):
             # one from starting while the previous drains, so the other layers run
             # without them
             if timed_index is None or l != timed_index % L:
-                caches[l].decode_attention(qs[l][s], out=outs[l])
+                caches[l].decode_attention(qs[l][s], out=outs[l], kernel=args.kernel)
             else:
                 e0, e1 = ev_pool[timed_index]
-                caches[l].decode_attention(qs[l][s], out=outs[l], split_start=e0.cuda_event, split_stop=e1.cuda_event)
+                caches[l].decode_attention(qs[l][s], out=outs[l], kernel=args.kernel, split_start=e0.cuda_event,
+                                           split_stop=e1.cuda_event)
 
     for s in range(W):
         one_step(s)
@@ -569,7 +575,7 @@ def run_ours(args):
         for l in range(L):
             k_l, v_l, q_l = views[cur][l]
             caches[l].append(k_l, v_l, 0)
-            caches[l].decode_attention(q_l, out=dev_out[cur][l])
+            caches[l].decode_attention(q_l, out=dev_out[cur][l], kernel=args.kernel)
         ev_done[cur].record(stream)
         down.wait_event(ev_done[cur])
         with torch.cuda.stream(down):
@@ -635,8 +641,8 @@ def run_ours(args):
                    "parallelism": f"dp{world} (global batch sharded by sequence, no collective on the data path)",
                    "l2": "working set per step ~10 GB >> 129 MB L2 (no flush needed)"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": load_traffic(),
-                     "kernel": "decode_mma_kernel<128,4> (split, one layer per launch)",
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": load_traffic(args.kernel),
+                     "kernel": SPLIT_KERNEL_NAMES[args.kernel],
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": round(sum(split_b) / len(split_b)),
                      "avg_launch_ms": round(split_avg_ms, 5),
@@ -693,6 +699,8 @@ def main():
     ap.add_argument("--no-foil", action="store_true", help="skip the dequantize-to-HBM foil measurement")
     ap.add_argument("--no-variants", action="store_true", help="skip the 2-bit and paged one-layer measurements")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; 0 = all 32)")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 2, 3],
+                    help="split kernel: 0 = automatic (mma.sync at this shape), 2 = mma.sync, 3 = tcgen05")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")

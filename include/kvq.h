@@ -119,8 +119,11 @@ typedef struct kvq_unit_view {
 /* Options of kvq_decode_attention_ex (zero-initialise for defaults). */
 typedef struct kvq_decode_opts {
   int32_t kernel;      /* 0 = automatic; 1 = CUDA-core kernel (any supported
-                          shape); 2 = tensor-core kernel (bf16, head_dim 64/128,
-                          G a multiple of 32); KVQ_EUNSUPPORTED if not applicable */
+                          shape); 2 = tensor-core kernel on mma.sync (bf16,
+                          head_dim 64/128, G a multiple of 32); 3 = tcgen05
+                          tensor-core kernel (bf16, head_dim 128, 4-bit codes,
+                          G a multiple of 32); KVQ_EUNSUPPORTED if not
+                          applicable */
   int32_t chunk_pages; /* 0 = automatic; else quantized groups per split item */
   void* split_start;   /* optional cudaEvent_t recorded just before the split kernel */
   void* split_stop;    /* optional cudaEvent_t recorded just after it */

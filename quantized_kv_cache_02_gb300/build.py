@@ -23,7 +23,8 @@ CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-
 LDFLAGS = ARCH + ["-shared", "-cudart", "shared", f"-Xlinker=-rpath={CUDA_HOME}/lib64"]
 
 SOURCES = ["kvq_host.cu", "kvq_append.cu", "kvq_decode_simt.cu", "kvq_decode_mma.cu", "kvq_decode_mma_b2.cu",
-           "kvq_decode_mma_b4.cu", "kvq_decode_mma_b8.cu", "kvq_restore.cu", "kvq_segment.cu"]
+           "kvq_decode_mma_b4.cu", "kvq_decode_mma_b8.cu", "kvq_decode_tc.cu", "kvq_restore.cu",
+           "kvq_segment.cu"]
 
 
 def _run(cmd):

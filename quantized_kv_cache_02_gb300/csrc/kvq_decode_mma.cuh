@@ -737,7 +737,7 @@ __device__ __forceinline__ void write_partial(const DecodeParams& p, int64_t uni
   float* mrg = reinterpret_cast<float*>(buf);  // [kMmaWarps][kMaxGqa][D + 2]
   const int hd0 = 2 * tig, hd1 = 2 * tig + 1;  // heads of the stream-0 columns
   float* mw = mrg + (size_t)warp * kMaxGqa * (D + 2);
-  const bool stream0 = 2 * tig < GP;
+  const bool stream0 = 2 * tig < GP && warp < kMmaWarps;  // a fifth (control) warp holds no rows
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     const int c_lo = 16 * mt + gid;
@@ -794,6 +794,37 @@ constexpr int kRowsBuf = NBUF * 32 * D * 2;
 // G = 32, and any larger G (either map) staged in 32-token units.
 constexpr int kFlat32 = 0, kPaged32 = 1, kStaged = 2;
 
+// The residual-window item of unit (sequence i of the launch, KV head h): its
+// ring rows on the tensor cores (plus, for kvq_decode_step, this step's token,
+// which it also stores into its ring row).  ``buf`` holds kRowsBuf<D, 1> bytes
+// per warp.
+template <int D, int GP>
+__device__ __forceinline__ void window_rows(const DecodeParams& p, int i, int h, int lane, int warp, int gid, int tig,
+                                            uint8_t* buf, WarpState<D>& st) {
+  const int b = p.seq_begin + i;
+  const int64_t unit = (int64_t)b * p.Hkv + h;
+  const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+  __nv_bfloat16* rk = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.ring_k)) + unit * p.Rcap * D;
+  __nv_bfloat16* rv = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.ring_v)) + unit * p.Rcap * D;
+  const __nv_bfloat16* lk = nullptr;
+  const __nv_bfloat16* lv = nullptr;
+  if (p.step_k) {
+    // this step's token: attended from the input and stored in its ring row
+    // (row (T0 - 1) mod Rcap holds no other token of the window, so no copy
+    // of this launch reads it)
+    lk = reinterpret_cast<const __nv_bfloat16*>(p.step_k) + ((int64_t)i * p.Hkv + h) * D;
+    lv = reinterpret_cast<const __nv_bfloat16*>(p.step_v) + ((int64_t)i * p.Hkv + h) * D;
+    const int64_t row = ((T0 - 1) % p.Rcap) * D;
+    for (int c = threadIdx.x; c < D / 8; c += blockDim.x) {
+      reinterpret_cast<uint4*>(rk + row)[c] = reinterpret_cast<const uint4*>(lk)[c];
+      reinterpret_cast<uint4*>(rv + row)[c] = reinterpret_cast<const uint4*>(lv)[c];
+    }
+  }
+  rows_mma<D, GP, 1, true>(p, rk, rv, Q0, p.Rcap, (int)(T0 - Q0),
+                           reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * p.g) * D, lane,
+                           warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st, lk, lv);
+}
+
 template <int D, int BITS, int GP, int MODE>
 __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const DecodeParams p, int slots) {
   using S = Shape<D, BITS, GP>;
@@ -840,27 +871,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   bool ok = true;
 
   if (win) {
-    const int64_t unit = (int64_t)b * p.Hkv + h;
-    const int64_t T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-    __nv_bfloat16* rk = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.ring_k)) + unit * p.Rcap * D;
-    __nv_bfloat16* rv = reinterpret_cast<__nv_bfloat16*>(const_cast<void*>(p.ring_v)) + unit * p.Rcap * D;
-    const __nv_bfloat16* lk = nullptr;
-    const __nv_bfloat16* lv = nullptr;
-    if (p.step_k) {
-      // this step's token: attended from the input and stored in its ring row
-      // (row (T0 - 1) mod Rcap holds no other token of the window, so no copy
-      // of this launch reads it)
-      lk = reinterpret_cast<const __nv_bfloat16*>(p.step_k) + ((int64_t)i * p.Hkv + h) * D;
-      lv = reinterpret_cast<const __nv_bfloat16*>(p.step_v) + ((int64_t)i * p.Hkv + h) * D;
-      const int64_t row = ((T0 - 1) % p.Rcap) * D;
-      for (int c = threadIdx.x; c < D / 8; c += blockDim.x) {
-        reinterpret_cast<uint4*>(rk + row)[c] = reinterpret_cast<const uint4*>(lk)[c];
-        reinterpret_cast<uint4*>(rv + row)[c] = reinterpret_cast<const uint4*>(lv)[c];
-      }
-    }
-    rows_mma<D, GP, 1, true>(p, rk, rv, Q0, p.Rcap, (int)(T0 - Q0),
-                             reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * g) * D, lane,
-                             warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st, lk, lv);
+    window_rows<D, GP>(p, i, h, lane, warp, gid, tig, buf, st);
   } else {
   // queries of the GP column heads (head n % g for the padding columns, so every
   // value stays finite), pre-scaled, in shared memory: channel c of head n goes

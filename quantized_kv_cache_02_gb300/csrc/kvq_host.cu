@@ -659,12 +659,17 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
   const int kernel = opts ? opts->kernel : 0;
-  if (kernel < 0 || kernel > 2) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
+  if (kernel < 0 || kernel > 3) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
   const bool mma_ok = c->cfg.dtype == KVQ_BF16 && (c->cfg.head_dim == 64 || c->cfg.head_dim == 128) &&
                       c->cfg.group % 32 == 0 && c->g >= 2;
   if (kernel == 2 && !mma_ok)
     return fail(KVQ_EUNSUPPORTED,
                 "tensor-core kernel needs bf16, head_dim 64/128, group %% 32 == 0 and >= 2 query heads per KV head");
+  const bool tc_ok = mma_ok && c->cfg.head_dim == 128 && c->bits == 4 && !c->segmented;
+  if (kernel == 3 && !tc_ok)
+    return fail(KVQ_EUNSUPPORTED,
+                "tcgen05 kernel needs bf16, head_dim 128, 4-bit codes, group %% 32 == 0 and >= 2 query heads per KV head");
+  const bool use_tc = kernel == 3;
   const bool use_mma = kernel == 2 || (kernel == 0 && mma_ok);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (opts && opts->split_start) {
@@ -695,7 +700,10 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     fill_counters(c, bt.s0, bt.n, p.ctr);
     cudaError_t e = cudaSuccess;
     int supported = 0;
-    if (use_mma) {
+    if (use_tc) {
+      e = kvq::launch_decode_tc(p, s, &supported);
+      if (e == cudaSuccess && !supported) return fail(KVQ_EUNSUPPORTED, "tcgen05 kernel does not fit this configuration");
+    } else if (use_mma) {
       e = kvq::launch_decode_mma(p, s, &supported);
       if (e == cudaSuccess && !supported && kernel == 2)
         return fail(KVQ_EUNSUPPORTED, "tensor-core kernel does not fit this configuration (shared memory)");

@@ -248,6 +248,9 @@ cudaError_t launch_mma_bits4(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_mma_bits8(const DecodeParams& p, cudaStream_t s);
 size_t decode_mma_smem_bytes(const DecodeParams& p);
 bool decode_mma_supported(const DecodeParams& p);
+// the fifth-generation tensor-core split kernel (head_dim 128, 4-bit codes)
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s, int* supported);
+bool decode_tc_supported(const DecodeParams& p);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t s);
 cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supported);
 cudaError_t launch_restore(const RestoreParams& p, cudaStream_t s);
