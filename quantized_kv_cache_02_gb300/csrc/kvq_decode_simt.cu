@@ -119,21 +119,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     M = Mn;
   }
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  float* out = p.out + ((int64_t)b * p.Hq + hq) * D;
-  const bool vec = (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;  // caller's buffer
+  // the entry points accept only 16-byte aligned outputs
+  float4* out = reinterpret_cast<float4*>(p.out + ((int64_t)b * p.Hq + hq) * D);
 #pragma unroll
   for (int e = 0; e < VPL; ++e) {
     const int c4 = lane + 32 * e;
-    if (c4 >= nvec) continue;
-    const float4 r = make_float4(o[e].x * inv, o[e].y * inv, o[e].z * inv, o[e].w * inv);
-    if (vec) {
-      reinterpret_cast<float4*>(out)[c4] = r;
-    } else {
-      out[4 * c4] = r.x;
-      out[4 * c4 + 1] = r.y;
-      out[4 * c4 + 2] = r.z;
-      out[4 * c4 + 3] = r.w;
-    }
+    if (c4 < nvec) out[c4] = make_float4(o[e].x * inv, o[e].y * inv, o[e].z * inv, o[e].w * inv);
   }
 }
 
