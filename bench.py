@@ -267,7 +267,8 @@ def segmented_layer(torch, kvq, w, dev, peak, batch=8, steps=10):
     """The segmented cache (the page's flush rule: each append's overflow is
     one segment) at the benchmark's head shape, 8 sequences of 8192 tokens:
     one prefill segment, then one-token segments.  Its decode runs on the
-    CUDA-core kernel; each token also carries its segment's Key scale row."""
+    CUDA-core kernel; a segment's Key scale row is stored once and each token
+    records the first token of its segment."""
     H, Hq, D, R = w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["residual_len"]
     T0 = w["context"]
     cache = kvq.KVQCache(batch, H, Hq, D, R, w["group"], w["qmax"], T0 + 3 + steps + 8, segmented=True)
@@ -292,9 +293,11 @@ def segmented_layer(torch, kvq, w, dev, peak, batch=8, steps=10):
     st = [cache.seq_state(b) for b in range(batch)]
     Q = sum(x["quantized"] for x in st)
     W = sum(x["window"] for x in st)
+    S = sum(x["n_groups"] for x in st)
     g = Hq // H
-    # codes (K and V), the per-token Key scale row and Value scale, window, q
-    nbytes = H * (Q * (D + 4 * D + 4) + W * 2 * D * 2 + batch * g * D * 2)
+    # per unit: codes (K and V), Value scale and segment index per token, one
+    # Key scale row per segment, window rows, q
+    nbytes = H * (Q * (D + 4 + 4) + S * 4 * D + W * 2 * D * 2 + batch * g * D * 2)
     gbs = nbytes / (ms / 1e3) / 1e9
     return {"workload": f"segmented cache, {batch} x 8192 tokens, Llama head shape, 4-bit",
             "split_ms": round(ms, 5), "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),

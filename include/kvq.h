@@ -210,8 +210,9 @@ kvq_status kvq_create_paged(const kvq_config* cfg, const int64_t* capacity_per_s
  * with one scale per token; the newest min(L + n, R) tokens stay at input
  * precision.  cfg->group is not used (any valid value).  Storage: per unit,
  * token-major code rows (each row packed like a group page's Key row, for
- * Keys and Values alike), each token's copy of its segment's Key scales
- * (head_dim fp32), its Value scale, and a window ring of R rows.  Decode
+ * Keys and Values alike), each segment's Key scales (head_dim fp32) in the
+ * row of its first token, each token's Value scale, per sequence the first
+ * token of each token's segment (int32), and a window ring of R rows.  Decode
  * attention runs on the CUDA-core kernel; kvq_export_unit returns one Key
  * scale row per segment; kvq_export_pages returns KVQ_EUNSUPPORTED; the other
  * calls work as on a grouped cache.  Arguments as kvq_required_bytes /

@@ -11,7 +11,7 @@
 namespace kvq {
 namespace {
 
-template <typename T, int BITS, int CPL>
+template <typename T, int BITS, int CPL, bool SEG>
 __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const DecodeParams p) {
   pdl_wait();
   pdl_release();
@@ -21,18 +21,23 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(const DecodeP
   int pg0, pg1, slot;
   __shared__ float scratch[simt_scratch_floats<CPL>()];
   if (!split_item(p, blockIdx.x, i, &win, &pg0, &pg1, &slot)) return;
-  simt_item<T, BITS, CPL>(p, i, h, win, pg0, pg1, slot, scratch);
+  simt_item<T, BITS, CPL, SEG>(p, i, h, win, pg0, pg1, slot, scratch);
+}
+
+template <typename T, int BITS, bool SEG>
+cudaError_t launch_seg(const DecodeParams& p, cudaStream_t s) {
+  const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
+  const int cpl = (p.D + 31) / 32;
+  const dim3 block(kSimtThreads);
+  if (cpl <= 1) return launch_pdl(decode_simt_kernel<T, BITS, 1, SEG>, grid, block, 0, s, p);
+  if (cpl <= 2) return launch_pdl(decode_simt_kernel<T, BITS, 2, SEG>, grid, block, 0, s, p);
+  if (cpl <= 4) return launch_pdl(decode_simt_kernel<T, BITS, 4, SEG>, grid, block, 0, s, p);
+  return launch_pdl(decode_simt_kernel<T, BITS, 8, SEG>, grid, block, 0, s, p);
 }
 
 template <typename T, int BITS>
 cudaError_t launch_bits(const DecodeParams& p, cudaStream_t s) {
-  const dim3 grid(p.grid_splits + 1, p.n_seqs * p.Hkv);
-  const int cpl = (p.D + 31) / 32;
-  const dim3 block(kSimtThreads);
-  if (cpl <= 1) return launch_pdl(decode_simt_kernel<T, BITS, 1>, grid, block, 0, s, p);
-  if (cpl <= 2) return launch_pdl(decode_simt_kernel<T, BITS, 2>, grid, block, 0, s, p);
-  if (cpl <= 4) return launch_pdl(decode_simt_kernel<T, BITS, 4>, grid, block, 0, s, p);
-  return launch_pdl(decode_simt_kernel<T, BITS, 8>, grid, block, 0, s, p);
+  return p.seg.kcodes ? launch_seg<T, BITS, true>(p, s) : launch_seg<T, BITS, false>(p, s);
 }
 
 constexpr int kCombineWarps = 4;

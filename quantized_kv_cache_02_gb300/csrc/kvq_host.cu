@@ -172,7 +172,7 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int
 // for capacity_max tokens per unit, the segment maxima, rings of R rows and
 // the split partials.
 struct SegPlan {
-  size_t status, layout, kcodes, vcodes, kscales, vscales, kmax, ring_k, ring_v, partials, total;
+  size_t status, layout, kcodes, vcodes, kscales, vscales, first, kmax, ring_k, ring_v, partials, total;
   int64_t cap;
   int max_splits;
 };
@@ -203,6 +203,8 @@ kvq_status plan_arena_seg(const kvq_config* c, const int64_t* cap, SegPlan* a) {
   o = align_up(o + rows * D * sizeof(float), kAlign);
   a->vscales = o;
   o = align_up(o + rows * sizeof(float), kAlign);
+  a->first = o;
+  o = align_up(o + (size_t)c->batch * (size_t)cmax * sizeof(int32_t), kAlign);
   a->kmax = o;
   o = align_up(o + units * D * sizeof(uint32_t), kAlign);
   const size_t ring = units * (size_t)c->residual_len * D * esize_of(c);
@@ -381,6 +383,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
     c->seg.vcodes = c->base + sp.vcodes;
     c->seg.kscales = reinterpret_cast<float*>(c->base + sp.kscales);
     c->seg.vscales = reinterpret_cast<float*>(c->base + sp.vscales);
+    c->seg.first = reinterpret_cast<int32_t*>(c->base + sp.first);
     c->seg.cap = sp.cap;
     c->seg.row_bytes = cfg->head_dim * c->bits / 8;
     c->kmax = reinterpret_cast<uint32_t*>(c->base + sp.kmax);
@@ -1008,7 +1011,8 @@ kvq_status kvq_export_unit(const kvq_cache* c, int32_t seq, int32_t kv_head, con
   kvq_status st = c->segmented ? KVQ_OK : kvq_export_pages(c, seq, kv_head, pages.data(), pages.size(), stream);
   if (st != KVQ_OK) return st;
   if (c->segmented && Q > 0) {
-    // token-major rows: codes, the segment's Key scale row per token, Value scales
+    // token-major rows: codes, Value scales, and each segment's Key scale row in
+    // the row of its first token
     const int64_t row0 = ((int64_t)seq * c->cfg.n_kv_heads + kv_head) * c->seg.cap;
     const int rb = c->seg.row_bytes;
     std::vector<uint8_t> kc((size_t)Q * rb), vc((size_t)Q * rb);

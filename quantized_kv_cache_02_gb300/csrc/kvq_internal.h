@@ -88,8 +88,9 @@ __host__ __device__ inline int64_t flush_groups(int64_t w, int64_t n, int64_t R,
 struct SegArrays {
   uint8_t* kcodes;             // [batch][Hkv][cap][row_bytes]; null: not segmented
   uint8_t* vcodes;
-  float* kscales;              // [batch][Hkv][cap][D]
+  float* kscales;              // [batch][Hkv][cap][D]; a segment's row at its first token
   float* vscales;              // [batch][Hkv][cap]
+  int32_t* first;              // [batch][cap]: first token of each token's segment
   int64_t cap;                 // token rows per unit
   int32_t row_bytes;           // D * bits / 8
 };

@@ -11,7 +11,8 @@
 // >= 0 order like unsigned integers) and, since Value scales are per token,
 // writes the Value codes and scales at once; pass 2 quantizes the Keys with
 // the final scales.  Codes are token-major rows packed like a group page's Key
-// rows; every token keeps its segment's Key scale row.
+// rows; a segment's Key scale row is stored once, in the row of its first
+// token, and every token records that first token.
 
 #include <cuda_bf16.h>
 
@@ -155,8 +156,14 @@ __global__ void __launch_bounds__(kSegThreads) seg_pass2_kernel(const SegFlushPa
   __syncthreads();
   pack_rows<BITS>(p.seg.kcodes + (unit * p.seg.cap + t_begin) * p.seg.row_bytes, p.seg.row_bytes, tile, cnt, D,
                   sK, false, qmax);
-  float* ks = p.seg.kscales + (unit * p.seg.cap + t_begin) * D;
-  for (int idx = threadIdx.x; idx < cnt * D; idx += blockDim.x) ks[idx] = sK[idx % D];
+  if (off == 0) {
+    float* ks = p.seg.kscales + (unit * p.seg.cap + Q0) * D;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) ks[c] = sK[c];
+  }
+  if (h == 0) {
+    int32_t* first = p.seg.first + (int64_t)(p.seq_begin + i) * p.seg.cap + t_begin;
+    for (int r = threadIdx.x; r < cnt; r += blockDim.x) first[r] = Q0;
+  }
 }
 
 // The new tokens that stay in the window, into their ring rows (t mod R).
@@ -204,8 +211,9 @@ __global__ void __launch_bounds__(kSegThreads) seg_restore_kernel(const RestoreP
     float kx, vx;
     if (t < Q0) {
       const int64_t row = unit * p.seg.cap + t;
+      const int64_t srow = unit * p.seg.cap + p.seg.first[(int64_t)(p.seq_begin + i) * p.seg.cap + t];
       kx = __fdiv_rn((float)row_code<BITS>(p.seg.kcodes + row * p.seg.row_bytes, c),
-                     fmaxf(p.seg.kscales[row * D + c], p.eps));
+                     fmaxf(p.seg.kscales[srow * D + c], p.eps));
       vx = __fdiv_rn((float)row_code<BITS>(p.seg.vcodes + row * p.seg.row_bytes, c), fmaxf(p.seg.vscales[row], p.eps));
     } else {
       const int64_t src = (unit * p.Rcap + t % p.Rcap) * D + c;

@@ -93,7 +93,8 @@ __host__ __device__ constexpr int simt_scratch_floats() {
 // ``win`` selects the residual window (tokens [Q, T) from the ring) instead of
 // pages [pg0, pg1) of the quantized prefix.
 
-template <typename T, int BITS, int CPL>
+// SEG: a segmented cache (token-major rows, a Key scale row per segment).
+template <typename T, int BITS, int CPL, bool SEG>
 __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, int pg0, int pg1, int slot,
                           float* scratch) {
   float (*qs)[CPL * 32] = reinterpret_cast<float (*)[CPL * 32]>(scratch);
@@ -141,25 +142,35 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
       }
       simt_token<CPL>(s, qv, kv, vv, g);
     }
-  } else if (p.seg.kcodes) {
-    // segmented cache: a "page" is one token of the token-major code rows,
-    // with its segment's Key scale row and its own Value scale
+  } else if constexpr (SEG) {
+    // segmented cache: a "page" is one token of the token-major code rows.
+    // q.k = sum_c q_c code_c / sK_c: the 1/sK of the token's segment is folded
+    // into q whenever the segment changes (a prefill segment spans thousands
+    // of tokens); the Value scale 1/sV goes onto the token's codes.
+    const int32_t* first = p.seg.first + (int64_t)b * p.seg.cap;
+    int cur = -1;
     for (int64_t t = pg0 + warp; t < pg1; t += kSimtWarps) {
+      const int f = first[t];  // the same for every lane of the warp
+      if (f != cur) {
+        const float* ks = p.seg.kscales + (unit * p.seg.cap + f) * D;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+          const int c = lane + 32 * k;
+          const float r = c < D ? __frcp_rn(fmaxf(ks[c], p.eps)) : 0.f;
+#pragma unroll
+          for (int j = 0; j < kMaxGqa; ++j) qv[j][k] = qs[j][c] * r;  // q / sK from here on
+        }
+        cur = f;
+      }
       const int64_t row = unit * p.seg.cap + t;
       const uint8_t* kr = p.seg.kcodes + row * p.seg.row_bytes;
       const uint8_t* vr = p.seg.vcodes + row * p.seg.row_bytes;
-      const float* ks = p.seg.kscales + row * D;
-      const float vs = p.seg.vscales[row];
+      const float iv = __frcp_rn(fmaxf(p.seg.vscales[row], p.eps));
 #pragma unroll
       for (int k = 0; k < CPL; ++k) {
         const int c = lane + 32 * k;
-        if (c < D) {
-          kv[k] = __fdiv_rn((float)key_code<BITS>(kr, 0, c, D), fmaxf(ks[c], p.eps));
-          vv[k] = __fdiv_rn((float)key_code<BITS>(vr, 0, c, D), fmaxf(vs, p.eps));
-        } else {
-          kv[k] = 0.f;
-          vv[k] = 0.f;
-        }
+        kv[k] = c < D ? (float)key_code<BITS>(kr, 0, c, D) : 0.f;
+        vv[k] = c < D ? (float)key_code<BITS>(vr, 0, c, D) * iv : 0.f;
       }
       simt_token<CPL>(s, qv, kv, vv, g);
     }
