@@ -128,8 +128,9 @@ __host__ __device__ constexpr uint32_t tc_idesc(int M, int N) {
 
 // ---- layout ---------------------------------------------------------------
 constexpr int kTcD = 128;
-constexpr int kTcWorkers = 128;                  // warps 0-3: one TMEM lane quarter each
-constexpr int kTcThreads = kTcWorkers + 64;      // warp 4: MMAs and TMEM; warp 5: copies
+constexpr int kTcGroup = 128;                        // threads of one worker group (4 warps)
+constexpr int kTcThreads = 2 * kTcGroup + 64;        // Key warps 0-3, Value warps 4-7, MMA warp 8, copy warp 9
+constexpr int kTcMmaWarp = 8, kTcCopyWarp = 9;
 constexpr int kTcUnit = 32 * kTcD / 2 * 2 + 4 * kTcD + 4 * 32;  // a G = 32 page: 4736 bytes
 constexpr int kTcUnitStride = kTcUnit + 16;  // units staggered by 16 bytes across the banks
 constexpr int kTcKsc = 2 * 32 * kTcD / 2;    // Key scales within a unit
@@ -139,18 +140,29 @@ constexpr int kTcSlots = 4;                  // blocks of 4 units in flight
 constexpr int kTcBlock = 4 * kTcUnitStride;
 constexpr int kTcBRow = 2 * kTcD;            // bytes of one B row (K = 128 f16)
 constexpr uint32_t kTcSbo = 16 * 128;        // next 8-row group: 16 core matrices along K
-// tensor-memory columns
-constexpr uint32_t kColAK = 0, kColAV = 64, kColS = 128, kColO = 192;
 
 template <int GP>
 struct TcShape {
   static constexpr int NS = 8 * GP;   // score columns: 4 units x (hi, lo) x GP heads
   static constexpr int CPG = GP / 2;  // heads of one unit per B_Q-building thread
+  // tensor memory: A_K, A_V, scores (two buffers), output accumulator
+  static constexpr uint32_t kColAK = 0, kColAV = 64, kColS0 = 128, kColS1 = kColS0 + NS, kColO = kColS1 + NS;
+  static constexpr uint32_t kCols = kColO + 16 <= 256 ? 256 : 512;
   static constexpr size_t kBOff = ((size_t)kTcSlots * kTcBlock + 1023) / 1024 * 1024;  // B operands
   static constexpr size_t kBq = (size_t)NS * kTcBRow;                                  // one B_Q buffer
   static constexpr size_t smem =
-      kBOff + 2 * kBq + 16 * kTcBRow + GP * kTcD * 4 + (64 + 2 * 4 * 8) * 4 + (2 * kTcSlots + 4) * 8 + 32;
+      kBOff + 2 * kBq + 16 * kTcBRow + GP * kTcD * 4 + (96 + 3 * 4 * 8) * 4 + (2 * kTcSlots + 5) * 8 + 32;
 };
+
+template <uint32_t N>
+__device__ __forceinline__ void tc_alloc_n(uint32_t dst_smem) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "n"(N) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+template <uint32_t N>
+__device__ __forceinline__ void tc_dealloc_n(uint32_t taddr) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(N) : "memory");
+}
 
 // Byte offset of element (n, k) of a K-major B matrix with K = 128.
 __device__ __forceinline__ int b_off(int n, int k) {
@@ -160,21 +172,22 @@ __device__ __forceinline__ int b_off(int n, int k) {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// barrier 1 over the four worker warps, with an OR of ``pred``
-__device__ __forceinline__ bool workers_or(bool pred) {
+// barrier 1 over the four Key warps, with an OR of ``pred``
+__device__ __forceinline__ bool kgroup_or(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)pred), "n"(kTcWorkers)
+      : "r"((uint32_t)pred), "n"(kTcGroup)
       : "memory");
   return r != 0;
 }
-// Bounded wait that also gives up as soon as ``*abort`` is set (another part
-// of the CTA stopped and will not complete the phase).
+__device__ __forceinline__ void kgroup_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTcGroup) : "memory"); }
+
 // Bounded wait; a warp that only issues copies or MMAs backs off with
-// __nanosleep between tries (``sleep_ns``) so that it does not take issue
-// slots from the workers.  About a second in all.
+// __nanosleep between tries (``sleep_ns``).  It also gives up as soon as
+// ``*abort`` is set (another part of the CTA stopped and will not complete
+// the phase).  About a second in all.
 constexpr uint32_t kTcWaitTries = 1u << 22;
 template <int sleep_ns = 0>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort) {
@@ -192,8 +205,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
   return false;
 }
 __device__ const int kNoAbort = 0;  // for waits that must not be cut short
-__device__ __forceinline__ void workers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTcWorkers) : "memory"); }
 
+// Every mbarrier of the CTA completes once per block.  A thread arrives on a
+// barrier for block b + 1 only after it has seen block b's phase complete, and
+// it waits on a phase only while no later phase can complete without its own
+// later arrival, so no phase is ever miscounted or mistaken for another.
 template <int GP, int MODE>
 __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodeParams p) {
   constexpr int D = kTcD;
@@ -214,7 +230,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   const int64_t unit = (int64_t)b * p.Hkv + h;
 
   if (win) {
-    // the window runs on the four worker warps; the other warps only join the merge
+    // the window runs on the four Key warps; the other warps only join the merge
     WarpState<D> st;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) st.O[mt][0] = st.O[mt][1] = st.O[mt][2] = st.O[mt][3] = 0.f;
@@ -232,39 +248,43 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   uint8_t* bq = smem + TS::kBOff;          // B_Q, two buffers of NS rows
   uint8_t* bpm = bq + 2 * TS::kBq;         // B_P: 16 rows
   float* qs = reinterpret_cast<float*>(bpm + 16 * kTcBRow);
-  float* red = qs + GP * D;                // [0, 32): maxima; [32, 64): l and bias sums
-  float* beta = red + 64;                  // [2][4 units][8 heads] Key bias sums
-  uint64_t* bars = reinterpret_cast<uint64_t*>(beta + 2 * 4 * 8);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kTcSlots + 4);
+  float* red = qs + GP * D;                // [0, 32): maxima; [32, 64): l; [64, 96): Value bias sums
+  float* beta = red + 96;                  // [3][4 units][8 heads] Key bias sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(beta + 3 * 4 * 8);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kTcSlots + 5);
   volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);  // set by whichever part stops
   // ring slots: ``full`` (copies landed) and ``empty`` (every worker is done with it)
   const uint32_t bar_ring = smem_addr(bars), bar_empty = bar_ring + 8 * kTcSlots;
-  const uint32_t bar_a = bar_empty + 8 * kTcSlots, bar_p = bar_a + 8, bar_s = bar_p + 8, bar_o = bar_s + 8;
+  // A: A_K and B_Q of a block ready (both groups); P: A_V and B_P ready (both
+  // groups); S[2]: the score MMAs of even / odd blocks done; O: the block's
+  // output MMAs done
+  const uint32_t bar_a = bar_empty + 8 * kTcSlots, bar_p = bar_a + 8, bar_s = bar_p + 8, bar_o = bar_s + 16;
 
   // ---- set-up -------------------------------------------------------------------
-  if (warp == 4) tc_alloc(smem_addr(tslot));
+  if (warp == kTcMmaWarp) tc_alloc_n<TS::kCols>(smem_addr(tslot));
   if (t == 0) {
     *abort = 0;
     for (int s = 0; s < kTcSlots; ++s) {
       mbar_init(bar_ring + 8 * s, 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
-    mbar_init(bar_a, kTcWorkers);
-    mbar_init(bar_p, kTcWorkers);
+    mbar_init(bar_a, 2 * kTcGroup);
+    mbar_init(bar_p, 2 * kTcGroup);
     mbar_init(bar_s, 1);
+    mbar_init(bar_s + 8, 1);
     mbar_init(bar_o, 1);
     fence_mbar_init();
   }
-  if (t < kTcWorkers) {
+  if (t < 2 * kTcGroup) {
     // queries (head n % g for the padding heads), pre-scaled
-    for (int idx = t; idx < GP * D; idx += kTcWorkers) {
+    for (int idx = t; idx < GP * D; idx += 2 * kTcGroup) {
       const int n = idx / D, c = idx - n * D;
       qs[idx] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(
                     p.q)[((int64_t)b * p.Hq + (int64_t)h * p.g + n % p.g) * D + c]) *
                 p.qk_scale;
     }
     // B operands start at zero (B_P rows GP..15 stay zero)
-    for (int idx = t; idx < (int)((2 * TS::kBq + 16 * kTcBRow) / 16); idx += kTcWorkers)
+    for (int idx = t; idx < (int)((2 * TS::kBq + 16 * kTcBRow) / 16); idx += 2 * kTcGroup)
       reinterpret_cast<uint4*>(bq)[idx] = make_uint4(0u, 0u, 0u, 0u);
     fence_proxy_async();
   }
@@ -279,8 +299,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   const int nunits = (pg1 - pg0) * upp;
   const int nblk = (nunits + 3) / 4;
   constexpr float kTwo24 = 16777216.f, kSlack = 8.f;
+  // TMEM lanes of this warp's quarter
+  const uint32_t lane_base = tm + ((uint32_t)(32 * (warp & 3)) << 16);
 
-  if (warp == 5) {
+  if (warp == kTcCopyWarp) {
     // ================= copy warp (lane 0): blocks of four units into the ring =======
     if (lane == 0) {
       const uint8_t* flat_base = MODE == kFlat32 ? p.pages + page_offset(p.map, stored, b, h, 0) : nullptr;
@@ -325,7 +347,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       for (int k = max(0, issued - kTcSlots); k < issued; ++k)
         wait_or_abort<256>(bar_ring + 8 * (k % kTcSlots), (uint32_t)(k / kTcSlots) & 1u, &kNoAbort);
     }
-  } else if (warp == 4) {
+  } else if (warp == kTcMmaWarp) {
     // ================= MMA warp (lane 0) =====================================
     if (lane == 0) {
       const uint32_t idesc_s = tc_idesc(128, NS), idesc_o = tc_idesc(128, 16);
@@ -333,18 +355,26 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       const uint64_t dq1 = tc_desc(smem_addr(bq + TS::kBq), 128, kTcSbo);
       const uint64_t dp = tc_desc(smem_addr(bpm), 128, kTcSbo);
       int n_s = 0, n_o = 0;
-      for (int blk = 0; blk < nblk; ++blk) {
-        if (!wait_or_abort<32>(bar_a, (uint32_t)blk & 1u, abort)) {
-          *abort = 1;
-          break;
-        }
+      // the score MMAs of block k, into score buffer k & 1
+      auto scores = [&](int k) -> bool {
+        if (!wait_or_abort<32>(bar_a, (uint32_t)k & 1u, abort)) return false;
         tc_fence_after();
-        const uint64_t dq = (blk & 1) ? dq1 : dq0;
+        const uint64_t dq = (k & 1) ? dq1 : dq0;
+        const uint32_t d = tm + ((k & 1) ? TS::kColS1 : TS::kColS0);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // the B start advances by 256 bytes (two core matrices) per k-step
-          tc_mma(tm + kColS, tm + kColAK + 8 * ks, dq + 16 * ks, idesc_s, ks > 0 ? 1u : 0u);
-        tc_commit(bar_s);
+          tc_mma(d, tm + TS::kColAK + 8 * ks, dq + 16 * ks, idesc_s, ks > 0 ? 1u : 0u);
+        tc_commit(bar_s + 8 * (k & 1));
         ++n_s;
+        return true;
+      };
+      bool go = scores(0);
+      for (int blk = 0; blk < nblk && go; ++blk) {
+        // the next block's scores run while the workers finish this block's softmax
+        if (blk + 1 < nblk && !scores(blk + 1)) {
+          go = false;
+          break;
+        }
         if (!wait_or_abort<32>(bar_p, (uint32_t)blk & 1u, abort)) {
           *abort = 1;
           break;
@@ -353,19 +383,21 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          tc_mma(tm + kColO, tm + kColAV + 8 * ks, dp + 16 * ks, idesc_o, (blk > 0 || ks > 0) ? 1u : 0u);
+          tc_mma(tm + TS::kColO, tm + TS::kColAV + 8 * ks, dp + 16 * ks, idesc_o, (blk > 0 || ks > 0) ? 1u : 0u);
         tc_commit(bar_o);
         ++n_o;
       }
-      // nothing in flight when the CTA ends
-      if (n_s > 0) wait_or_abort<32>(bar_s, (uint32_t)(n_s - 1) & 1u, &kNoAbort);
+      if (!go) *abort = 1;
+      // nothing in flight when the CTA ends (the last score commit's completion
+      // implies every earlier MMA's)
+      if (n_s > 0)
+        wait_or_abort<32>(bar_s + 8 * ((n_s - 1) & 1), (uint32_t)((n_s - 1) >> 1) & 1u, &kNoAbort);
       if (n_o > 0) wait_or_abort<32>(bar_o, (uint32_t)(n_o - 1) & 1u, &kNoAbort);
     }
-  } else {
-    // ================= workers: one token per thread (scores), one channel (output) ===
-    const uint32_t lane_base = tm + ((uint32_t)(32 * warp) << 16);
-    // B_Q share: unit ``warp``, K octet ``oct`` (channels 8 oct .. 8 oct + 7),
-    // heads e0 .. e0 + CPG - 1
+  } else if (warp >= 4) {
+    // ================= Value warps: A_V (one channel per thread), B_Q and the
+    // Key bias sums of unit ``vw`` ============================================
+    const int vw = warp - 4, c = t - kTcGroup;
     const int oct = lane >> 1, e0 = (lane & 1) * CPG;
     float qreg[CPG][8];
 #pragma unroll
@@ -374,21 +406,20 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       for (int kk = 0; kk < 8; ++kk) {
         // k-slot kk of the octet holds channel 8 oct + kk/2 + 4 (kk % 2); the
         // slots whose codes carry x16 get 1/16 here
-        const int c = 8 * oct + (kk >> 1) + 4 * (kk & 1);
-        qreg[e][kk] = qs[(e0 + e) * D + c] * (((kk >> 1) & 1) ? 0.0625f : 1.f);
+        const int ch = 8 * oct + (kk >> 1) + 4 * (kk & 1);
+        qreg[e][kk] = qs[(e0 + e) * D + ch] * (((kk >> 1) & 1) ? 0.0625f : 1.f);
       }
     bool fail = false;
-    // Score inputs of block blk: B_Q rows of unit ``warp`` into buffer blk & 1, the
-    // Key bias sums, and this thread's Key codes into ``ak``.
-    uint32_t ak[64];
-    auto score_inputs = [&](int blk) {
+    // B_Q rows of unit vw for block blk (hi: vw * 2GP + e; lo: + GP) and the
+    // unit's Key bias sums, then the arrival on A
+    auto b_build = [&](int blk) {
       const int s = blk % kTcSlots;
       const int nu = min(4, nunits - 4 * blk);
       const uint8_t* sb = ring + s * kTcBlock;
       fail |= !wait_or_abort(bar_ring + 8 * s, (uint32_t)(blk / kTcSlots) & 1u, abort);
       uint8_t* bqb = bq + (blk & 1) * TS::kBq;
-      if (warp < nu) {
-        const float4* ks4 = reinterpret_cast<const float4*>(sb + warp * kTcUnitStride + kTcKsc) + 2 * oct;
+      if (vw < nu) {
+        const float4* ks4 = reinterpret_cast<const float4*>(sb + vw * kTcUnitStride + kTcKsc) + 2 * oct;
         const float4 s0 = ks4[0], s1 = ks4[1];
         const float r[8] = {fast_rcp(s0.x), fast_rcp(s0.y), fast_rcp(s0.z), fast_rcp(s0.w),
                             fast_rcp(s1.x), fast_rcp(s1.y), fast_rcp(s1.z), fast_rcp(s1.w)};
@@ -408,35 +439,70 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
             hw[pr] = *reinterpret_cast<const uint32_t*>(&hi);
             lw[pr] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          const int nh = warp * 2 * GP + e0 + e;
+          const int nh = vw * 2 * GP + e0 + e;
           *reinterpret_cast<uint4*>(bqb + b_off(nh, 8 * oct)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
           *reinterpret_cast<uint4*>(bqb + b_off(nh + GP, 8 * oct)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           // sum over the 16 octets (lanes of the same parity)
 #pragma unroll
           for (int off = 2; off < 32; off <<= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, off);
-          if (oct == 0) beta[((blk & 1) * 4 + warp) * 8 + e0 + e] = bsum;
+          if (oct == 0) beta[((blk % 3) * 4 + vw) * 8 + e0 + e] = bsum;
         }
       }
-      __syncwarp();  // the bias sums are read by the other lanes of this warp
-      const uint4* kr = reinterpret_cast<const uint4*>(sb + warp * kTcUnitStride + lane * (D / 2));
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) {
-        const uint4 w = kr[qq];
-        nibble_regs(w.x, *reinterpret_cast<uint32_t(*)[4]>(ak + 16 * qq + 0));
-        nibble_regs(w.y, *reinterpret_cast<uint32_t(*)[4]>(ak + 16 * qq + 4));
-        nibble_regs(w.z, *reinterpret_cast<uint32_t(*)[4]>(ak + 16 * qq + 8));
-        nibble_regs(w.w, *reinterpret_cast<uint32_t(*)[4]>(ak + 16 * qq + 12));
-      }
-    };
-    auto store_ak = [&]() {
-#pragma unroll
-      for (int qq = 0; qq < 4; ++qq) tc_st16(lane_base + kColAK + 16 * qq, *reinterpret_cast<uint32_t(*)[16]>(ak + 16 * qq));
-      tc_wait_st();
-      tc_fence_before();
       fence_proxy_async();
       mbar_arrive(bar_a);
     };
-
+    b_build(0);
+    for (int blk = 0; blk < nblk && !fail; ++blk) {
+      if (blk + 1 < nblk) {
+        // B_Q buffer (blk + 1) & 1 was last read by the score MMAs of block blk - 1
+        if (blk > 0) fail |= !wait_or_abort(bar_s + 8 * ((blk - 1) & 1), (uint32_t)((blk - 1) >> 1) & 1u, abort);
+        fail |= !wait_or_abort(bar_a, (uint32_t)blk & 1u, abort);  // block blk's A phase is complete
+        b_build(blk + 1);
+      }
+      const uint8_t* sb = ring + (blk % kTcSlots) * kTcBlock;  // landed: b_build(blk) waited for it
+      uint32_t vr[4][16];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4*>(sb + j * kTcUnitStride + kTcVcode + c * 16);
+        nibble_regs(w.x, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][0]));
+        nibble_regs(w.y, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][4]));
+        nibble_regs(w.z, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][8]));
+        nibble_regs(w.w, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][12]));
+      }
+      // the previous block's O MMAs have read A_V
+      if (blk > 0) fail |= !wait_or_abort(bar_o, (uint32_t)(blk - 1) & 1u, abort);
+      tc_fence_after();
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tc_st16(lane_base + TS::kColAV + 16 * j, vr[j]);
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    if (fail) *abort = 1;
+  } else {
+    // ================= Key warps: A_K (one token per thread), scores, softmax,
+    // B_P, and the unit's partial =============================================
+    bool fail = false;
+    auto k_codes = [&](int blk) {
+      const int s = blk % kTcSlots;
+      const uint8_t* sb = ring + s * kTcBlock;
+      fail |= !wait_or_abort(bar_ring + 8 * s, (uint32_t)(blk / kTcSlots) & 1u, abort);
+      const uint4* kr = reinterpret_cast<const uint4*>(sb + warp * kTcUnitStride + lane * (D / 2));
+      const uint32_t colk = TS::kColAK;
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const uint4 w = kr[qq];
+        uint32_t r[16];
+        nibble_regs(w.x, *reinterpret_cast<uint32_t(*)[4]>(r + 0));
+        nibble_regs(w.y, *reinterpret_cast<uint32_t(*)[4]>(r + 4));
+        nibble_regs(w.z, *reinterpret_cast<uint32_t(*)[4]>(r + 8));
+        nibble_regs(w.w, *reinterpret_cast<uint32_t(*)[4]>(r + 12));
+        tc_st16(lane_base + colk + 16 * qq, r);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_a);
+    };
     float m_run[GP], l_part[GP], c_part[GP];
 #pragma unroll
     for (int e = 0; e < GP; ++e) {
@@ -444,60 +510,45 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       l_part[e] = 0.f;
       c_part[e] = 0.f;
     }
-    score_inputs(0);
-    store_ak();
+    k_codes(0);
     int n_o = 0;
     for (int blk = 0; blk < nblk; ++blk) {
-      const int s = blk % kTcSlots;
       const int nu = min(4, nunits - 4 * blk);
-      const uint8_t* sb = ring + s * kTcBlock;
-      // -- the next block's score inputs first: the previous block's O MMAs and
-      // this block's score MMAs run meanwhile
-      const bool more = blk + 1 < nblk;
-      if (more) score_inputs(blk + 1);
-      // -- A_V: channel t of the four units (tokens in order, 8 per word)
-      {
-        uint32_t vr[4][16];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint4 w = *reinterpret_cast<const uint4*>(sb + j * kTcUnitStride + kTcVcode + t * 16);
-          nibble_regs(w.x, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][0]));
-          nibble_regs(w.y, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][4]));
-          nibble_regs(w.z, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][8]));
-          nibble_regs(w.w, *reinterpret_cast<uint32_t(*)[4]>(&vr[j][12]));
-        }
-        if (n_o > 0) fail |= !wait_or_abort(bar_o, (uint32_t)(n_o - 1) & 1u, abort);  // previous O MMAs
-        tc_fence_after();
-#pragma unroll
-        for (int j = 0; j < 4; ++j) tc_st16(lane_base + kColAV + 16 * j, vr[j]);
-      }
-      // -- scores of this thread's token: hi and lo columns of its unit, minus the bias
-      fail |= !wait_or_abort(bar_s, (uint32_t)blk & 1u, abort);
+      const uint8_t* sb = ring + (blk % kTcSlots) * kTcBlock;
+      // block blk's A phase is complete (also: the Value warps' bias sums are
+      // visible) and its score MMAs are done with A_K: the next block's Key
+      // codes go in at once, so that its score MMAs overlap this softmax
+      fail |= !wait_or_abort(bar_a, (uint32_t)blk & 1u, abort);
+      fail |= !wait_or_abort(bar_s + 8 * (blk & 1), (uint32_t)(blk >> 1) & 1u, abort);
       tc_fence_after();
+      if (blk + 1 < nblk) k_codes(blk + 1);
+      // -- scores of this thread's token: hi and lo columns of its unit, minus the bias
+      const uint32_t cols = (blk & 1) ? TS::kColS1 : TS::kColS0;
       const bool valid = warp < nu;
       float sc2[2 * GP];
       if constexpr (GP == 2) {
-        tc_ld<4>(lane_base + kColS + warp * 2 * GP, sc2);
+        tc_ld<4>(lane_base + cols + warp * 2 * GP, sc2);
       } else if constexpr (GP == 4) {
-        tc_ld<8>(lane_base + kColS + warp * 2 * GP, sc2);
+        tc_ld<8>(lane_base + cols + warp * 2 * GP, sc2);
       } else {
-        tc_ld<8>(lane_base + kColS + warp * 2 * GP, *reinterpret_cast<float(*)[8]>(sc2));
-        tc_ld<8>(lane_base + kColS + warp * 2 * GP + 8, *reinterpret_cast<float(*)[8]>(sc2 + 8));
+        tc_ld<8>(lane_base + cols + warp * 2 * GP, *reinterpret_cast<float(*)[8]>(sc2));
+        tc_ld<8>(lane_base + cols + warp * 2 * GP + 8, *reinterpret_cast<float(*)[8]>(sc2 + 8));
       }
       tc_wait_ld();
-      // A_K is free again: the next block's Key codes go in now
-      if (more) store_ak();
       float sc[GP];
       bool up = fail;
 #pragma unroll
       for (int e = 0; e < GP; ++e) {
-        const float bias = 8.f * beta[((blk & 1) * 4 + warp) * 8 + e];
+        const float bias = 8.f * beta[((blk % 3) * 4 + warp) * 8 + e];
         sc[e] = valid ? fmaf(sc2[e] + sc2[GP + e], kTwo24, -bias) : -INFINITY;
         up |= sc[e] > m_run[e] + kSlack;
       }
-      if (workers_or(up)) {
-        // move the running max (CTA-wide maxima; rescale l, the Value bias sum
-        // and the O accumulator), or stop everything after a failed wait
+      // the previous block's O MMAs are done: B_P and the O accumulator are free
+      if (n_o > 0) fail |= !wait_or_abort(bar_o, (uint32_t)(n_o - 1) & 1u, abort);
+      tc_fence_after();
+      if (kgroup_or(up || fail)) {
+        // move the running max (maxima over the four Key warps; rescale l, the
+        // Value bias sum and the O accumulator), or stop after a failed wait
         float a[GP];
 #pragma unroll
         for (int e = 0; e < GP; ++e) {
@@ -506,7 +557,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
           for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
           if (lane == 0) red[warp * 8 + e] = mx;
         }
-        const bool stop = workers_or(fail);  // also publishes the maxima (a barrier)
+        const bool stop = kgroup_or(fail);  // also publishes the maxima (a barrier)
         if (stop) {
           fail = true;
           *abort = 1;
@@ -522,13 +573,14 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
         }
         if (n_o > 0) {
           float o[GP];
-          tc_ld<GP>(lane_base + kColO, o);
+          tc_ld<GP>(lane_base + TS::kColO, o);
           tc_wait_ld();
 #pragma unroll
           for (int e = 0; e < GP; ++e) o[e] *= a[e];
-          tc_st_f<GP>(lane_base + kColO, o);
+          tc_st_f<GP>(lane_base + TS::kColO, o);
+          tc_wait_st();
         }
-        workers_sync();  // every warp has read the maxima before they are written again
+        kgroup_sync();  // every warp has read the maxima before they are written again
       }
       // -- P / sV into B_P (row e, k-slot = block token), x1/16 on the x16 slots;
       // the Value bias is 8 times the sum of exactly these f16 values
@@ -546,7 +598,6 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
           *reinterpret_cast<__half*>(bpm + b_off(e, k)) = hv;
         }
       }
-      tc_wait_st();
       tc_fence_before();
       fence_proxy_async();
       mbar_arrive(bar_p);
@@ -557,9 +608,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
     tc_fence_after();
     float o[GP];
     if (!fail) {
-      tc_ld<GP>(lane_base + kColO, o);
+      tc_ld<GP>(lane_base + TS::kColO, o);
       tc_wait_ld();
     }
+    float* csum = red + 64;
 #pragma unroll
     for (int e = 0; e < GP; ++e) {
       float ls = l_part[e], cs = c_part[e];
@@ -570,16 +622,17 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       }
       if (lane == 0) {
         red[32 + warp * 8 + e] = ls;
-        beta[warp * 8 + e] = cs;  // the Key bias sums are no longer needed
+        csum[warp * 8 + e] = cs;
       }
     }
-    const bool bad = workers_or(fail);
+    const bool bad = kgroup_or(fail);
+    if (bad) *abort = 1;
     if (bad && t == 0) atomicOr(p.status, kStatusWaitTimeout);
     float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)p.g * part_row(D);
 #pragma unroll
     for (int e = 0; e < GP; ++e) {
       if (e < p.g) {
-        const float C = (beta[e] + beta[8 + e]) + (beta[16 + e] + beta[24 + e]);
+        const float C = (csum[e] + csum[8 + e]) + (csum[16 + e] + csum[24 + e]);
         part[(int64_t)e * part_row(D) + t] = bad ? 0.f : fmaf(o[e], kTwo24, -8.f * C);
         if (t == 0) {
           part[(int64_t)e * part_row(D) + D] = bad ? -INFINITY : m_run[e];
@@ -591,9 +644,9 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) {
+  if (warp == kTcMmaWarp) {
     __syncwarp();
-    tc_dealloc(tm);
+    tc_dealloc_n<TS::kCols>(tm);
   }
 }
 
