@@ -131,8 +131,11 @@ __device__ void load_group(float* tile, const T* ring, const T* input, int t_fir
 }
 
 // DC: head_dim as a compile-time constant (64, 128), or 0 for any other.
-template <typename T, int BITS, int DC>
-__global__ void __launch_bounds__(kAppendThreads, 3) append_kernel(const AppendParams p) {
+// KB: rows a flush thread loads per batch (2 when the group is only a pass or
+// two of rows deep, 4 for deeper groups), so that short groups do not issue
+// predicated-off loads; four CTAs fit per SM.
+template <typename T, int BITS, int DC, int KB>
+__global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendParams p) {
   extern __shared__ float smem[];
   pdl_wait();
   pdl_release();
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(kAppendThreads, 3) append_kernel(const AppendP
   // four loads in flight, and keeps the column's Key absmax in registers; the
   // Value absmax of a row is reduced over the threads of the row with shuffles.
   constexpr int kVec = 16 / sizeof(T);
-  constexpr int kBatch = 8;
+  constexpr int kBatch = KB;
   T* tileT = reinterpret_cast<T*>(smem);                         // [G][D]
   float* sK = reinterpret_cast<float*>(tileT + (size_t)G * D);   // [D] Key scales
   float* sV = sK + D;                                            // [G] Value scales
@@ -313,16 +316,16 @@ __global__ void __launch_bounds__(kAppendThreads, 3) append_kernel(const AppendP
       for (int e = 0; e < kVec; ++e) a = fmaxf(a, fabsf(x[e]));
       if (shuffle_rows) {
         for (int o = 1; o < per_row; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-        if (act && r < G && col == 0) sV[r] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+        if (act && r < G && col == 0) sV[r] = a;  // the row's absmax; its scale below
       } else if (act && r < G) {
         atomicMax(rmax + r, __float_as_uint(a));
       }
     });
     __syncthreads();
-    if (!shuffle_rows) {
-      for (int t = threadIdx.x; t < G; t += blockDim.x) sV[t] = __fdiv_rn(qmax, fmaxf(__uint_as_float(rmax[t]), p.eps));
-      __syncthreads();
-    }
+    // one division per token, spread over the CTA (not inside the row loop)
+    for (int t = threadIdx.x; t < G; t += blockDim.x)
+      sV[t] = __fdiv_rn(qmax, fmaxf(shuffle_rows ? sV[t] : __uint_as_float(rmax[t]), p.eps));
+    __syncthreads();
   }
   {
     // channel fastest across threads (each token row is read at consecutive
@@ -455,24 +458,34 @@ __global__ void __launch_bounds__(kCompareThreads) compare_kernel(const CompareP
   }
 }
 
+template <typename T, int BITS, int KB>
+cudaError_t launch_kb(const AppendParams& p, const dim3& grid, size_t smem, cudaStream_t s) {
+  if (p.D == 128) return launch_pdl(append_kernel<T, BITS, 128, KB>, grid, dim3(kAppendThreads), smem, s, p);
+  if (p.D == 64) return launch_pdl(append_kernel<T, BITS, 64, KB>, grid, dim3(kAppendThreads), smem, s, p);
+  return launch_pdl(append_kernel<T, BITS, 0, KB>, grid, dim3(kAppendThreads), smem, s, p);
+}
+
 template <typename T, int BITS>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
   const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
   const size_t smem = p.flush_blocks ? flush_smem_bytes(p.G, p.D, (int)sizeof(T)) : 0;
-  if (p.D == 128) return launch_pdl(append_kernel<T, BITS, 128>, grid, dim3(kAppendThreads), smem, s, p);
-  if (p.D == 64) return launch_pdl(append_kernel<T, BITS, 64>, grid, dim3(kAppendThreads), smem, s, p);
-  return launch_pdl(append_kernel<T, BITS, 0>, grid, dim3(kAppendThreads), smem, s, p);
+  const int rows_per_pass = kAppendThreads / (p.D / (16 / (int)sizeof(T)));
+  return p.G <= 2 * rows_per_pass ? launch_kb<T, BITS, 2>(p, grid, smem, s) : launch_kb<T, BITS, 4>(p, grid, smem, s);
 }
-
-template <typename T, int BITS>
-cudaError_t configure_t(size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(append_kernel<T, BITS, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+template <typename T, int BITS, int KB>
+cudaError_t configure_kb(size_t smem) {
+  cudaError_t e = cudaFuncSetAttribute(append_kernel<T, BITS, 0, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(append_kernel<T, BITS, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(append_kernel<T, BITS, 64, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(append_kernel<T, BITS, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(append_kernel<T, BITS, 128, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return e;
+}
+template <typename T, int BITS>
+cudaError_t configure_t(size_t smem) {
+  const cudaError_t e = configure_kb<T, BITS, 2>(smem);
+  return e == cudaSuccess ? configure_kb<T, BITS, 4>(smem) : e;
 }
 
 }  // namespace
