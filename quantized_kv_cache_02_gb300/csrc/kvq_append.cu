@@ -29,12 +29,23 @@ __device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
   return (int)r;
 }
 
-// code = clamp(rint(x * scale), -qmax, qmax) with one rounding conversion:
-// |x| <= absmax makes |x * scale| <= qmax, so the conversion cannot overflow,
-// and round-to-nearest-even conversion is rint.
-__device__ __forceinline__ int quantize_int(float x, float scale, int qmax) {
-  const int r = __float2int_rn(__fmul_rn(x, scale));
-  return min(max(r, -qmax), qmax);
+// code = clamp(rint(x * scale), -qmax, qmax) as one rounding conversion.  The
+// clamp never acts here: |x| <= absmax and scale = qmax / max(absmax, eps)
+// (each rounded once) make |x * scale| <= qmax (1 + 2^-23) < qmax + 1/2, so
+// rint already lies in [-qmax, qmax]; round-to-nearest-even conversion is rint.
+__device__ __forceinline__ int quantize_int(float x, float scale) { return __float2int_rn(__fmul_rn(x, scale)); }
+
+// The low BITS bits of a code's two's complement, at field k of a word.  The
+// stored offset binary code + 2^(BITS-1) is those bits with the top one
+// flipped (for every code the width holds), which bias_word does for a whole
+// word at once.
+template <int BITS>
+__device__ __forceinline__ uint32_t code_field(int code, int k) {
+  return ((uint32_t)code & ((1u << BITS) - 1u)) << (BITS * k);
+}
+template <int BITS>
+__device__ __forceinline__ constexpr uint32_t bias_word() {
+  return BITS == 2 ? 0xAAAAAAAAu : BITS == 4 ? 0x88888888u : 0x80808080u;
 }
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
@@ -219,9 +230,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
   float* sK = reinterpret_cast<float*>(tileT + (size_t)G * D);   // [D] Key scales
   float* sV = sK + D;                                            // [G] Value scales
   float* part = sV + G;                                          // [rows_per_pass][D] partial Key maxima
-  const int qmax_i = p.qmax;
   const float qmax = (float)p.qmax;
-  constexpr int kBias = BITS == 2 ? 2 : BITS == 4 ? 8 : 128;  // stored offset binary: code + bias
   const int per_row = D / kVec;
   const int rows_per_pass = blockDim.x / per_row;
   const bool act = (int)threadIdx.x < rows_per_pass * per_row;
@@ -293,8 +302,8 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
         uint32_t word = 0;
 #pragma unroll
         for (int k = 0; k < kPerWord; ++k)
-          word |= (uint32_t)(quantize_int(x[k], sc[k], qmax_i) + kBias) << (BITS * k);
-        kc[t * words_per_row + w] = word;
+          word |= code_field<BITS>(quantize_int(x[k], sc[k]), k);
+        kc[t * words_per_row + w] = word ^ bias_word<BITS>();
       }
     }
     float* ks = reinterpret_cast<float*>(page + geom.kscale_off);
@@ -351,10 +360,10 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
 #pragma unroll
             for (int f = 0; f < 4; ++f) {
               const int te = 32 * st + 8 * w + 2 * f;
-              piece |= (uint32_t)(quantize_int(x_at(te, c), sV[te], qmax_i) + kBias) << (2 * f);
-              piece |= (uint32_t)(quantize_int(x_at(te + 1, c), sV[te + 1], qmax_i) + kBias) << (8 + 2 * f);
+              piece |= code_field<2>(quantize_int(x_at(te, c), sV[te]), f);
+              piece |= code_field<2>(quantize_int(x_at(te + 1, c), sV[te + 1]), 4 + f);
             }
-            vp[c * np + w] = (uint16_t)piece;
+            vp[c * np + w] = (uint16_t)(piece ^ bias_word<2>());
           }
         } else if (BITS == 4) {
           const int nw = n_st / 8;  // words per channel row
@@ -363,9 +372,9 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
 #pragma unroll
             for (int jn = 0; jn < 8; ++jn) {
               const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
-              word |= (uint32_t)(quantize_int(x_at(tok, c), sV[tok], qmax_i) + kBias) << (4 * jn);
+              word |= code_field<4>(quantize_int(x_at(tok, c), sV[tok]), jn);
             }
-            vc[c * nw + w] = word;
+            vc[c * nw + w] = word ^ bias_word<4>();
           }
         } else {
           const int nw = n_st / 4;
@@ -374,9 +383,9 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int tok = 32 * st + 4 * w + k;
-              word |= (uint32_t)(quantize_int(x_at(tok, c), sV[tok], qmax_i) + kBias) << (8 * k);
+              word |= code_field<8>(quantize_int(x_at(tok, c), sV[tok]), k);
             }
-            vc[c * nw + w] = word;
+            vc[c * nw + w] = word ^ bias_word<8>();
           }
         }
       }
