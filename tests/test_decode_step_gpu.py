@@ -31,6 +31,8 @@ def kvq(torch):
     (128, 32, 7, "bf16", 400, 0),   # fused, paged
     (64, 64, 1, "bf16", 0, 0),      # fused, staged large group, 2-bit
     (128, 32, 127, "bf16", 0, 2),   # fused, 8-bit, kernel forced
+    (128, 32, 7, "bf16", 0, 3),     # fused, the tcgen05 kernel's window items
+    (128, 64, 7, "bf16", 300, 3),   # fused, tcgen05 kernel, paged, staged units
     (64, 32, 7, "fp32", 0, 0),      # falls back (fp32 runs the CUDA-core kernel)
     (128, 32, 7, "bf16", 0, 1),     # falls back (CUDA-core kernel asked for)
 ])
