@@ -51,6 +51,11 @@ __device__ __forceinline__ constexpr uint32_t bias_word() {
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+
 // 16 bytes of elements -> fp32 values
 __device__ __forceinline__ void unpack16(const uint4& raw, float (&x)[4]) {
   const float* f = reinterpret_cast<const float*>(&raw);
@@ -263,6 +268,21 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     }
   };
 
+  // With room for a second tile the Values are copied into it now (cp.async),
+  // so that their latency passes while the Keys are reduced and packed.
+  T* tileV = p.v_prefetch ? reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(smem) + flush_smem_bytes(G, D, sizeof(T)))
+                          : tileT;
+  if (p.v_prefetch) {
+    if (act) {
+      for (int r = r0; r < G; r += rows_per_pass) {
+        const int t = t_first + r;
+        cp_async16(tileV + (size_t)r * D + col,
+                   t < T0 ? ring_v + (size_t)(ring_row0 + r) * D + col : in_v + (size_t)(t - T0) * D + col);
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  }
+
   // ---- Key: per-channel absmax over the group's tokens --------------------
   {
     float amax[kVec];
@@ -319,7 +339,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       for (int t = threadIdx.x; t < G; t += blockDim.x) rmax[t] = 0u;
       __syncthreads();
     }
-    load_rows(ring_v, in_v, [&](int r, const float (&x)[kVec]) {
+    auto row_max = [&](int r, const float (&x)[kVec]) {
       float a = 0.f;
 #pragma unroll
       for (int e = 0; e < kVec; ++e) a = fmaxf(a, fabsf(x[e]));
@@ -329,7 +349,25 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       } else if (act && r < G) {
         atomicMax(rmax + r, __float_as_uint(a));
       }
-    });
+    };
+    if (p.v_prefetch) {
+      asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+      __syncthreads();
+      // the same rows per thread as the copies, read back from the tile
+      for (int base = 0; base < G; base += kBatch * rows_per_pass) {
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+          const int r = base + r0 + k * rows_per_pass;
+          const uint4 v = act && r < G ? *reinterpret_cast<const uint4*>(tileV + (size_t)r * D + col)
+                                       : make_uint4(0u, 0u, 0u, 0u);
+          float x[kVec];
+          unpack16(v, x);
+          row_max(r, x);
+        }
+      }
+    } else {
+      load_rows(ring_v, in_v, row_max);
+    }
     __syncthreads();
     // one division per token, spread over the CTA (not inside the row loop)
     for (int t = threadIdx.x; t < G; t += blockDim.x)
@@ -344,7 +382,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     const int per_pass = blockDim.x / D > 0 ? blockDim.x / D : 1;  // words of a channel per pass
     const bool vact = (int)threadIdx.x < per_pass * D;
     const int c_me = (int)threadIdx.x % D, w_me = (int)threadIdx.x / D;
-    auto x_at = [&](int tok, int c) { return to_f32(tileT[(size_t)tok * D + c]); };
+    auto x_at = [&](int tok, int c) { return to_f32(tileV[(size_t)tok * D + c]); };
     for (int st = 0; st < n_sub && vact; ++st) {
       const int n_st = min(32, G - 32 * st);
       uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
@@ -477,7 +515,7 @@ cudaError_t launch_kb(const AppendParams& p, const dim3& grid, size_t smem, cuda
 template <typename T, int BITS>
 cudaError_t launch_t(const AppendParams& p, cudaStream_t s) {
   const dim3 grid(p.flush_blocks + p.window_blocks, p.n_seqs, p.Hkv);
-  const size_t smem = p.flush_blocks ? flush_smem_bytes(p.G, p.D, (int)sizeof(T)) : 0;
+  const size_t smem = p.flush_blocks ? flush_launch_smem(p.G, p.D, (int)sizeof(T)) : 0;
   const int rows_per_pass = kAppendThreads / (p.D / (16 / (int)sizeof(T)));
   return p.G <= 2 * rows_per_pass ? launch_kb<T, BITS, 2>(p, grid, smem, s) : launch_kb<T, BITS, 4>(p, grid, smem, s);
 }

@@ -105,7 +105,7 @@ kvq_status check_config(const kvq_config* c) {
   if (c->dtype != KVQ_BF16 && c->dtype != KVQ_FP32) return fail(KVQ_EINVAL, "unknown dtype %d", c->dtype);
   if (!(c->eps > 0.f) || !std::isfinite(c->eps)) return fail(KVQ_EINVAL, "eps must be positive and finite");
   const size_t flush_smem = kvq::flush_smem_bytes(c->group, c->head_dim, c->dtype == KVQ_BF16 ? 2 : 4);
-  if (flush_smem > 200 * 1024)
+  if (flush_smem > kvq::kFlushSmemMax)
     return fail(KVQ_EUNSUPPORTED, "group * head_dim too large for one flush tile (%zu bytes)", flush_smem);
   return KVQ_OK;
 }
@@ -404,7 +404,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   e = cudaMemcpy(c->layout, table.data(), table.size() * sizeof(kvq::SeqLayout), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(int32_t));
   if (e == cudaSuccess) {
-    const size_t smem = kvq::flush_smem_bytes(cfg->group, cfg->head_dim, esize_of(cfg));
+    const size_t smem = kvq::flush_launch_smem(cfg->group, cfg->head_dim, esize_of(cfg));
     e = kvq::configure_append(cfg->dtype, c->bits, smem);
   }
   if (cur != attr.device) cudaSetDevice(cur);
@@ -580,6 +580,7 @@ static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v
     p.qmax = c->cfg.qmax;
     p.bits = c->bits;
     p.eps = c->cfg.eps;
+    p.v_prefetch = kvq::flush_v_prefetch((int)G, p.D, (int)c->esize);
     p.geom = c->geom;
     p.pages = c->pages;
     p.map = page_map(c);

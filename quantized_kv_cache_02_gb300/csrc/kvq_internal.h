@@ -116,10 +116,20 @@ struct SegFlushParams {
 // the threads' 16-byte columns (rows per pass x D floats; 16 / esize channels
 // a column, kAppendThreads threads).
 constexpr int kAppendThreads = 256;
-inline size_t flush_smem_bytes(int G, int D, int esize) {
+__host__ __device__ inline size_t flush_smem_bytes(int G, int D, int esize) {
   const size_t partials = (size_t)kAppendThreads * (16 / esize) > (size_t)D ? (size_t)kAppendThreads * (16 / esize)
                                                                             : (size_t)D;
   return (size_t)G * D * esize + ((size_t)D + G + partials + G) * sizeof(float);
+}
+// Whether a flush CTA also holds a second tile, into which the Values are
+// copied (cp.async) while the Keys are reduced and packed; and the shared
+// memory of a flush launch with that choice.
+constexpr size_t kFlushSmemMax = 200 * 1024;
+inline bool flush_v_prefetch(int G, int D, int esize) {
+  return flush_smem_bytes(G, D, esize) + (size_t)G * D * esize <= kFlushSmemMax;
+}
+inline size_t flush_launch_smem(int G, int D, int esize) {
+  return flush_smem_bytes(G, D, esize) + (flush_v_prefetch(G, D, esize) ? (size_t)G * D * esize : 0);
 }
 
 struct AppendParams {
@@ -136,6 +146,7 @@ struct AppendParams {
   int32_t seq_begin, n_seqs;
   int32_t flush_blocks;        // grid.x slots for flush groups (0 if none in this launch)
   int32_t window_blocks;       // grid.x slots for window writes (0 or 1)
+  int32_t v_prefetch;          // flush_v_prefetch(G, D, esize)
   SeqCounters old[kMaxSeqsPerLaunch];
   // paged caches: the blocks of sequence i's new groups are
   // blk_ids[blk_first[i] ..]; the flush writes them into the block table
