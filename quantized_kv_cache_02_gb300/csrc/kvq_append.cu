@@ -268,19 +268,26 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     }
   };
 
-  // With room for a second tile the Values are copied into it now (cp.async),
-  // so that their latency passes while the Keys are reduced and packed.
+  // With room for a second tile both tiles are copied in at once (cp.async,
+  // Keys then Values): the Value latency passes while the Keys are reduced and
+  // packed.  Each thread copies the rows it reads back for the maxima.
   T* tileV = p.v_prefetch ? reinterpret_cast<T*>(reinterpret_cast<uint8_t*>(smem) + flush_smem_bytes(G, D, sizeof(T)))
                           : tileT;
   if (p.v_prefetch) {
-    if (act) {
-      for (int r = r0; r < G; r += rows_per_pass) {
-        const int t = t_first + r;
-        cp_async16(tileV + (size_t)r * D + col,
-                   t < T0 ? ring_v + (size_t)(ring_row0 + r) * D + col : in_v + (size_t)(t - T0) * D + col);
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const T* ring = kv ? ring_v : ring_k;
+      const T* input = kv ? in_v : in_k;
+      T* tile = kv ? tileV : tileT;
+      if (act) {
+        for (int r = r0; r < G; r += rows_per_pass) {
+          const int t = t_first + r;
+          cp_async16(tile + (size_t)r * D + col,
+                     t < T0 ? ring + (size_t)(ring_row0 + r) * D + col : input + (size_t)(t - T0) * D + col);
+        }
       }
+      asm volatile("cp.async.commit_group;\n" ::: "memory");
     }
-    asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
 
   // ---- Key: per-channel absmax over the group's tokens --------------------
@@ -288,10 +295,22 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     float amax[kVec];
 #pragma unroll
     for (int e = 0; e < kVec; ++e) amax[e] = 0.f;
-    load_rows(ring_k, in_k, [&](int, const float (&x)[kVec]) {
+    if (p.v_prefetch) {
+      asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // this thread's Key rows
+      if (act) {
+        for (int r = r0; r < G; r += rows_per_pass) {
+          float x[kVec];
+          unpack16(*reinterpret_cast<const uint4*>(tileT + (size_t)r * D + col), x);
 #pragma unroll
-      for (int e = 0; e < kVec; ++e) amax[e] = fmaxf(amax[e], fabsf(x[e]));
-    });
+          for (int e = 0; e < kVec; ++e) amax[e] = fmaxf(amax[e], fabsf(x[e]));
+        }
+      }
+    } else {
+      load_rows(ring_k, in_k, [&](int, const float (&x)[kVec]) {
+#pragma unroll
+        for (int e = 0; e < kVec; ++e) amax[e] = fmaxf(amax[e], fabsf(x[e]));
+      });
+    }
     if (act) {
 #pragma unroll
       for (int e = 0; e < kVec; ++e) part[r0 * D + col + e] = amax[e];
