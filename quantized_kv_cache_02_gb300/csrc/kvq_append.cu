@@ -17,6 +17,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "kvq_internal.h"
 
 namespace kvq {
@@ -47,6 +49,20 @@ template <int BITS>
 __device__ __forceinline__ constexpr uint32_t bias_word() {
   return BITS == 2 ? 0xAAAAAAAAu : BITS == 4 ? 0x88888888u : 0x80808080u;
 }
+
+// Two consecutive elements of shared memory, kept packed until used.
+struct PairF {
+  float2 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float2*>(p); }
+  __device__ __forceinline__ float get(int e) const { return e ? v.y : v.x; }
+};
+struct PairB {
+  uint32_t v;  // two bf16, the first in the low half
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint32_t*>(p); }
+  __device__ __forceinline__ float get(int e) const { return __uint_as_float(e ? (v & 0xFFFF0000u) : (v << 16)); }
+};
+template <typename T>
+using PairOf = typename std::conditional<sizeof(T) == 4, PairF, PairB>::type;
 
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
@@ -394,56 +410,45 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     __syncthreads();
   }
   {
-    // channel fastest across threads (each token row is read at consecutive
-    // addresses); each thread keeps one channel and steps over the words
+    // Value sub-tiles of 32 tokens, channel-major.  A work item is 8 tokens x 2
+    // channels: eight 2-channel loads from the tile, both channels' codes packed
+    // in registers (a word's token order is fixed), then one 4-bit word, one
+    // 2-bit piece or two 8-bit words per channel.
     uint8_t* vbase = page + geom.code_bytes;
-    const int n_sub = (G + 31) / 32;
-    const int per_pass = blockDim.x / D > 0 ? blockDim.x / D : 1;  // words of a channel per pass
-    const bool vact = (int)threadIdx.x < per_pass * D;
-    const int c_me = (int)threadIdx.x % D, w_me = (int)threadIdx.x / D;
-    auto x_at = [&](int tok, int c) { return to_f32(tileV[(size_t)tok * D + c]); };
-    for (int st = 0; st < n_sub && vact; ++st) {
-      const int n_st = min(32, G - 32 * st);
-      uint32_t* vc = reinterpret_cast<uint32_t*>(vbase + (int64_t)st * 32 * D * BITS / 8);
-      for (int c0 = 0; c0 < D; c0 += blockDim.x) {
-        const int c = c0 + c_me;
-        if (c >= D) break;
-        if (BITS == 2) {
-          // 16-bit pieces of 8 tokens: even tokens in the low byte, odd in the high
-          const int np = n_st / 8;  // pieces per channel row
-          uint16_t* vp = reinterpret_cast<uint16_t*>(vc);
-          for (int w = w_me; w < np; w += per_pass) {
-            uint32_t piece = 0;
+    const int n_cp = D / 2;
+    for (int item = threadIdx.x; item < (G / 8) * n_cp; item += blockDim.x) {
+      const int oct = item / n_cp, c = 2 * (item - oct * n_cp), t8 = 8 * oct;
+      const int st = t8 >> 5, n_st = min(32, G - 32 * st), o8 = (t8 & 31) >> 3;  // sub-tile, its length, octet
+      PairOf<T> xp[8];
 #pragma unroll
-            for (int f = 0; f < 4; ++f) {
-              const int te = 32 * st + 8 * w + 2 * f;
-              piece |= code_field<2>(quantize_int(x_at(te, c), sV[te]), f);
-              piece |= code_field<2>(quantize_int(x_at(te + 1, c), sV[te + 1]), 4 + f);
-            }
-            vp[c * np + w] = (uint16_t)(piece ^ bias_word<2>());
-          }
-        } else if (BITS == 4) {
-          const int nw = n_st / 8;  // words per channel row
-          for (int w = w_me; w < nw; w += per_pass) {
-            uint32_t word = 0;
+      for (int k = 0; k < 8; ++k) xp[k].load(tileV + (size_t)(t8 + k) * D + c);
+      uint8_t* sub = vbase + (int64_t)st * 32 * D * BITS / 8;
 #pragma unroll
-            for (int jn = 0; jn < 8; ++jn) {
-              const int tok = 32 * st + 8 * w + (jn < 4 ? 2 * jn : 2 * (jn - 4) + 1);
-              word |= code_field<4>(quantize_int(x_at(tok, c), sV[tok]), jn);
-            }
-            vc[c * nw + w] = word ^ bias_word<4>();
+      for (int e = 0; e < 2; ++e) {
+        if (BITS == 4) {
+          uint32_t word = 0;  // nibble jn holds token 2 jn (jn < 4) or 2 (jn - 4) + 1
+#pragma unroll
+          for (int jn = 0; jn < 8; ++jn) {
+            const int k = jn < 4 ? 2 * jn : 2 * (jn - 4) + 1;
+            word |= code_field<4>(quantize_int(xp[k].get(e), sV[t8 + k]), jn);
           }
+          reinterpret_cast<uint32_t*>(sub)[(c + e) * (n_st / 8) + o8] = word ^ bias_word<4>();
+        } else if (BITS == 2) {
+          uint32_t piece = 0;  // token 2f in bits 2f, token 2f + 1 in bits 8 + 2f
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            piece |= code_field<2>(quantize_int(xp[k].get(e), sV[t8 + k]), (k & 1) * 4 + (k >> 1));
+          reinterpret_cast<uint16_t*>(sub)[(c + e) * (n_st / 8) + o8] = (uint16_t)(piece ^ bias_word<2>());
         } else {
-          const int nw = n_st / 4;
-          for (int w = w_me; w < nw; w += per_pass) {
-            uint32_t word = 0;
+          uint32_t w0 = 0, w1 = 0;  // byte k of word w holds token 4 w + k
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int tok = 32 * st + 4 * w + k;
-              word |= code_field<8>(quantize_int(x_at(tok, c), sV[tok]), k);
-            }
-            vc[c * nw + w] = word ^ bias_word<8>();
+          for (int k = 0; k < 4; ++k) {
+            w0 |= code_field<8>(quantize_int(xp[k].get(e), sV[t8 + k]), k);
+            w1 |= code_field<8>(quantize_int(xp[4 + k].get(e), sV[t8 + 4 + k]), k);
           }
+          uint32_t* vc = reinterpret_cast<uint32_t*>(sub) + (c + e) * (n_st / 4) + 2 * o8;
+          vc[0] = w0 ^ bias_word<8>();
+          vc[1] = w1 ^ bias_word<8>();
         }
       }
     }
