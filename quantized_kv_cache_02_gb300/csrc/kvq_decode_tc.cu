@@ -6,20 +6,20 @@
 // of four 32-token units (128 tokens): one row of the 128 TMEM lanes per token
 // for the scores, one per channel for the output.
 //
-//   S[t][n] = sum_k A_K[t][k] B_Q[k][n]      (M = 128 tokens, N = 4 units x GP heads)
+//   S[t][n] = sum_k A_K[t][k] B_Q[k][n]      (M = 128 tokens, N = 4 units x (hi, lo) x GP heads)
 //   O^T[c][h] += sum_t A_V[c][t] B_P[t][h]   (M = 128 channels, N = 16)
 //
 // A_K (Key codes, one token per lane) and A_V (Value codes, one channel per
 // lane) are cut out of the stored words as f16 subnormals (code + 8) * 2^-24
 // exactly as in decode_mma_kernel and written to tensor memory with
-// tcgen05.st; B_Q = q / sK as an f16 hi + lo pair and B_P = p / sV as f16 sit in
+// tcgen05.st; B_Q = q / sK as f16 hi and lo rows and B_P = p / sV as f16 sit in
 // shared memory (K-major, no swizzle: 8-row x 16-byte core matrices, LBO the
-// step along K, SBO the step along N).  The offset bias comes back inside the
-// same accumulators: a constant A operand of -8 * 2^-24 (in every k-slot) times
-// the same B adds -8 * sum_k B.  One thread issues every MMA; completion is
-// signalled through tcgen05.commit on an mbarrier.  Softmax (base 2, the same
-// lazy running max as decode_mma_kernel, shared by the whole CTA) runs one token
-// per thread on the scores read back with tcgen05.ld.
+// step along K, SBO the step along N).  The offset bias is taken out on the CUDA
+// cores: 8 * sum_c q / sK per unit and head for the scores, and for the output
+// 8 times the sum of exactly the f16 values B_P held.  One thread issues every
+// MMA; completion is signalled through tcgen05.commit on mbarriers.  Softmax
+// (base 2, the same lazy running max as decode_mma_kernel, shared by the whole
+// CTA) runs one token per thread on the scores read back with tcgen05.ld.
 // ("KV Cache Quantization Strategies", restore; "KV Cache 与自回归视频生成"
 // 3.1, attn_step and section 05, FlashDecoding.)
 
@@ -29,16 +29,6 @@ namespace kvq {
 namespace {
 
 // ---- tcgen05 PTX -----------------------------------------------------------
-constexpr uint32_t kTmemCols = 256;
-
-__device__ __forceinline__ void tc_alloc(uint32_t dst_smem) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "n"(kTmemCols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tc_dealloc(uint32_t taddr) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kTmemCols) : "memory");
-}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
