@@ -796,8 +796,8 @@ constexpr int kFlat32 = 0, kPaged32 = 1, kStaged = 2;
 
 // The residual-window item of unit (sequence i of the launch, KV head h): its
 // ring rows on the tensor cores (plus, for kvq_decode_step, this step's token,
-// which it also stores into its ring row).  ``buf`` holds kRowsBuf<D, 1> bytes
-// per warp.
+// which it also stores into its ring row).  ``buf`` holds kRowsBuf<D, 2> bytes
+// per warp: each warp's next 16 rows are copied in while it works on these.
 template <int D, int GP>
 __device__ __forceinline__ void window_rows(const DecodeParams& p, int i, int h, int lane, int warp, int gid, int tig,
                                             uint8_t* buf, WarpState<D>& st) {
@@ -820,9 +820,9 @@ __device__ __forceinline__ void window_rows(const DecodeParams& p, int i, int h,
       reinterpret_cast<uint4*>(rv + row)[c] = reinterpret_cast<const uint4*>(lv)[c];
     }
   }
-  rows_mma<D, GP, 1, true>(p, rk, rv, Q0, p.Rcap, (int)(T0 - Q0),
+  rows_mma<D, GP, 2, true>(p, rk, rv, Q0, p.Rcap, (int)(T0 - Q0),
                            reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + h * p.g) * D, lane,
-                           warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 1>, st, lk, lv);
+                           warp, gid, tig, buf + (size_t)warp * kRowsBuf<D, 2>, st, lk, lv);
 }
 
 template <int D, int BITS, int GP, int MODE>
@@ -1111,7 +1111,7 @@ size_t smem_for(const DecodeParams& p) {
   const int slots = mma_slots(unit_bytes(p), p.g);
   size_t pages = (size_t)kMmaWarps * slots * unit_bytes(p);
   const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
-  const size_t window = (size_t)kMmaWarps * kRowsBuf<D, 1>;
+  const size_t window = (size_t)kMmaWarps * kRowsBuf<D, 2>;
   if (pages < merge) pages = merge;
   if (pages < window) pages = window;
   const size_t scratch = ((size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D + (size_t)gqa_pad(p.g) * D) * sizeof(float);
