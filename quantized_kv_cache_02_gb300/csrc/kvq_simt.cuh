@@ -149,30 +149,50 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
     // of tokens); the Value scale 1/sV goes onto the token's codes.
     const int32_t* first = p.seg.first + (int64_t)b * p.seg.cap;
     int cur = -1;
-    for (int64_t t = pg0 + warp; t < pg1; t += kSimtWarps) {
-      const int f = first[t];  // the same for every lane of the warp
-      if (f != cur) {
-        const float* ks = p.seg.kscales + (unit * p.seg.cap + f) * D;
+    // two tokens per pass (head_dim <= 128): both tokens' codes and scales are loaded before
+    // either is used, so their memory latencies overlap
+    constexpr int kTok = CPL <= 4 ? 2 : 1;
+    for (int64_t t0 = pg0 + warp; t0 < pg1; t0 += kTok * kSimtWarps) {
+      int fk[kTok], kc[kTok][CPL], vc[kTok][CPL];
+      float vsr[kTok];
+#pragma unroll
+      for (int u = 0; u < kTok; ++u) {
+        const int64_t t = t0 + u * kSimtWarps;
+        const bool ok = t < pg1;  // the same for every lane of the warp
+        const int64_t row = unit * p.seg.cap + (ok ? t : t0);
+        const uint8_t* kr = p.seg.kcodes + row * p.seg.row_bytes;
+        const uint8_t* vr = p.seg.vcodes + row * p.seg.row_bytes;
+        fk[u] = ok ? first[t] : -1;
+        vsr[u] = p.seg.vscales[row];
 #pragma unroll
         for (int k = 0; k < CPL; ++k) {
           const int c = lane + 32 * k;
-          const float r = c < D ? __frcp_rn(fmaxf(ks[c], p.eps)) : 0.f;
-#pragma unroll
-          for (int j = 0; j < kMaxGqa; ++j) qv[j][k] = qs[j][c] * r;  // q / sK from here on
+          kc[u][k] = c < D ? key_code<BITS>(kr, 0, c, D) : 0;
+          vc[u][k] = c < D ? key_code<BITS>(vr, 0, c, D) : 0;
         }
-        cur = f;
       }
-      const int64_t row = unit * p.seg.cap + t;
-      const uint8_t* kr = p.seg.kcodes + row * p.seg.row_bytes;
-      const uint8_t* vr = p.seg.vcodes + row * p.seg.row_bytes;
-      const float iv = __frcp_rn(fmaxf(p.seg.vscales[row], p.eps));
 #pragma unroll
-      for (int k = 0; k < CPL; ++k) {
-        const int c = lane + 32 * k;
-        kv[k] = c < D ? (float)key_code<BITS>(kr, 0, c, D) : 0.f;
-        vv[k] = c < D ? (float)key_code<BITS>(vr, 0, c, D) * iv : 0.f;
+      for (int u = 0; u < kTok; ++u) {
+        if (fk[u] < 0) break;
+        if (fk[u] != cur) {
+          const float* ks = p.seg.kscales + (unit * p.seg.cap + fk[u]) * D;
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) {
+            const int c = lane + 32 * k;
+            const float r = c < D ? __frcp_rn(fmaxf(ks[c], p.eps)) : 0.f;
+#pragma unroll
+            for (int j = 0; j < kMaxGqa; ++j) qv[j][k] = qs[j][c] * r;  // q / sK from here on
+          }
+          cur = fk[u];
+        }
+        const float iv = __frcp_rn(fmaxf(vsr[u], p.eps));
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+          kv[k] = (float)kc[u][k];
+          vv[k] = (float)vc[u][k] * iv;
+        }
+        simt_token<CPL>(s, qv, kv, vv, g);
       }
-      simt_token<CPL>(s, qv, kv, vv, g);
     }
   } else {
     const int64_t ntok = (int64_t)(pg1 - pg0) * G;
