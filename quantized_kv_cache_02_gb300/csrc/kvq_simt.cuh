@@ -89,6 +89,36 @@ __host__ __device__ constexpr int simt_scratch_floats() {
   return kMaxGqa * CPL * 32 + 2 * kSimtWarps * kMaxGqa + kSimtWarps * kMaxGqa * CPL * 32;
 }
 
+// Channel of register k of a lane: strided (lane + 32 k) in general; for a
+// segmented cache contiguous (CPL lane + k), so that a token's codes for the
+// lane are one load.
+template <int CPL, bool SEG>
+__device__ __forceinline__ constexpr int lane_chan(int lane, int k) {
+  return SEG ? CPL * lane + k : lane + 32 * k;
+}
+
+// Codes of channels CPL lane .. CPL lane + CPL - 1 of a token row.
+template <int BITS, int CPL>
+__device__ __forceinline__ void row_codes(const uint8_t* row, int lane, int D, int (&code)[CPL]) {
+  constexpr int kBits = CPL * BITS;  // bits of the lane's slice: 2 .. 64, aligned to its size
+  const int c0 = CPL * lane;
+  if (c0 >= D) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) code[k] = 0;
+    return;
+  }
+  uint64_t v;
+  const uint8_t* src = row + c0 * BITS / 8;
+  if constexpr (kBits < 8) v = (uint64_t)(*src >> ((c0 * BITS) & 7));  // inside one byte
+  else if constexpr (kBits == 8) v = *src;
+  else if constexpr (kBits == 16) v = *reinterpret_cast<const uint16_t*>(src);
+  else if constexpr (kBits == 32) v = *reinterpret_cast<const uint32_t*>(src);
+  else v = *reinterpret_cast<const uint64_t*>(src);
+  constexpr int kBias = BITS == 2 ? 2 : BITS == 4 ? 8 : 128;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) code[k] = (int)((v >> (BITS * k)) & ((1u << BITS) - 1u)) - kBias;
+}
+
 // Whole split item on CUDA cores; writes the partial of slot ``slot``.
 // ``win`` selects the residual window (tokens [Q, T) from the ring) instead of
 // pages [pg0, pg1) of the quantized prefix.
@@ -116,7 +146,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
 #pragma unroll
   for (int j = 0; j < kMaxGqa; ++j)
 #pragma unroll
-    for (int k = 0; k < CPL; ++k) qv[j][k] = qs[j][lane + 32 * k];
+    for (int k = 0; k < CPL; ++k) qv[j][k] = qs[j][lane_chan<CPL, SEG>(lane, k)];
 
   SimtState<CPL> s;
 #pragma unroll
@@ -136,7 +166,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
       const int64_t row = (t % p.Rcap) * D;
 #pragma unroll
       for (int k = 0; k < CPL; ++k) {
-        const int c = lane + 32 * k;
+        const int c = lane_chan<CPL, SEG>(lane, k);
         kv[k] = c < D ? ld_f32(rk, row + c) : 0.f;
         vv[k] = c < D ? ld_f32(rv, row + c) : 0.f;
       }
@@ -164,12 +194,8 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
         const uint8_t* vr = p.seg.vcodes + row * p.seg.row_bytes;
         fk[u] = ok ? first[t] : -1;
         vsr[u] = p.seg.vscales[row];
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-          const int c = lane + 32 * k;
-          kc[u][k] = c < D ? key_code<BITS>(kr, 0, c, D) : 0;
-          vc[u][k] = c < D ? key_code<BITS>(vr, 0, c, D) : 0;
-        }
+        row_codes<BITS, CPL>(kr, lane, D, kc[u]);
+        row_codes<BITS, CPL>(vr, lane, D, vc[u]);
       }
 #pragma unroll
       for (int u = 0; u < kTok; ++u) {
@@ -178,7 +204,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
           const float* ks = p.seg.kscales + (unit * p.seg.cap + fk[u]) * D;
 #pragma unroll
           for (int k = 0; k < CPL; ++k) {
-            const int c = lane + 32 * k;
+            const int c = lane_chan<CPL, SEG>(lane, k);
             const float r = c < D ? __frcp_rn(fmaxf(ks[c], p.eps)) : 0.f;
 #pragma unroll
             for (int j = 0; j < kMaxGqa; ++j) qv[j][k] = qs[j][c] * r;  // q / sK from here on
@@ -227,7 +253,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
 #pragma unroll
   for (int j = 0; j < kMaxGqa; ++j)
 #pragma unroll
-    for (int k = 0; k < CPL; ++k) wo[warp][j][lane + 32 * k] = s.o[j][k];
+    for (int k = 0; k < CPL; ++k) wo[warp][j][lane_chan<CPL, SEG>(lane, k)] = s.o[j][k];
   __syncthreads();
   float* part = p.partials + (unit * p.max_splits + slot) * (int64_t)g * part_row(D);
   for (int idx = threadIdx.x; idx < g * D; idx += blockDim.x) {
