@@ -31,19 +31,26 @@ __device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
   return (int)r;
 }
 
-// code = clamp(rint(x * scale), -qmax, qmax) as one rounding conversion.  The
-// clamp never acts here: |x| <= absmax and scale = qmax / max(absmax, eps)
-// (each rounded once) make |x * scale| <= qmax (1 + 2^-23) < qmax + 1/2, so
-// rint already lies in [-qmax, qmax]; round-to-nearest-even conversion is rint.
-__device__ __forceinline__ int quantize_int(float x, float scale) { return __float2int_rn(__fmul_rn(x, scale)); }
+// code = clamp(rint(x * scale), -qmax, qmax), returned as a word whose low
+// bits are the code's two's complement.  The clamp never acts here: |x| <=
+// absmax and scale = qmax / max(absmax, eps) (each rounded once) make
+// |x * scale| <= qmax (1 + 2^-23) < qmax + 1/2, so rint already lies in
+// [-qmax, qmax].  rint is the add of 1.5 * 2^23: the sum's unit in the last
+// place is 1, so the add rounds x * scale to the nearest integer n, ties to
+// even as rint does, and the sum's mantissa field holds 2^22 + n, whose low
+// bits (2^22 is a multiple of 256) are n's.  One add on the FMA pipe instead
+// of a float-to-int conversion; the product is rounded on its own first.
+__device__ __forceinline__ uint32_t quantize_bits(float x, float scale) {
+  return __float_as_uint(__fadd_rn(__fmul_rn(x, scale), 12582912.f));
+}
 
-// The low BITS bits of a code's two's complement, at field k of a word.  The
-// stored offset binary code + 2^(BITS-1) is those bits with the top one
-// flipped (for every code the width holds), which bias_word does for a whole
-// word at once.
+// The low BITS bits of a code's two's complement (the low bits of ``bits``),
+// at field k of a word.  The stored offset binary code + 2^(BITS-1) is those
+// bits with the top one flipped (for every code the width holds), which
+// bias_word does for a whole word at once.
 template <int BITS>
-__device__ __forceinline__ uint32_t code_field(int code, int k) {
-  return ((uint32_t)code & ((1u << BITS) - 1u)) << (BITS * k);
+__device__ __forceinline__ uint32_t code_field(uint32_t bits, int k) {
+  return (bits & ((1u << BITS) - 1u)) << (BITS * k);
 }
 template <int BITS>
 __device__ __forceinline__ constexpr uint32_t bias_word() {
@@ -357,7 +364,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
         uint32_t word = 0;
 #pragma unroll
         for (int k = 0; k < kPerWord; ++k)
-          word |= code_field<BITS>(quantize_int(x[k], sc[k]), k);
+          word |= code_field<BITS>(quantize_bits(x[k], sc[k]), k);
         kc[t * words_per_row + w] = word ^ bias_word<BITS>();
       }
     }
@@ -430,21 +437,21 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
 #pragma unroll
           for (int jn = 0; jn < 8; ++jn) {
             const int k = jn < 4 ? 2 * jn : 2 * (jn - 4) + 1;
-            word |= code_field<4>(quantize_int(xp[k].get(e), sV[t8 + k]), jn);
+            word |= code_field<4>(quantize_bits(xp[k].get(e), sV[t8 + k]), jn);
           }
           reinterpret_cast<uint32_t*>(sub)[(c + e) * (n_st / 8) + o8] = word ^ bias_word<4>();
         } else if (BITS == 2) {
           uint32_t piece = 0;  // token 2f in bits 2f, token 2f + 1 in bits 8 + 2f
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            piece |= code_field<2>(quantize_int(xp[k].get(e), sV[t8 + k]), (k & 1) * 4 + (k >> 1));
+            piece |= code_field<2>(quantize_bits(xp[k].get(e), sV[t8 + k]), (k & 1) * 4 + (k >> 1));
           reinterpret_cast<uint16_t*>(sub)[(c + e) * (n_st / 8) + o8] = (uint16_t)(piece ^ bias_word<2>());
         } else {
           uint32_t w0 = 0, w1 = 0;  // byte k of word w holds token 4 w + k
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            w0 |= code_field<8>(quantize_int(xp[k].get(e), sV[t8 + k]), k);
-            w1 |= code_field<8>(quantize_int(xp[4 + k].get(e), sV[t8 + 4 + k]), k);
+            w0 |= code_field<8>(quantize_bits(xp[k].get(e), sV[t8 + k]), k);
+            w1 |= code_field<8>(quantize_bits(xp[4 + k].get(e), sV[t8 + 4 + k]), k);
           }
           uint32_t* vc = reinterpret_cast<uint32_t*>(sub) + (c + e) * (n_st / 4) + 2 * o8;
           vc[0] = w0 ^ bias_word<8>();
