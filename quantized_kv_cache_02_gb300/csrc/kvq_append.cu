@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     constexpr int kVec = 16 / sizeof(T);
     constexpr int kBatch = 4;
     const int per_row = D / kVec;
-    const int rows_per_pass = blockDim.x / per_row;
+    const int rows_per_pass = kAppendThreads / per_row;
     if ((int)threadIdx.x >= rows_per_pass * per_row) return;
     const int r0 = threadIdx.x / per_row, c = (threadIdx.x - r0 * per_row) * kVec;
     const int t_lo = Q1 > T0 ? Q1 : T0;
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
   float* part = sV + G;                                          // [rows_per_pass][D] partial Key maxima
   const float qmax = (float)p.qmax;
   const int per_row = D / kVec;
-  const int rows_per_pass = blockDim.x / per_row;
+  const int rows_per_pass = kAppendThreads / per_row;
   const bool act = (int)threadIdx.x < rows_per_pass * per_row;
   const int r0 = act ? threadIdx.x / per_row : 0, col = act ? (threadIdx.x - r0 * per_row) * kVec : 0;
   const int ring_row0 = t_first % Rcap;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       for (int e = 0; e < kVec; ++e) part[r0 * D + col + e] = amax[e];
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    for (int c = threadIdx.x; c < D; c += kAppendThreads) {
       float a = 0.f;
       for (int r = 0; r < rows_per_pass; ++r) a = fmaxf(a, part[r * D + c]);
       sK[c] = __fdiv_rn(qmax, fmaxf(a, p.eps));
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     // word column (and its scales) and steps over the token rows
     constexpr int kPerWord = 32 / BITS;  // codes per 32-bit word
     const int words_per_row = D / kPerWord;
-    const int rows_pp = blockDim.x / words_per_row;
+    const int rows_pp = kAppendThreads / words_per_row;
     uint32_t* kc = reinterpret_cast<uint32_t*>(page);
     if ((int)threadIdx.x < rows_pp * words_per_row) {
       const int t0 = threadIdx.x / words_per_row, w = threadIdx.x - t0 * words_per_row;
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       }
     }
     float* ks = reinterpret_cast<float*>(page + geom.kscale_off);
-    for (int c = threadIdx.x; c < D; c += blockDim.x) ks[c] = sK[c];
+    for (int c = threadIdx.x; c < D; c += kAppendThreads) ks[c] = sK[c];
   }
   __syncthreads();  // the tile is rewritten with the Values
 
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     const bool shuffle_rows = (per_row & (per_row - 1)) == 0 && per_row <= 32;
     uint32_t* rmax = reinterpret_cast<uint32_t*>(part);  // [G] bits of row maxima (other widths)
     if (!shuffle_rows) {
-      for (int t = threadIdx.x; t < G; t += blockDim.x) rmax[t] = 0u;
+      for (int t = threadIdx.x; t < G; t += kAppendThreads) rmax[t] = 0u;
       __syncthreads();
     }
     auto row_max = [&](int r, const float (&x)[kVec]) {
@@ -412,7 +412,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     }
     __syncthreads();
     // one division per token, spread over the CTA (not inside the row loop)
-    for (int t = threadIdx.x; t < G; t += blockDim.x)
+    for (int t = threadIdx.x; t < G; t += kAppendThreads)
       sV[t] = __fdiv_rn(qmax, fmaxf(shuffle_rows ? sV[t] : __uint_as_float(rmax[t]), p.eps));
     __syncthreads();
   }
@@ -423,7 +423,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     // 2-bit piece or two 8-bit words per channel.
     uint8_t* vbase = page + geom.code_bytes;
     const int n_cp = D / 2;
-    for (int item = threadIdx.x; item < (G / 8) * n_cp; item += blockDim.x) {
+    for (int item = threadIdx.x; item < (G / 8) * n_cp; item += kAppendThreads) {
       const int oct = item / n_cp, c = 2 * (item - oct * n_cp), t8 = 8 * oct;
       const int st = t8 >> 5, n_st = min(32, G - 32 * st), o8 = (t8 & 31) >> 3;  // sub-tile, its length, octet
       PairOf<T> xp[8];
@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       }
     }
     float* vs = reinterpret_cast<float*>(page + geom.vscale_off);
-    for (int t = threadIdx.x; t < G; t += blockDim.x) vs[t] = sV[t];
+    for (int t = threadIdx.x; t < G; t += kAppendThreads) vs[t] = sV[t];
   }
 }
 
