@@ -116,59 +116,6 @@ __device__ __forceinline__ void load_elems(const T* src, float (&x)[N]) {
   }
 }
 
-// 16 bytes of elements -> fp32 into shared memory.
-__device__ __forceinline__ void store_f32(float* dst, const uint4& raw, float) {
-  const float* f = reinterpret_cast<const float*>(&raw);
-  dst[0] = f[0];
-  dst[1] = f[1];
-  dst[2] = f[2];
-  dst[3] = f[3];
-}
-__device__ __forceinline__ void store_f32(float* dst, const uint4& raw, __nv_bfloat16) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float2 f = __bfloat1622float2(h[e]);
-    dst[2 * e] = f.x;
-    dst[2 * e + 1] = f.y;
-  }
-}
-
-// Stage the G x D tile of tokens [t_first, t_first + G) as fp32 in shared
-// memory, 16 bytes per load and four loads in flight per thread.  Tokens below
-// T0 come from the ring: a group starts at a multiple of G and the ring length
-// is a multiple of G, so its rows are contiguous there.  Later tokens come from
-// the input.  Each thread keeps one 16-byte column and steps over rows, so no
-// index is divided inside the loop.
-template <typename T>
-__device__ void load_group(float* tile, const T* ring, const T* input, int t_first, int T0, int G, int D,
-                           int Rcap) {
-  constexpr int kVec = 16 / sizeof(T);
-  constexpr int kBatch = 4;
-  const int per_row = D / kVec;
-  const int rows_per_pass = blockDim.x / per_row;
-  if ((int)threadIdx.x >= rows_per_pass * per_row) return;
-  const int r0 = threadIdx.x / per_row, c = (threadIdx.x - r0 * per_row) * kVec;
-  const int ring_row0 = t_first % Rcap;
-  for (int tl = r0; tl < G; tl += kBatch * rows_per_pass) {
-    uint4 v[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int r = tl + k * rows_per_pass;
-      if (r < G) {
-        const int t = t_first + r;
-        const T* src = t < T0 ? ring + (size_t)(ring_row0 + r) * D + c : input + (size_t)(t - T0) * D + c;
-        v[k] = *reinterpret_cast<const uint4*>(src);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int r = tl + k * rows_per_pass;
-      if (r < G) store_f32(tile + r * D + c, v[k], T());
-    }
-  }
-}
-
 // DC: head_dim as a compile-time constant (64, 128), or 0 for any other.
 // KB: rows a flush thread loads per batch (2 when the group is only a pass or
 // two of rows deep, 4 for deeper groups), so that short groups do not issue
@@ -303,11 +250,13 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       const T* input = kv ? in_v : in_k;
       T* tile = kv ? tileV : tileT;
       if (act) {
-        for (int r = r0; r < G; r += rows_per_pass) {
-          const int t = t_first + r;
-          cp_async16(tile + (size_t)r * D + col,
-                     t < T0 ? ring + (size_t)(ring_row0 + r) * D + col : input + (size_t)(t - T0) * D + col);
-        }
+        // rows below ``split`` come from the ring (contiguous from ring_row0),
+        // the rest from the input (row r at element in_off + r * D)
+        const int split = T0 - t_first;
+        const T* ring_r = ring + (size_t)ring_row0 * D + col;
+        const int64_t in_off = ((int64_t)t_first - T0) * D + col;
+        for (int r = r0; r < G; r += rows_per_pass)
+          cp_async16(tile + (size_t)r * D + col, r < split ? ring_r + (size_t)r * D : input + (in_off + (int64_t)r * D));
       }
       asm volatile("cp.async.commit_group;\n" ::: "memory");
     }
