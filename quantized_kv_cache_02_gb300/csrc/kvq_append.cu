@@ -31,30 +31,39 @@ __device__ __forceinline__ int quantize_one(float x, float scale, float qmax) {
   return (int)r;
 }
 
-// code = clamp(rint(x * scale), -qmax, qmax), returned as a word whose low
-// bits are the code's two's complement.  The clamp never acts here: |x| <=
-// absmax and scale = qmax / max(absmax, eps) (each rounded once) make
-// |x * scale| <= qmax (1 + 2^-23) < qmax + 1/2, so rint already lies in
-// [-qmax, qmax].  rint is the add of 1.5 * 2^23: the sum's unit in the last
-// place is 1, so the add rounds x * scale to the nearest integer n, ties to
-// even as rint does, and the sum's mantissa field holds 2^22 + n, whose low
-// bits (2^22 is a multiple of 256) are n's.  One add on the FMA pipe instead
-// of a float-to-int conversion; the product is rounded on its own first.
+// The stored offset-binary code clamp(rint(x * scale), -qmax, qmax) +
+// 2^(BITS-1), in the low BITS bits of the returned word.  The clamp never
+// acts here: |x| <= absmax and scale = qmax / max(absmax, eps) (each rounded
+// once) make |x * scale| <= qmax (1 + 2^-23) < qmax + 1/2, so rint already
+// lies in [-qmax, qmax].  The product, rounded on its own, then gets one add
+// of 1.5 * 2^23 + 2^(BITS-1): the sum's unit in the last place is 1, so the
+// add rounds to the nearest integer with ties to even, which is rint(x *
+// scale) + 2^(BITS-1) because the bias is even; the sum's mantissa field
+// holds 2^22 plus that integer, and 2^22 being a multiple of 256, its low
+// bits are the offset code (in [1, 2^BITS - 1]).  One FMA-pipe add stands for
+// the conversion, the clamp and the bias.
+template <int BITS>
 __device__ __forceinline__ uint32_t quantize_bits(float x, float scale) {
-  return __float_as_uint(__fadd_rn(__fmul_rn(x, scale), 12582912.f));
+  constexpr float kMagic = 12582912.f + (float)(1 << (BITS - 1));
+  return __float_as_uint(__fadd_rn(__fmul_rn(x, scale), kMagic));
 }
 
-// The low BITS bits of a code's two's complement (the low bits of ``bits``),
-// at field k of a word.  The stored offset binary code + 2^(BITS-1) is those
-// bits with the top one flipped (for every code the width holds), which
-// bias_word does for a whole word at once.
+// The offset code in the low BITS bits of ``bits`` at field k of a word.
 template <int BITS>
 __device__ __forceinline__ uint32_t code_field(uint32_t bits, int k) {
   return (bits & ((1u << BITS) - 1u)) << (BITS * k);
 }
-template <int BITS>
-__device__ __forceinline__ constexpr uint32_t bias_word() {
-  return BITS == 2 ? 0xAAAAAAAAu : BITS == 4 ? 0x88888888u : 0x80808080u;
+
+// The low bytes of four words as the bytes 0..3 of one word.
+__device__ __forceinline__ uint32_t low_bytes(uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  return __byte_perm(__byte_perm(b0, b1, 0x0040), __byte_perm(b2, b3, 0x0040), 0x5410);
+}
+// Eight 4-bit codes (low nibbles of the arguments) into one word: lo0..lo3
+// go to the low nibbles of bytes 0..3, hi0..hi3 to their high nibbles.
+__device__ __forceinline__ uint32_t pack_nibbles(uint32_t lo0, uint32_t lo1, uint32_t lo2, uint32_t lo3, uint32_t hi0,
+                                                 uint32_t hi1, uint32_t hi2, uint32_t hi3) {
+  const uint32_t lo = low_bytes(lo0, lo1, lo2, lo3), hi = low_bytes(hi0, hi1, hi2, hi3);
+  return (lo & 0x0F0F0F0Fu) | ((hi << 4) & 0xF0F0F0F0u);
 }
 
 // Two consecutive elements of shared memory, kept packed until used.
@@ -310,11 +319,19 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       for (int t = t0; t < G; t += rows_pp) {
         float x[kPerWord];
         load_elems<T, kPerWord>(tileT + (size_t)t * D + w * kPerWord, x);
-        uint32_t word = 0;
+        uint32_t c[kPerWord];
 #pragma unroll
-        for (int k = 0; k < kPerWord; ++k)
-          word |= code_field<BITS>(quantize_bits(x[k], sc[k]), k);
-        kc[t * words_per_row + w] = word ^ bias_word<BITS>();
+        for (int k = 0; k < kPerWord; ++k) c[k] = quantize_bits<BITS>(x[k], sc[k]);
+        uint32_t word = 0;  // channel k of the word in field k
+        if constexpr (BITS == 4) {
+          word = pack_nibbles(c[0], c[2], c[4], c[6], c[1], c[3], c[5], c[7]);
+        } else if constexpr (BITS == 8) {
+          word = low_bytes(c[0], c[1], c[2], c[3]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kPerWord; ++k) word |= code_field<BITS>(c[k], k);
+        }
+        kc[t * words_per_row + w] = word;
       }
     }
     float* ks = reinterpret_cast<float*>(page + geom.kscale_off);
@@ -381,30 +398,24 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       uint8_t* sub = vbase + (int64_t)st * 32 * D * BITS / 8;
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        if (BITS == 4) {
-          uint32_t word = 0;  // nibble jn holds token 2 jn (jn < 4) or 2 (jn - 4) + 1
+        uint32_t cv[8];
 #pragma unroll
-          for (int jn = 0; jn < 8; ++jn) {
-            const int k = jn < 4 ? 2 * jn : 2 * (jn - 4) + 1;
-            word |= code_field<4>(quantize_bits(xp[k].get(e), sV[t8 + k]), jn);
-          }
-          reinterpret_cast<uint32_t*>(sub)[(c + e) * (n_st / 8) + o8] = word ^ bias_word<4>();
+        for (int k = 0; k < 8; ++k) cv[k] = quantize_bits<BITS>(xp[k].get(e), sV[t8 + k]);
+        if (BITS == 4) {
+          // nibbles 0..7 hold tokens 0, 2, 4, 6, 1, 3, 5, 7: bytes 0..3 pair
+          // tokens (0, 2), (4, 6), (1, 3), (5, 7)
+          reinterpret_cast<uint32_t*>(sub)[(c + e) * (n_st / 8) + o8] =
+              pack_nibbles(cv[0], cv[4], cv[1], cv[5], cv[2], cv[6], cv[3], cv[7]);
         } else if (BITS == 2) {
           uint32_t piece = 0;  // token 2f in bits 2f, token 2f + 1 in bits 8 + 2f
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            piece |= code_field<2>(quantize_bits(xp[k].get(e), sV[t8 + k]), (k & 1) * 4 + (k >> 1));
-          reinterpret_cast<uint16_t*>(sub)[(c + e) * (n_st / 8) + o8] = (uint16_t)(piece ^ bias_word<2>());
+          for (int k = 0; k < 8; ++k) piece |= code_field<2>(cv[k], (k & 1) * 4 + (k >> 1));
+          reinterpret_cast<uint16_t*>(sub)[(c + e) * (n_st / 8) + o8] = (uint16_t)piece;
         } else {
-          uint32_t w0 = 0, w1 = 0;  // byte k of word w holds token 4 w + k
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            w0 |= code_field<8>(quantize_bits(xp[k].get(e), sV[t8 + k]), k);
-            w1 |= code_field<8>(quantize_bits(xp[4 + k].get(e), sV[t8 + 4 + k]), k);
-          }
+          // byte k of word w holds token 4 w + k
           uint32_t* vc = reinterpret_cast<uint32_t*>(sub) + (c + e) * (n_st / 4) + 2 * o8;
-          vc[0] = w0 ^ bias_word<8>();
-          vc[1] = w1 ^ bias_word<8>();
+          vc[0] = low_bytes(cv[0], cv[1], cv[2], cv[3]);
+          vc[1] = low_bytes(cv[4], cv[5], cv[6], cv[7]);
         }
       }
     }
