@@ -119,6 +119,42 @@ __device__ __forceinline__ void row_codes(const uint8_t* row, int lane, int D, i
   for (int k = 0; k < CPL; ++k) code[k] = (int)((v >> (BITS * k)) & ((1u << BITS) - 1u)) - kBias;
 }
 
+// Sums over the 32 lanes of N values (N = 4 or 8), every lane ending with all
+// N sums.  The first log2(N) exchange steps halve the set each time, a lane
+// keeping the half its lane bit selects, so each exchange carries half as many
+// values as the last; the remaining steps finish one sum per lane, and N
+// shuffles hand the sums back: 17 shuffles for 8 values instead of 40.
+template <int N>
+__device__ __forceinline__ void warp_sum_n(float (&v)[N], int lane) {
+  static_assert(N == 4 || N == 8, "4 or 8 values");
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+  float a[N / 2];
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float mine = b4 ? v[N / 2 + i] : v[i], other = b4 ? v[i] : v[N / 2 + i];
+    a[i] = mine + __shfl_xor_sync(0xffffffffu, other, 16);
+  }
+  float x;
+  if constexpr (N == 8) {
+    float c[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float mine = b3 ? a[2 + i] : a[i], other = b3 ? a[i] : a[2 + i];
+      c[i] = mine + __shfl_xor_sync(0xffffffffu, other, 8);
+    }
+    x = (b2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, b2 ? c[0] : c[1], 4);  // value 4 b4 + 2 b3 + b2
+  } else {
+    x = (b3 ? a[1] : a[0]) + __shfl_xor_sync(0xffffffffu, b3 ? a[0] : a[1], 8);  // value 2 b4 + b3
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+  }
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+#pragma unroll
+  for (int i = 0; i < N; ++i)
+    v[i] = N == 8 ? __shfl_sync(0xffffffffu, x, ((i >> 2) & 1) * 16 + ((i >> 1) & 1) * 8 + (i & 1) * 4)
+                  : __shfl_sync(0xffffffffu, x, ((i >> 1) & 1) * 16 + (i & 1) * 8);
+}
+
 // Whole split item on CUDA cores; writes the partial of slot ``slot``.
 // ``win`` selects the residual window (tokens [Q, T) from the ring) instead of
 // pages [pg0, pg1) of the quantized prefix.
@@ -176,12 +212,17 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
     // segmented cache: a "page" is one token of the token-major code rows.
     // q.k = sum_c q_c code_c / sK_c: the 1/sK of the token's segment is folded
     // into q whenever the segment changes (a prefill segment spans thousands
-    // of tokens); the Value scale 1/sV goes onto the token's codes.
+    // of tokens); the Value scale 1/sV goes onto the token's codes.  Two
+    // tokens per pass (head_dim <= 128): both tokens' codes and scales are
+    // loaded before either is used, so their memory latencies overlap, and
+    // the pass's (token, head) dot products are summed over the warp at once.
+    // The running max moves only when a score exceeds it by more than 8 (in
+    // base 2), as in the tensor-core kernel: l and o always share m, so o / l
+    // is exact, and a token costs one exp2 per head.
     const int32_t* first = p.seg.first + (int64_t)b * p.seg.cap;
     int cur = -1;
-    // two tokens per pass (head_dim <= 128): both tokens' codes and scales are loaded before
-    // either is used, so their memory latencies overlap
     constexpr int kTok = CPL <= 4 ? 2 : 1;
+    constexpr float kSlack = 8.f;
     for (int64_t t0 = pg0 + warp; t0 < pg1; t0 += kTok * kSimtWarps) {
       int fk[kTok], kc[kTok][CPL], vc[kTok][CPL];
       float vsr[kTok];
@@ -197,10 +238,11 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
         row_codes<BITS, CPL>(kr, lane, D, kc[u]);
         row_codes<BITS, CPL>(vr, lane, D, vc[u]);
       }
+      // this lane's share of every (token, head) dot product
+      float part[kTok][kMaxGqa];
 #pragma unroll
       for (int u = 0; u < kTok; ++u) {
-        if (fk[u] < 0) break;
-        if (fk[u] != cur) {
+        if (fk[u] >= 0 && fk[u] != cur) {
           const float* ks = p.seg.kscales + (unit * p.seg.cap + fk[u]) * D;
 #pragma unroll
           for (int k = 0; k < CPL; ++k) {
@@ -211,13 +253,67 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
           }
           cur = fk[u];
         }
+#pragma unroll
+        for (int j = 0; j < kMaxGqa; ++j) {
+          float a = 0.f;
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) a = fmaf(qv[j][k], (float)kc[u][k], a);
+          part[u][j] = a;
+        }
+      }
+      // sums over the warp, four heads of every token per exchange set
+      // (eight heads: two sets)
+#pragma unroll
+      for (int j0 = 0; j0 < kMaxGqa; j0 += 4) {
+        if (j0 >= g) break;
+        float v[4 * kTok];
+#pragma unroll
+        for (int u = 0; u < kTok; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) v[4 * u + j] = part[u][j0 + j];
+        warp_sum_n<4 * kTok>(v, lane);
+#pragma unroll
+        for (int u = 0; u < kTok; ++u)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) part[u][j0 + j] = v[4 * u + j];
+      }
+      // move the reference max only when some score passes it by kSlack (the
+      // sums are the same in every lane, so the branch is the warp's)
+      bool up = false;
+#pragma unroll
+      for (int u = 0; u < kTok; ++u)
+#pragma unroll
+        for (int j = 0; j < kMaxGqa; ++j)
+          if (j < g && fk[u] >= 0) up |= part[u][j] > s.m[j] + kSlack;
+      if (up) {
+#pragma unroll
+        for (int j = 0; j < kMaxGqa; ++j) {
+          if (j >= g) break;
+          float mx = s.m[j];
+#pragma unroll
+          for (int u = 0; u < kTok; ++u)
+            if (fk[u] >= 0) mx = fmaxf(mx, part[u][j]);
+          const float corr = s.m[j] == -INFINITY ? 0.f : exp2f(s.m[j] - mx);
+          s.m[j] = mx;
+          s.l[j] *= corr;
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) s.o[j][k] *= corr;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kTok; ++u) {
+        if (fk[u] < 0) break;
         const float iv = __frcp_rn(fmaxf(vsr[u], p.eps));
 #pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-          kv[k] = (float)kc[u][k];
-          vv[k] = (float)vc[u][k] * iv;
+        for (int k = 0; k < CPL; ++k) vv[k] = (float)vc[u][k] * iv;
+#pragma unroll
+        for (int j = 0; j < kMaxGqa; ++j) {
+          if (j >= g) break;
+          const float pw = exp2f(part[u][j] - s.m[j]);
+          s.l[j] += pw;
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) s.o[j][k] = fmaf(pw, vv[k], s.o[j][k]);
         }
-        simt_token<CPL>(s, qv, kv, vv, g);
       }
     }
   } else {
