@@ -97,28 +97,6 @@ __device__ __forceinline__ constexpr int lane_chan(int lane, int k) {
   return SEG ? CPL * lane + k : lane + 32 * k;
 }
 
-// Codes of channels CPL lane .. CPL lane + CPL - 1 of a token row.
-template <int BITS, int CPL>
-__device__ __forceinline__ void row_codes(const uint8_t* row, int lane, int D, int (&code)[CPL]) {
-  constexpr int kBits = CPL * BITS;  // bits of the lane's slice: 2 .. 64, aligned to its size
-  const int c0 = CPL * lane;
-  if (c0 >= D) {
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) code[k] = 0;
-    return;
-  }
-  uint64_t v;
-  const uint8_t* src = row + c0 * BITS / 8;
-  if constexpr (kBits < 8) v = (uint64_t)(*src >> ((c0 * BITS) & 7));  // inside one byte
-  else if constexpr (kBits == 8) v = *src;
-  else if constexpr (kBits == 16) v = *reinterpret_cast<const uint16_t*>(src);
-  else if constexpr (kBits == 32) v = *reinterpret_cast<const uint32_t*>(src);
-  else v = *reinterpret_cast<const uint64_t*>(src);
-  constexpr int kBias = BITS == 2 ? 2 : BITS == 4 ? 8 : 128;
-#pragma unroll
-  for (int k = 0; k < CPL; ++k) code[k] = (int)((v >> (BITS * k)) & ((1u << BITS) - 1u)) - kBias;
-}
-
 // Sums over the 32 lanes of N values (N = 4 or 8), every lane ending with all
 // N sums.  The first log2(N) exchange steps halve the set each time, a lane
 // keeping the half its lane bit selects, so each exchange carries half as many
@@ -153,6 +131,32 @@ __device__ __forceinline__ void warp_sum_n(float (&v)[N], int lane) {
   for (int i = 0; i < N; ++i)
     v[i] = N == 8 ? __shfl_sync(0xffffffffu, x, ((i >> 2) & 1) * 16 + ((i >> 1) & 1) * 8 + (i & 1) * 4)
                   : __shfl_sync(0xffffffffu, x, ((i >> 1) & 1) * 16 + (i & 1) * 8);
+}
+
+// Codes of channels CPL lane .. CPL lane + CPL - 1 of a token row, as floats.
+// A field u (code + bias) OR-ed into the mantissa of 2^23 is the float 2^23 + u
+// exactly, and subtracting 2^23 + bias leaves the code: a logic op and an add
+// instead of an integer-to-float conversion.
+template <int BITS, int CPL>
+__device__ __forceinline__ void row_codes_f(const uint8_t* row, int lane, int D, float (&code)[CPL]) {
+  constexpr int kBits = CPL * BITS;
+  const int c0 = CPL * lane;
+  if (c0 >= D) {
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) code[k] = 0.f;
+    return;
+  }
+  uint64_t v;
+  const uint8_t* src = row + c0 * BITS / 8;
+  if constexpr (kBits < 8) v = (uint64_t)(*src >> ((c0 * BITS) & 7));
+  else if constexpr (kBits == 8) v = *src;
+  else if constexpr (kBits == 16) v = *reinterpret_cast<const uint16_t*>(src);
+  else if constexpr (kBits == 32) v = *reinterpret_cast<const uint32_t*>(src);
+  else v = *reinterpret_cast<const uint64_t*>(src);
+  constexpr float kOff = 8388608.f + (BITS == 2 ? 2.f : BITS == 4 ? 8.f : 128.f);
+#pragma unroll
+  for (int k = 0; k < CPL; ++k)
+    code[k] = __uint_as_float(0x4B000000u | (uint32_t)((v >> (BITS * k)) & ((1u << BITS) - 1u))) - kOff;
 }
 
 // Whole split item on CUDA cores; writes the partial of slot ``slot``.
@@ -224,8 +228,8 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
     constexpr int kTok = CPL <= 4 ? 2 : 1;
     constexpr float kSlack = 8.f;
     for (int64_t t0 = pg0 + warp; t0 < pg1; t0 += kTok * kSimtWarps) {
-      int fk[kTok], kc[kTok][CPL], vc[kTok][CPL];
-      float vsr[kTok];
+      int fk[kTok];
+      float kc[kTok][CPL], vc[kTok][CPL], vsr[kTok];
 #pragma unroll
       for (int u = 0; u < kTok; ++u) {
         const int64_t t = t0 + u * kSimtWarps;
@@ -235,8 +239,8 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
         const uint8_t* vr = p.seg.vcodes + row * p.seg.row_bytes;
         fk[u] = ok ? first[t] : -1;
         vsr[u] = p.seg.vscales[row];
-        row_codes<BITS, CPL>(kr, lane, D, kc[u]);
-        row_codes<BITS, CPL>(vr, lane, D, vc[u]);
+        row_codes_f<BITS, CPL>(kr, lane, D, kc[u]);
+        row_codes_f<BITS, CPL>(vr, lane, D, vc[u]);
       }
       // this lane's share of every (token, head) dot product
       float part[kTok][kMaxGqa];
@@ -257,7 +261,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
         for (int j = 0; j < kMaxGqa; ++j) {
           float a = 0.f;
 #pragma unroll
-          for (int k = 0; k < CPL; ++k) a = fmaf(qv[j][k], (float)kc[u][k], a);
+          for (int k = 0; k < CPL; ++k) a = fmaf(qv[j][k], kc[u][k], a);
           part[u][j] = a;
         }
       }
@@ -305,7 +309,7 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
         if (fk[u] < 0) break;
         const float iv = __frcp_rn(fmaxf(vsr[u], p.eps));
 #pragma unroll
-        for (int k = 0; k < CPL; ++k) vv[k] = (float)vc[u][k] * iv;
+        for (int k = 0; k < CPL; ++k) vv[k] = vc[u][k] * iv;
 #pragma unroll
         for (int j = 0; j < kMaxGqa; ++j) {
           if (j >= g) break;
