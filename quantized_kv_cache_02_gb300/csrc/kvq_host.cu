@@ -248,7 +248,14 @@ void plan_splits(const kvq_cache* c, int s0, int n, int requested, int* chunk, i
   if (requested > 0) {
     ch = requested;
   } else {
-    const int64_t target = (int64_t)c->n_sm * 8;
+    // about 6 work items per SM for group pages, 8 for a segmented cache's
+    // one-token pages (CUDA-core kernel).  Measured on the 32 x 8 x 8192
+    // decode layer (CUDA events, split + combine): 6 per SM makes the chunk
+    // 72 pages (three columns of 72 and a half column of 36, so the last wave
+    // is short) and the split 78.1 -> 74.8 us; 8 per SM (chunk 56) and chunks
+    // of 64 or 68 (a nearly full last column) are slower.  The segmented
+    // decode is 2.8 % faster at 8 per SM.
+    const int64_t target = (int64_t)c->n_sm * (c->segmented ? 8 : 6);
     ch = std::max<int64_t>(c->min_chunk_pages, (total_pages + target - 1) / target);
   }
   ch = std::max<int64_t>(ch, (pmax + c->max_splits - 2) / std::max(1, c->max_splits - 1));
