@@ -26,6 +26,11 @@ bool decode_mma_supported(const DecodeParams& p) {
          decode_mma_smem_bytes(p) <= kMaxSmem;
 }
 
+int decode_mma_resident_per_sm(const DecodeParams& p) {
+  if (!decode_mma_supported(p)) return 0;
+  return p.bits == 2 ? resident_mma_bits2(p) : p.bits == 4 ? resident_mma_bits4(p) : resident_mma_bits8(p);
+}
+
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported) {
   *supported = decode_mma_supported(p);
   if (!*supported) return cudaSuccess;

@@ -29,6 +29,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <type_traits>
+
 #include "kvq_simt.cuh"
 
 namespace kvq {
@@ -1118,9 +1120,10 @@ size_t smem_for(const DecodeParams& p) {
   return 128 * ((kMmaWarps * slots * 8 + 127) / 128) + scratch + pages;
 }
 
+// Allows the split kernel instance ``smem`` bytes of dynamic shared memory
+// on the current device (once per device and size).
 template <int D, int BITS, int GP, int MODE>
-cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
-  const size_t smem = smem_for<D>(p);
+cudaError_t configure_t(size_t smem) {
   int dev = 0;
   cudaGetDevice(&dev);
   static size_t configured[64] = {};
@@ -1131,6 +1134,40 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     configured[dev] = smem;
   }
+  return cudaSuccess;
+}
+
+// CTAs of the split kernel one SM holds at once for these parameters (0 on error).
+template <int D, int BITS, int GP, int MODE>
+int resident_t(const DecodeParams& p) {
+  const size_t smem = smem_for<D>(p);
+  int per_sm = 0;
+  if (configure_t<D, BITS, GP, MODE>(smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BITS, GP, MODE>, kMmaThreads,
+                                                    smem) != cudaSuccess)
+    return 0;
+  return per_sm;
+}
+
+template <int D, int BITS>
+int resident_g(const DecodeParams& p) {
+  auto pick = [&](auto gp) {
+    constexpr int GP = decltype(gp)::value;
+    if (p.G != 32) return resident_t<D, BITS, GP, kStaged>(p);
+    return p.map.table ? resident_t<D, BITS, GP, kPaged32>(p) : resident_t<D, BITS, GP, kFlat32>(p);
+  };
+  switch (gqa_pad(p.g)) {
+    case 2: return pick(std::integral_constant<int, 2>{});
+    case 4: return pick(std::integral_constant<int, 4>{});
+    default: return pick(std::integral_constant<int, 8>{});
+  }
+}
+
+template <int D, int BITS, int GP, int MODE>
+cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
+  const size_t smem = smem_for<D>(p);
+  const cudaError_t e = configure_t<D, BITS, GP, MODE>(smem);
+  if (e != cudaSuccess) return e;
   const dim3 grid((p.grid_splits + 1) * p.n_seqs * p.Hkv);
   return launch_pdl(decode_mma_kernel<D, BITS, GP, MODE>, grid, dim3(kMmaThreads), smem, s, p,
                     mma_slots(unit_bytes(p), p.g));

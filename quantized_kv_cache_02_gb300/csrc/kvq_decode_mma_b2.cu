@@ -5,6 +5,10 @@
 
 namespace kvq {
 
+int resident_mma_bits2(const DecodeParams& p) {
+  return p.D == 64 ? resident_g<64, 2>(p) : resident_g<128, 2>(p);
+}
+
 cudaError_t launch_mma_bits2(const DecodeParams& p, cudaStream_t s) {
   return p.D == 64 ? launch_g<64, 2>(p, s) : launch_g<128, 2>(p, s);
 }

@@ -5,6 +5,10 @@
 
 namespace kvq {
 
+int resident_mma_bits4(const DecodeParams& p) {
+  return p.D == 64 ? resident_g<64, 4>(p) : resident_g<128, 4>(p);
+}
+
 cudaError_t launch_mma_bits4(const DecodeParams& p, cudaStream_t s) {
   return p.D == 64 ? launch_g<64, 4>(p, s) : launch_g<128, 4>(p, s);
 }

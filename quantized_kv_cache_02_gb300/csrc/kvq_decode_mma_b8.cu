@@ -5,6 +5,10 @@
 
 namespace kvq {
 
+int resident_mma_bits8(const DecodeParams& p) {
+  return p.D == 64 ? resident_g<64, 8>(p) : resident_g<128, 8>(p);
+}
+
 cudaError_t launch_mma_bits8(const DecodeParams& p, cudaStream_t s) {
   return p.D == 64 ? launch_g<64, 8>(p, s) : launch_g<128, 8>(p, s);
 }

@@ -236,8 +236,9 @@ void fill_counters(const kvq_cache* c, int seq_begin, int n, SeqCounters* out) {
   }
 }
 
-// Split plan for the decode launch over sequences [s0, s0 + n).
-void plan_splits(const kvq_cache* c, int s0, int n, int requested, int* chunk, int* grid_splits) {
+// Split plan for the decode launch over sequences [s0, s0 + n).  ``slots``:
+// the CTAs of the split kernel the GPU holds at once (0 if unknown).
+void plan_splits(const kvq_cache* c, int s0, int n, int requested, int slots, int* chunk, int* grid_splits) {
   int64_t total_pages = 0, pmax = 0;
   for (int i = s0; i < s0 + n; ++i) {
     const int64_t P = c->quantized[i] / c->cfg.group;
@@ -258,11 +259,28 @@ void plan_splits(const kvq_cache* c, int s0, int n, int requested, int* chunk, i
     const int64_t target = (int64_t)c->n_sm * (c->segmented ? 8 : 6);
     ch = std::max<int64_t>(c->min_chunk_pages, (total_pages + target - 1) / target);
   }
+  // Few units (at least 4 split columns per wave): choose the columns so that
+  // the launch, its window items included, fills whole waves of the resident
+  // CTAs -- half the waves the plan above would take, at least one, since
+  // equal items need no later waves to even out.  A launch only a few CTAs
+  // past a wave boundary takes about a whole CTA longer: on the long-video
+  // decode (8 units of 3373 pages of G = 128, 456 resident CTAs) 59 columns
+  // (472 CTAs) took 162 us, 113 columns (912, two waves) 116 us and 56 (456,
+  // one wave) 114 us, against 121 us for the 106 columns above.
+  const int64_t units = (int64_t)n * c->cfg.n_kv_heads;
+  if (requested <= 0 && slots > 0 && units * 4 <= slots && pmax > 0) {
+    const int64_t base_ctas = units * ((pmax + ch - 1) / ch + 1);
+    const int64_t waves = std::max<int64_t>(1, base_ctas / (2 * (int64_t)slots));
+    const int64_t cols = waves * slots / units - 1;
+    if (cols >= 1) ch = std::max<int64_t>(c->min_chunk_pages, (pmax + cols - 1) / cols);
+  }
   ch = std::max<int64_t>(ch, (pmax + c->max_splits - 2) / std::max(1, c->max_splits - 1));
   ch = std::max<int64_t>(ch, 1);
   // whole page groups for each of the tensor-core kernel's 4 warps (8 pages =
-  // 4 warps x 2 pages at g = 4): every warp of a CTA gets the same work
-  if (requested <= 0 && ch > 8) ch = (ch + 7) / 8 * 8;
+  // 4 warps x 2 pages at g = 4): every warp of a CTA gets the same work.  A
+  // larger G is split into 32-token units, four warps' worth per page or more,
+  // so any chunk keeps the warps even there.
+  if (requested <= 0 && ch > 8 && c->cfg.group == 32) ch = (ch + 7) / 8 * 8;
   *chunk = (int)ch;
   *grid_splits = (int)((pmax + ch - 1) / ch);
 }
@@ -687,6 +705,13 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opts->split_start), s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   }
+  // resident CTAs of the tensor-core split kernel, for the planner
+  int mma_slots = 0;
+  if (use_mma && !use_tc) {
+    kvq::DecodeParams qp;
+    base_decode_params(c, &qp);
+    mma_slots = kvq::decode_mma_resident_per_sm(qp) * c->n_sm;
+  }
   struct Batch {
     int s0, n, chunk, grid;
   };
@@ -695,7 +720,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     Batch bt;
     bt.s0 = s0;
     bt.n = std::min(kvq::kMaxSeqsPerLaunch, c->cfg.batch - s0);
-    plan_splits(c, bt.s0, bt.n, opts ? opts->chunk_pages : 0, &bt.chunk, &bt.grid);
+    plan_splits(c, bt.s0, bt.n, opts ? opts->chunk_pages : 0, mma_slots, &bt.chunk, &bt.grid);
     kvq::DecodeParams p;
     base_decode_params(c, &p);
     p.q = q;
@@ -843,7 +868,7 @@ kvq_status kvq_decode_attention_noalloc(kvq_cache* c, const void* q, float* out,
                 "decode needs %zu floats of split scratch, more than the %zu floats (8 MiB) the library reserves",
                 per_slot * min_slots, kNoAllocScratchFloats);
   int chunk = 1, grid = 0;
-  plan_splits(c, 0, B, 0, &chunk, &grid);
+  plan_splits(c, 0, B, 0, 0, &chunk, &grid);
   const int64_t fit = (int64_t)(kNoAllocScratchFloats / per_slot);  // >= min_slots
   if (grid + 1 > fit) {
     chunk = (int)((pmax + (fit - 1) - 1) / (fit - 1));

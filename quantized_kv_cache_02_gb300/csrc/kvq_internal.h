@@ -255,6 +255,12 @@ cudaError_t configure_append(int dtype, int bits, size_t smem_bytes);
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported);
 // the split kernel for one code width (one translation unit each)
+// CTAs of the tensor-core split kernel one SM holds at once for p (0: not
+// supported or unknown).
+int decode_mma_resident_per_sm(const DecodeParams& p);
+int resident_mma_bits2(const DecodeParams& p);
+int resident_mma_bits4(const DecodeParams& p);
+int resident_mma_bits8(const DecodeParams& p);
 cudaError_t launch_mma_bits2(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_mma_bits4(const DecodeParams& p, cudaStream_t s);
 cudaError_t launch_mma_bits8(const DecodeParams& p, cudaStream_t s);
