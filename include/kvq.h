@@ -124,7 +124,14 @@ typedef struct kvq_decode_opts {
                           tensor-core kernel (bf16, head_dim 128, 4-bit codes,
                           G a multiple of 32); KVQ_EUNSUPPORTED if not
                           applicable */
-  int32_t chunk_pages; /* 0 = automatic; else quantized groups per split item */
+  int32_t chunk_pages; /* 0 = automatic: about 6 split items per SM (8 on a
+                          segmented cache), rounded to whole 8-page groups at
+                          G = 32; with few (sequence, KV head) units on the
+                          tensor-core kernel, as many columns as fill whole
+                          waves of its resident CTAs.  Else quantized groups
+                          per split item.  Results agree for any choice within
+                          the attention tolerance (the summation order of the
+                          splits differs). */
   void* split_start;   /* optional cudaEvent_t recorded just before the split kernel */
   void* split_stop;    /* optional cudaEvent_t recorded just after it */
 } kvq_decode_opts;
