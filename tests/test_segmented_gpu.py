@@ -186,3 +186,24 @@ def test_segment_schedule_matches_oracle(kvq, torch, dtype, qmax, D):
     np.testing.assert_array_equal(k_out.cpu().numpy()[0].view(np.uint32), K[0].view(np.uint32))
     np.testing.assert_array_equal(v_out.cpu().numpy()[0].view(np.uint32), V[0].view(np.uint32))
     assert pair.cache.device_status() == 0
+
+
+@pytest.mark.parametrize("dtype,D,Hkv,Hq", [("bf16", 128, 2, 16), ("bf16", 128, 2, 12), ("bf16", 256, 2, 8),
+                                            ("fp32", 16, 2, 2), ("bf16", 256, 1, 6)])
+def test_segment_head_groups(kvq, torch, dtype, D, Hkv, Hq):
+    """The segmented decode sums each pass's (token, head) dot products over
+    the warp in sets of four heads: eight and six query heads per KV head take
+    two sets (the second partly padding), one head pads a single set, and
+    head_dim 256 runs one token per pass (sets of four values)."""
+    R = 32
+    spec = gen.InputSpec(seed=43, n_kv_heads=Hkv, n_q_heads=Hq, head_dim=D, bf16=dtype == "bf16", spikes=True)
+    pair = SegPair(kvq, torch, Hkv, Hq, D, R, qmax=7, capacity=400, dtype=dtype)
+    t = 0
+    for n in [90, 1, 1, 40, 1, 3, 1, 60]:
+        k, v = spec.kv_block(0, [0], t, n)
+        t += n
+        pair.append(k[0], v[0])
+        pair.attend(spec.q_block(0, [0], t)[0])
+    for h in range(Hkv):
+        pair.check_unit(h)
+    assert pair.cache.device_status() == 0
