@@ -80,8 +80,11 @@ struct PairB {
 template <typename T>
 using PairOf = typename std::conditional<sizeof(T) == 4, PairF, PairB>::type;
 
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+template <typename T>
+__device__ __forceinline__ float to_f32(T x) {
+  if constexpr (sizeof(T) == 4) return x;
+  else return __bfloat162float(x);
+}
 
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)

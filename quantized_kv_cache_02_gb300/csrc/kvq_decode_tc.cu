@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   constexpr int D = kTcD;
   using TS = TcShape<GP>;
   constexpr int NS = TS::NS, CPG = TS::CPG;
-  extern __shared__ __align__(1024) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t tc_smem[];
   pdl_wait();
   pdl_release();
   const int n_units = p.n_seqs * p.Hkv;
@@ -227,15 +227,15 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
     st.C[0] = st.C[1] = st.C[2] = st.C[3] = 0.f;
     st.m0 = st.m1 = -INFINITY;
     st.l0 = st.l1 = 0.f;
-    if (warp < 4) window_rows<D, GP>(p, i, h, lane, warp, lane >> 2, lane & 3, smem, st);
+    if (warp < 4) window_rows<D, GP>(p, i, h, lane, warp, lane >> 2, lane & 3, tc_smem, st);
     __syncthreads();
-    write_partial<D, GP>(p, unit, slot, warp, lane >> 2, lane & 3, st, smem);
+    write_partial<D, GP>(p, unit, slot, warp, lane >> 2, lane & 3, st, tc_smem);
     return;
   }
 
   // ---- shared memory ----------------------------------------------------------
-  uint8_t* ring = smem;
-  uint8_t* bq = smem + TS::kBOff;          // B_Q, two buffers of NS rows
+  uint8_t* ring = tc_smem;
+  uint8_t* bq = tc_smem + TS::kBOff;          // B_Q, two buffers of NS rows
   uint8_t* bpm = bq + 2 * TS::kBq;         // B_P: 16 rows
   float* qs = reinterpret_cast<float*>(bpm + 16 * kTcBRow);
   float* red = qs + GP * D;                // [0, 32): maxima; [32, 64): l; [64, 96): Value bias sums
