@@ -40,7 +40,7 @@ def close(got, ref, what):
     assert excess.max() <= 0, f"{what}: |d| {np.abs(got - ref).max():.3e}"
 
 
-def run_case(kvq, torch, lens, Hkv, Hq, D, R, G, qmax, dtype, kernels, seed, check_heads=(0,), steps=2):
+def run_case(kvq, torch, lens, Hkv, Hq, D, R, G, qmax, dtype, kernels, seed, check_heads=(0,), steps=2, chunks=(0,)):
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     spec = gen.InputSpec(seed=seed, n_kv_heads=Hkv, n_q_heads=Hq, head_dim=D, bf16=dtype == "bf16")
     cache = kvq.KVQCache(len(lens), Hkv, Hq, D, R, G, qmax, [n + steps + 1 for n in lens], dtype=dtype)
@@ -59,10 +59,12 @@ def run_case(kvq, torch, lens, Hkv, Hq, D, R, G, qmax, dtype, kernels, seed, che
         for b in range(B):
             seqs[b].append(k[b], v[b])
     q = spec.q_block(0, range(B), steps)
+    refs = [seq.attend(q[b]) for b, seq in enumerate(seqs)]
     for kernel in kernels:
-        out = cache.decode_attention(dev(q), kernel=kernel).cpu().numpy()
-        for b, seq in enumerate(seqs):
-            close(out[b], seq.attend(q[b]), f"kernel {kernel} seq {b} (T={seq.total})")
+        for chunk in chunks:
+            out = cache.decode_attention(dev(q), kernel=kernel, chunk_pages=chunk).cpu().numpy()
+            for b, seq in enumerate(seqs):
+                close(out[b], refs[b], f"kernel {kernel} chunk {chunk} seq {b} (T={seq.total})")
     for b in {0, B - 1}:
         for h in check_heads:
             got = cache.export_unit(b, h)
@@ -97,3 +99,11 @@ def test_gqa_on_tensor_cores(kvq, torch, Hq):
 @pytest.mark.parametrize("G", [64, 256])
 def test_large_groups_staged(kvq, torch, G):
     run_case(kvq, torch, [G * 5 + 129, G + 128, 100], 4, 16, 64, 128, G, 7, "bf16", kernels=(1, 2), seed=65)
+
+
+@pytest.mark.parametrize("G", [32, 128])
+def test_odd_chunks_tensor_cores(kvq, torch, G):
+    """Split items of odd page counts on the mma.sync kernel (as the whole-wave
+    plan picks for long staged units): each warp's run ends on a one-page group."""
+    run_case(kvq, torch, [G * 9 + 50, G * 4 + 3, 130], 4, 16, 128, 128, G, 7, "bf16", kernels=(2,), seed=66,
+             chunks=(0, 1, 3, 5, 7))
