@@ -172,6 +172,30 @@ def test_restore_divides_by_scale():
     assert O.restore(np.int8([-3]), np.float32([0.0]), eps=1e-8)[0] == np.float32(-3) / np.float32(1e-8)
 
 
+def test_restore_is_correctly_rounded_division():
+    # "54. KV Cache Quantization Strategies", Step 4 ``restore``: codes in fp32
+    # divided by scale.clamp_min(eps).  One IEEE division rounds once, so every
+    # result lies within half an ulp of the exact quotient code / max(scale, eps)
+    # taken in fp64 (exact for these operands up to fp64 rounding).
+    rng = np.random.default_rng(11)
+    n = 50000
+    codes = rng.integers(-127, 128, n).astype(np.int8)
+    scales = np.exp(rng.uniform(np.log(1e-3), np.log(1e9), n)).astype(np.float32)
+    scales[:64] = np.float32(3e-9)          # below eps: the clamp takes over
+    scales[64:96] = np.float32(0.0)
+    got = O.restore(codes, scales).astype(np.float64)
+    eps32 = np.float64(np.float32(1e-8))
+    exact = codes.astype(np.float64) / np.maximum(scales.astype(np.float64), eps32)
+    ulp = np.spacing(np.abs(got).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(got - exact) <= 0.5 * ulp)
+    # the sample separates a true division from a reciprocal product: the
+    # product 1/s * code rounds twice and misses the quotient on many pairs
+    recip = (np.float32(1) / np.maximum(scales, np.float32(1e-8))) * codes.astype(np.float32)
+    assert np.count_nonzero(recip != got.astype(np.float32)) > n // 50
+    # the clamp: a scale below eps divides by eps
+    assert got[0] == np.float64(np.float32(codes[0]) / np.float32(1e-8))
+
+
 # --------------------------------------------------------------------------
 # The datawhale page's eight mechanism checks, page rule (group=None)
 # --------------------------------------------------------------------------
@@ -226,6 +250,25 @@ def test_page_restore_and_budget():
     assert math.isfinite(res["key_mse"]) and math.isfinite(res["value_mse"])
     assert res["packed_quantized_bytes"] < res["raw_bytes"]
     assert res["packed_quantized_bytes"] < res["container_quantized_bytes"]
+
+
+@pytest.mark.parametrize("shape,raw_el,expect", [
+    # [1, 2, 7, 8] fp32: 112 Key + 112 Value scalars; Key scales [1, 2, 1, 8] = 16
+    # fp32 (64 B), Value scales [1, 2, 7, 1] = 14 fp32 (56 B).
+    # raw 224 * 4 = 896; int8 container 224 + 120 = 344; packed (224 + 1) // 2 + 120 = 232
+    ((1, 2, 7, 8), 4, (896, 344, 232)),
+    # [2, 1, 3, 5] bf16: 30 + 30 scalars; Key scales 2 * 5 = 10 fp32 (40 B),
+    # Value scales 2 * 3 = 6 fp32 (24 B).  raw 60 * 2 = 120; container 60 + 64 = 124;
+    # packed 61 // 2 + 64 = 94
+    ((2, 1, 3, 5), 2, (120, 124, 94)),
+])
+def test_compare_byte_ledger_hand_values(shape, raw_el, expect):
+    # "54. KV Cache Quantization Strategies", Step 4 ``compare``: raw bytes are
+    # numel * element_size of Key and Value; the int8 container adds one byte a
+    # code plus the fp32 scales; packed 4-bit bytes are (nK + nV + 1) // 2 plus
+    # the same fp32 scale bytes.  Values worked out by hand above.
+    res = O.compare_bytes(_r(*shape), _r(*shape, seed=1), raw_element_bytes=raw_el)
+    assert (res["raw_bytes"], res["container_quantized_bytes"], res["packed_quantized_bytes"]) == expect
 
 
 def test_page_rule_rejects_bad_arguments():
