@@ -122,8 +122,12 @@ typedef struct kvq_decode_opts {
                           shape); 2 = tensor-core kernel on mma.sync (bf16,
                           head_dim 64/128, G a multiple of 32); 3 = tcgen05
                           tensor-core kernel (bf16, head_dim 128, 4-bit codes,
-                          G a multiple of 32); KVQ_EUNSUPPORTED if not
-                          applicable */
+                          G a multiple of 32; it handles the input range per
+                          block of 128 tokens: groups with a Key scale below
+                          the bound of kvq_decode_attention enter with signed
+                          codes and q / sK scaled by a power of two, blocks
+                          with a Value absmax above 16 are summed in fp32);
+                          KVQ_EUNSUPPORTED if not applicable */
   int32_t chunk_pages; /* 0 = automatic: about 6 split items per SM (8 on a
                           segmented cache), rounded to whole 8-page groups at
                           G = 32; with few (sequence, KV head) units on the
@@ -251,7 +255,21 @@ kvq_status kvq_append(kvq_cache* cache, const void* new_k, const void* new_v, in
 
 /* Decode attention for every sequence: q device [batch][n_q_heads][head_dim] of
  * the cache dtype; out device float [batch][n_q_heads][head_dim].  A sequence
- * with no tokens yields zeros.  Uses the arena's split scratch region. */
+ * with no tokens yields zeros.  Uses the arena's split scratch region.
+ *
+ * Input range.  Any finite Key, Value and query values are accepted; scales
+ * below eps (absmax > qmax / eps) restore as code / eps, as the page's restore
+ * does.  The tensor-core kernels carry q / sK and p / sV as f16 operands, so
+ * the cache tracks, per (sequence, KV head), the largest Key and Value absmax
+ * it has flushed (reset when a sequence starts from empty).  A split item
+ * runs on the tensor cores only while those bound every group of its unit:
+ * |q| * qk_scale * (Key absmax) / qmax <= 2^9 (2^14 at 2-bit codes, x 1/16
+ * below the f16 limit) -- i.e. every Key scale >= 2^(e + 1 - 9) with e the
+ * binary exponent of the largest |q| / sqrt(head_dim) * log2(e) -- and every
+ * Value absmax <= 16.  Other items run the CUDA-core path inside the same
+ * launch (fp32, IEEE division with the eps clamp), so results stay within the
+ * attention tolerance for any range, at CUDA-core speed for those units.
+ * The residual window is attended from its bf16 rows on either path. */
 kvq_status kvq_decode_attention(kvq_cache* cache, const void* q, float* out, void* stream);
 
 /* Same as kvq_decode_attention with explicit options (kernel choice, split

@@ -300,11 +300,16 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
       for (int e = 0; e < kVec; ++e) part[r0 * D + col + e] = amax[e];
     }
     __syncthreads();
+    float kmx = 0.f;
     for (int c = threadIdx.x; c < D; c += kAppendThreads) {
       float a = 0.f;
       for (int r = 0; r < rows_per_pass; ++r) a = fmaxf(a, part[r * D + c]);
       sK[c] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+      kmx = fmaxf(kmx, a);
     }
+    // the unit's largest flushed Key absmax (the decode's range guard)
+    for (int o = 16; o > 0; o >>= 1) kmx = fmaxf(kmx, __shfl_xor_sync(0xffffffffu, kmx, o));
+    if ((threadIdx.x & 31) == 0 && kmx > 0.f && p.range) atomicMax(p.range + 2 * unit, __float_as_uint(kmx));
     __syncthreads();
   }
   {
@@ -381,8 +386,14 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     }
     __syncthreads();
     // one division per token, spread over the CTA (not inside the row loop)
-    for (int t = threadIdx.x; t < G; t += kAppendThreads)
-      sV[t] = __fdiv_rn(qmax, fmaxf(shuffle_rows ? sV[t] : __uint_as_float(rmax[t]), p.eps));
+    float vmx = 0.f;
+    for (int t = threadIdx.x; t < G; t += kAppendThreads) {
+      const float a = shuffle_rows ? sV[t] : __uint_as_float(rmax[t]);
+      sV[t] = __fdiv_rn(qmax, fmaxf(a, p.eps));
+      vmx = fmaxf(vmx, a);
+    }
+    for (int o = 16; o > 0; o >>= 1) vmx = fmaxf(vmx, __shfl_xor_sync(0xffffffffu, vmx, o));
+    if ((threadIdx.x & 31) == 0 && vmx > 0.f && p.range) atomicMax(p.range + 2 * unit + 1, __float_as_uint(vmx));
     __syncthreads();
   }
   {

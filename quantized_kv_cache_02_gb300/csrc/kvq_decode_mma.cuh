@@ -170,6 +170,15 @@ __device__ __forceinline__ void piece_regs(uint32_t piece, uint32_t (&r)[4]) {
   for (int j = 0; j < 4; ++j) r[j] = hsub2(r[j], 0x00020002u << (2 * j));
 }
 
+// The same for 4-bit registers (u = code + 8; registers 1 and 3 carry x16)
+// and 8-bit ones (u = code + 128): afterwards they hold code * 2^-24 (x16).
+__device__ __forceinline__ void unbias_nibbles(uint32_t (&r)[4]) {
+  r[0] = hsub2(r[0], 0x00080008u);
+  r[1] = hsub2(r[1], 0x00800080u);
+  r[2] = hsub2(r[2], 0x00080008u);
+  r[3] = hsub2(r[3], 0x00800080u);
+}
+
 // 8-bit: word of four bytes -> r[0] = (byte 0, byte 2), r[1] = (byte 1, byte 3).
 __device__ __forceinline__ void byte_regs(uint32_t w, uint32_t (&r)[2]) {
   r[0] = w & 0x00FF00FFu;
@@ -235,6 +244,29 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[N]) {
       w[2 * i + 1] = v.y;
     }
   }
+}
+
+// ---- range of the f16 operands ------------------------------------------
+// The pages hold any finite scale, so q / sK and p / sV can leave the f16
+// range (65504), the fp32 bias sums of large q / sK lose the scores'
+// precision, one f16 p / sV (11 bits) keeps the output error near 2^-12 of
+// the p-weighted |v| only while |v| is small, and a scale can drop below eps,
+// where the page's restore divides by eps.  A tensor-core item therefore
+// runs only when the unit's flushed maxima bound every group: all Key scales
+// at least kthr (|q / sK| <= 2^9, 2^14 at 2 bits where the codes enter
+// signed and only the f16 range limits) and every Value absmax at most
+// kVWideAbs.  Other items take the CUDA-core path (fp32, IEEE division with
+// the eps clamp) inside the same kernel.
+constexpr float kVWideAbs = 16.f;
+constexpr int kMaxRangeShift = 100;
+
+// Binary exponent of a positive finite float (floor(log2 x)); 0 gives -127.
+__device__ __forceinline__ int float_exp2i(float x) { return (int)((__float_as_uint(x) >> 23) & 0xFFu) - 127; }
+// 2^-e for 0 <= e <= 126, exactly.
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+// 2^e for -126 <= e <= 127 (0 below, infinity above).
+__device__ __forceinline__ float pow2i(int e) {
+  return e < -126 ? 0.f : e > 127 ? INFINITY : __uint_as_float((uint32_t)(e + 127) << 23);
 }
 
 // GP = query heads per KV head rounded up to 2, 4 or 8.  The MMA's 8 columns
@@ -860,7 +892,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   float* scratch = reinterpret_cast<float*>(smem + 128 * ((kMmaWarps * slots * 8 + 127) / 128));
   float* my_rsc = scratch + warp * S::PB * D;
   float4* q4 = reinterpret_cast<float4*>(scratch + kMmaWarps * S::PB * D);  // GP * D floats
-  uint8_t* buf = reinterpret_cast<uint8_t*>(scratch + kMmaWarps * S::PB * D + GP * D);
+  uint8_t* buf = reinterpret_cast<uint8_t*>(scratch + kMmaWarps * S::PB * D + GP * D + 32);
   uint8_t* my_buf = buf + (size_t)warp * slots * page_bytes;
   const uint32_t my_bar = smem_addr(bars + warp * slots);
 
@@ -879,14 +911,37 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   // value stays finite), pre-scaled, in shared memory: channel c of head n goes
   // to float4 ((i * GP + n) * 4 + tig) with tig = c / (D/4), i = (c % (D/4)) / 4,
   // so the lanes that read together hit distinct banks
+  float qa = 0.f;
   for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) {
     const int n = idx / D, c = idx - n * D;
     const __nv_bfloat16* qrow =
         reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D;
     const int tg = c / S::kChan, i4 = (c - tg * S::kChan) >> 2;
-    reinterpret_cast<float*>(q4)[((i4 * GP + n) * 4 + tg) * 4 + (c & 3)] = __bfloat162float(qrow[c]) * p.qk_scale;
+    const float qv = __bfloat162float(qrow[c]) * p.qk_scale;
+    qa = fmaxf(qa, fabsf(qv));
+    reinterpret_cast<float*>(q4)[((i4 * GP + n) * 4 + tg) * 4 + (c & 3)] = qv;
   }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) qa = fmaxf(qa, __shfl_xor_sync(0xffffffffu, qa, off));
+  float* qred = reinterpret_cast<float*>(q4) + GP * D;  // kMmaWarps floats
+  if (lane == 0) qred[warp] = qa;
   __syncthreads();
+  {
+    // the range test (see kVWideAbs): every flushed Key scale is at least
+    // qmax / max(largest Key absmax, eps) rounded, which is >= kthr when the
+    // product below stays under qmax by more than its rounding
+#pragma unroll
+    for (int w = 0; w < kMmaWarps; ++w) qa = fmaxf(qa, qred[w]);
+    const int qexp = float_exp2i(qa);
+    const float kthr = fmaxf(pow2i(BITS == 2 ? qexp + 1 + 4 - 14 : qexp + 1 - 9), p.eps);
+    const int64_t unit = (int64_t)b * p.Hkv + h;
+    const float kabs = p.range ? __uint_as_float(p.range[2 * unit]) : 0.f;
+    const float vabs = p.range ? __uint_as_float(p.range[2 * unit + 1]) : 0.f;
+    if (!(fmaxf(kabs, p.eps) * kthr <= (float)p.qmax * 0.9999f && vabs <= kVWideAbs * 0.999f)) {
+      simt_item<__nv_bfloat16, BITS, D / 32, false>(p, i, h, false, pg0, pg1, slot, reinterpret_cast<float*>(buf));
+      return;
+    }
+  }
 
   // source of this warp's pos-th unit (units u0 + warp, + 4, ...), through
   // the block table for a paged cache
@@ -1116,7 +1171,7 @@ size_t smem_for(const DecodeParams& p) {
   const size_t window = (size_t)kMmaWarps * kRowsBuf<D, 2>;
   if (pages < merge) pages = merge;
   if (pages < window) pages = window;
-  const size_t scratch = ((size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D + (size_t)gqa_pad(p.g) * D) * sizeof(float);
+  const size_t scratch = ((size_t)kMmaWarps * (8 / gqa_pad(p.g)) * D + (size_t)gqa_pad(p.g) * D + 32) * sizeof(float);
   return 128 * ((kMmaWarps * slots * 8 + 127) / 128) + scratch + pages;
 }
 

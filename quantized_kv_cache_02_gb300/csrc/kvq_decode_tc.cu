@@ -141,7 +141,7 @@ struct TcShape {
   static constexpr size_t kBOff = ((size_t)kTcSlots * kTcBlock + 1023) / 1024 * 1024;  // B operands
   static constexpr size_t kBq = (size_t)NS * kTcBRow;                                  // one B_Q buffer
   static constexpr size_t smem =
-      kBOff + 2 * kBq + 16 * kTcBRow + GP * kTcD * 4 + (96 + 3 * 4 * 8) * 4 + (2 * kTcSlots + 5) * 8 + 32;
+      kBOff + 2 * kBq + 16 * kTcBRow + GP * kTcD * 4 + (96 + 3 * 4 * 8 + 8 + 3 * 4 + 2) * 4 + (2 * kTcSlots + 5) * 8 + 32;
 };
 
 template <uint32_t N>
@@ -196,6 +196,30 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
 }
 __device__ const int kNoAbort = 0;  // for waits that must not be cut short
 
+// Range of the f16 operands (as in decode_mma_kernel, 4-bit codes).  The
+// smallest Key scale for which a unit keeps biased codes and an unscaled
+// B_Q: |q / sK| <= 2^9.  ``qred`` holds the largest |q * qk_scale| of each
+// of the 8 warps that filled the queries.
+__device__ __forceinline__ float tc_kthr(const float* qred, float eps, int* qexp) {
+  float qa = qred[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) qa = fmaxf(qa, qred[w]);
+  *qexp = float_exp2i(qa);
+  const int e = *qexp + 1 - 9;
+  return fmaxf(e < -126 ? 0.f : e > 127 ? INFINITY : __uint_as_float((uint32_t)(e + 127) << 23), eps);
+}
+// Whether block ``sb`` of up to four units has a token whose Value absmax
+// (qmax / sV) exceeds kVWideAbs: its output terms are then summed in fp32
+// (every Key warp decides alike).
+__device__ __forceinline__ bool tc_value_wide(const uint8_t* sb, int nu, int lane, int vsc_off, int unit_stride,
+                                              float vwide) {
+  bool w = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (j < nu) w |= fast_rcp(reinterpret_cast<const float*>(sb + j * unit_stride + vsc_off)[lane]) > vwide;
+  return __any_sync(0xffffffffu, w);
+}
+
 // Every mbarrier of the CTA completes once per block.  A thread arrives on a
 // barrier for block b + 1 only after it has seen block b's phase complete, and
 // it waits on a phase only while no later phase can complete without its own
@@ -240,7 +264,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   float* qs = reinterpret_cast<float*>(bpm + 16 * kTcBRow);
   float* red = qs + GP * D;                // [0, 32): maxima; [32, 64): l; [64, 96): Value bias sums
   float* beta = red + 96;                  // [3][4 units][8 heads] Key bias sums
-  uint64_t* bars = reinterpret_cast<uint64_t*>(beta + 3 * 4 * 8);
+  float* qred = beta + 3 * 4 * 8;          // [8]: largest |q| seen by each filling warp
+  float* kback = qred + 8;                 // [3][4 units]: 2^F taken out of the unit's B_Q
+  int* vflag = reinterpret_cast<int*>(kback + 3 * 4);  // [2]: block (by parity) is wide (no output MMAs)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(vflag + 2);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kTcSlots + 5);
   volatile int* abort = reinterpret_cast<volatile int*>(tslot + 1);  // set by whichever part stops
   // ring slots: ``full`` (copies landed) and ``empty`` (every worker is done with it)
@@ -267,12 +294,17 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
   }
   if (t < 2 * kTcGroup) {
     // queries (head n % g for the padding heads), pre-scaled
+    float qa = 0.f;
     for (int idx = t; idx < GP * D; idx += 2 * kTcGroup) {
       const int n = idx / D, c = idx - n * D;
       qs[idx] = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(
                     p.q)[((int64_t)b * p.Hq + (int64_t)h * p.g + n % p.g) * D + c]) *
                 p.qk_scale;
+      qa = fmaxf(qa, fabsf(qs[idx]));
     }
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) qa = fmaxf(qa, __shfl_xor_sync(0xffffffffu, qa, off));
+    if (lane == 0) qred[warp] = qa;
     // B operands start at zero (B_P rows GP..15 stay zero)
     for (int idx = t; idx < (int)((2 * TS::kBq + 16 * kTcBRow) / 16); idx += 2 * kTcGroup)
       reinterpret_cast<uint4*>(bq)[idx] = make_uint4(0u, 0u, 0u, 0u);
@@ -371,9 +403,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
         }
         mbar_arrive(bar_empty + 8 * (blk % kTcSlots));  // the copy warp may refill this block's slot
         tc_fence_after();
+        // a wide block's output terms are added by the Key warps in fp32;
+        // O starts at zero (the Key warps clear it before block 0)
+        if (vflag[blk & 1] == 0) {
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          tc_mma(tm + TS::kColO, tm + TS::kColAV + 8 * ks, dp + 16 * ks, idesc_o, (blk > 0 || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks)
+            tc_mma(tm + TS::kColO, tm + TS::kColAV + 8 * ks, dp + 16 * ks, idesc_o, 1u);
+        }
         tc_commit(bar_o);
         ++n_o;
       }
@@ -389,6 +425,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
     // Key bias sums of unit ``vw`` ============================================
     const int vw = warp - 4, c = t - kTcGroup;
     const int oct = lane >> 1, e0 = (lane & 1) * CPG;
+    // range of q / sK (as in decode_mma_kernel): the plain path needs every
+    // Key scale of the unit >= kthr; otherwise the unit's B_Q carries 2^-F
+    int qexp;
+    const float kthr = tc_kthr(qred, p.eps, &qexp);
     float qreg[CPG][8];
 #pragma unroll
     for (int e = 0; e < CPG; ++e)
@@ -410,9 +450,24 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       uint8_t* bqb = bq + (blk & 1) * TS::kBq;
       if (vw < nu) {
         const float4* ks4 = reinterpret_cast<const float4*>(sb + vw * kTcUnitStride + kTcKsc) + 2 * oct;
-        const float4 s0 = ks4[0], s1 = ks4[1];
-        const float r[8] = {fast_rcp(s0.x), fast_rcp(s0.y), fast_rcp(s0.z), fast_rcp(s0.w),
-                            fast_rcp(s1.x), fast_rcp(s1.y), fast_rcp(s1.z), fast_rcp(s1.w)};
+        float4 s0 = ks4[0], s1 = ks4[1];
+        const float smin = fminf(fminf(fminf(s0.x, s0.y), fminf(s0.z, s0.w)), fminf(fminf(s1.x, s1.y), fminf(s1.z, s1.w)));
+        float fs = 1.f, fb = 1.f;
+        const bool wide = __any_sync(0xffffffffu, smin < kthr);
+        if (wide) {
+          // scales below eps divide by eps; 2^-F keeps every B element below 2^14
+          float m = fmaxf(smin, p.eps);
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) m = fminf(m, __shfl_xor_sync(0xffffffffu, m, off));
+          const int F = min(kMaxRangeShift, max(0, qexp + 1 + 4 - float_exp2i(m) + 1 - 14));
+          fs = pow2_neg(F);
+          fb = __uint_as_float((uint32_t)(127 + F) << 23);
+          s0 = make_float4(fmaxf(s0.x, p.eps), fmaxf(s0.y, p.eps), fmaxf(s0.z, p.eps), fmaxf(s0.w, p.eps));
+          s1 = make_float4(fmaxf(s1.x, p.eps), fmaxf(s1.y, p.eps), fmaxf(s1.z, p.eps), fmaxf(s1.w, p.eps));
+        }
+        if (lane == 0) kback[(blk % 3) * 4 + vw] = fb;
+        const float r[8] = {fast_rcp(s0.x) * fs, fast_rcp(s0.y) * fs, fast_rcp(s0.z) * fs, fast_rcp(s0.w) * fs,
+                            fast_rcp(s1.x) * fs, fast_rcp(s1.y) * fs, fast_rcp(s1.z) * fs, fast_rcp(s1.w) * fs};
 #pragma unroll
         for (int e = 0; e < CPG; ++e) {
           uint32_t hw[4], lw[4];
@@ -435,7 +490,8 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
           // sum over the 16 octets (lanes of the same parity)
 #pragma unroll
           for (int off = 2; off < 32; off <<= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, off);
-          if (oct == 0) beta[((blk % 3) * 4 + vw) * 8 + e0 + e] = bsum;
+          // signed Key codes (a wide unit) take no bias out
+          if (oct == 0) beta[((blk % 3) * 4 + vw) * 8 + e0 + e] = wide ? 0.f : bsum;
         }
       }
       fence_proxy_async();
@@ -473,12 +529,22 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
     // ================= Key warps: A_K (one token per thread), scores, softmax,
     // B_P, and the unit's partial =============================================
     bool fail = false;
+    int qexp;
+    const float kthr = tc_kthr(qred, p.eps, &qexp);
     auto k_codes = [&](int blk) {
       const int s = blk % kTcSlots;
       const uint8_t* sb = ring + s * kTcBlock;
       fail |= !wait_or_abort(bar_ring + 8 * s, (uint32_t)(blk / kTcSlots) & 1u, abort);
       const uint4* kr = reinterpret_cast<const uint4*>(sb + warp * kTcUnitStride + lane * (D / 2));
       const uint32_t colk = TS::kColAK;
+      // a wide unit (some Key scale below kthr, decided as its B_Q builder
+      // decides) enters with signed codes
+      bool wide = false;
+      if (warp < min(4, nunits - 4 * blk)) {
+        const float4 s4 = reinterpret_cast<const float4*>(sb + warp * kTcUnitStride + kTcKsc)[lane];
+        wide = fminf(fminf(s4.x, s4.y), fminf(s4.z, s4.w)) < kthr;
+      }
+      wide = __any_sync(0xffffffffu, wide);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         const uint4 w = kr[qq];
@@ -487,6 +553,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
         nibble_regs(w.y, *reinterpret_cast<uint32_t(*)[4]>(r + 4));
         nibble_regs(w.z, *reinterpret_cast<uint32_t(*)[4]>(r + 8));
         nibble_regs(w.w, *reinterpret_cast<uint32_t(*)[4]>(r + 12));
+        if (wide) {
+#pragma unroll
+          for (int q4i = 0; q4i < 4; ++q4i) unbias_nibbles(*reinterpret_cast<uint32_t(*)[4]>(r + 4 * q4i));
+        }
         tc_st16(lane_base + colk + 16 * qq, r);
       }
       tc_wait_st();
@@ -499,6 +569,13 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       m_run[e] = -INFINITY;
       l_part[e] = 0.f;
       c_part[e] = 0.f;
+    }
+    {
+      float z[GP];
+#pragma unroll
+      for (int e = 0; e < GP; ++e) z[e] = 0.f;
+      tc_st_f<GP>(lane_base + TS::kColO, z);
+      tc_wait_st();
     }
     k_codes(0);
     int n_o = 0;
@@ -526,11 +603,16 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
       }
       tc_wait_ld();
       float sc[GP];
+      // this thread's token: 1/sV (x1/16 on the x16 slots)
+      const float* vs = reinterpret_cast<const float*>(sb + warp * kTcUnitStride + kTcVsc);
+      const bool x16 = (lane >> 1) & 1;
+      float iv = valid ? fast_rcp(vs[lane]) * (x16 ? 0.0625f : 1.f) : 0.f;
       bool up = fail;
+      const float kb = kback[(blk % 3) * 4 + warp];
 #pragma unroll
       for (int e = 0; e < GP; ++e) {
         const float bias = 8.f * beta[((blk % 3) * 4 + warp) * 8 + e];
-        sc[e] = valid ? fmaf(sc2[e] + sc2[GP + e], kTwo24, -bias) : -INFINITY;
+        sc[e] = valid ? fmaf(sc2[e] + sc2[GP + e], kTwo24, -bias) * kb : -INFINITY;
         up |= sc[e] > m_run[e] + kSlack;
       }
       // the previous block's O MMAs are done: B_P and the O accumulator are free
@@ -573,19 +655,63 @@ __global__ void __launch_bounds__(kTcThreads, 2) decode_tc_kernel(const DecodePa
         kgroup_sync();  // every warp has read the maxima before they are written again
       }
       // -- P / sV into B_P (row e, k-slot = block token), x1/16 on the x16 slots;
-      // the Value bias is 8 times the sum of exactly these f16 values
+      // the Value bias is 8 times the sum of exactly these f16 values.  A wide
+      // block (some Value absmax > kVWideAbs, or a Value scale below eps,
+      // which divides by eps) has no output MMAs: each thread adds its
+      // channel's terms code * p * min(1/sV, 1/eps) * 2^-24 over the block's
+      // tokens to O in fp32 (signed codes, no bias; the weights pass through
+      // the B_P area, which no MMA reads for this block).
       {
-        const float* vs = reinterpret_cast<const float*>(sb + warp * kTcUnitStride + kTcVsc);
-        const bool x16 = (lane >> 1) & 1;
-        const float iv = valid ? fast_rcp(vs[lane]) * (x16 ? 0.0625f : 1.f) : 0.f;
         const int k = 32 * warp + lane;
+        const bool vwide = tc_value_wide(sb, nu, lane, kTcVsc, kTcUnitStride, kVWideAbs / (float)p.qmax);
+        if (t == 0) vflag[blk & 1] = vwide ? 1 : 0;
+        float pw[GP];
 #pragma unroll
         for (int e = 0; e < GP; ++e) {
-          const float pw = valid ? fast_exp2(sc[e] - (m_run[e] == -INFINITY ? 0.f : m_run[e])) : 0.f;
-          l_part[e] += pw;
-          const __half hv = __float2half_rn(pw * iv);
-          c_part[e] = fmaf(__half2float(hv), x16 ? 16.f : 1.f, c_part[e]);
-          *reinterpret_cast<__half*>(bpm + b_off(e, k)) = hv;
+          pw[e] = valid ? fast_exp2(sc[e] - (m_run[e] == -INFINITY ? 0.f : m_run[e])) : 0.f;
+          l_part[e] += pw[e];
+        }
+        if (!vwide) {
+#pragma unroll
+          for (int e = 0; e < GP; ++e) {
+            const __half hv = __float2half_rn(pw[e] * iv);
+            c_part[e] = fmaf(__half2float(hv), x16 ? 16.f : 1.f, c_part[e]);
+            *reinterpret_cast<__half*>(bpm + b_off(e, k)) = hv;
+          }
+        } else {
+          float* wts = reinterpret_cast<float*>(bpm);  // [128 tokens][GP]
+          const float ivr = fminf(iv * (x16 ? 16.f : 1.f), fast_rcp(p.eps)) * 5.9604644775390625e-8f;
+#pragma unroll
+          for (int e = 0; e < GP; ++e) wts[k * GP + e] = pw[e] * ivr;
+          kgroup_sync();
+          // this thread's channel c = k: its 16-byte code row in each unit
+          float acc[GP];
+#pragma unroll
+          for (int e = 0; e < GP; ++e) acc[e] = 0.f;
+#pragma unroll 1
+          for (int j = 0; j < nu; ++j) {
+            const uint4 cw = *reinterpret_cast<const uint4*>(sb + j * kTcUnitStride + kTcVcode + k * 16);
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+#pragma unroll
+              for (int nb = 0; nb < 8; ++nb) {
+                // nibble nb of word wi is token 8 wi + 2 nb (nb < 4), else 8 wi + 2 (nb - 4) + 1
+                const int tok = 32 * j + 8 * wi + (nb < 4 ? 2 * nb : 2 * (nb - 4) + 1);
+                const float code = (float)((int)((words[wi] >> (4 * nb)) & 0xFu) - 8);
+#pragma unroll
+                for (int e = 0; e < GP; ++e) acc[e] = fmaf(code, wts[tok * GP + e], acc[e]);
+              }
+            }
+          }
+          float o[GP];
+          tc_ld<GP>(lane_base + TS::kColO, o);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < GP; ++e) o[e] += acc[e];
+          tc_st_f<GP>(lane_base + TS::kColO, o);
+          tc_wait_st();
+          kgroup_sync();  // every thread has read the weights before B_P is written again
         }
       }
       tc_fence_before();

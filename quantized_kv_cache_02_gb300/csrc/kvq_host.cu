@@ -56,6 +56,7 @@ struct kvq_cache {
   uint8_t* base;
   size_t arena_bytes;
   int32_t* status;
+  uint32_t* range;  // [batch][Hkv][2]: largest flushed Key / Value absmax (null: segmented)
   kvq::SeqLayout* layout;
   uint8_t* pages;
   void* ring_k;
@@ -118,7 +119,7 @@ int rcap_of(const kvq_config* c) {
 }
 
 struct ArenaPlan {
-  size_t status, layout, table, pages, ring_k, ring_v, partials, total;
+  size_t status, range, layout, table, pages, ring_k, ring_v, partials, total;
   std::vector<int64_t> pages_cap, page_base;
   int max_splits, min_chunk_pages;
   int32_t table_stride;
@@ -151,6 +152,8 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int
   size_t o = 0;
   a->status = o;
   o = align_up(o + sizeof(int32_t), kAlign);
+  a->range = o;
+  o = align_up(o + units * 2 * sizeof(uint32_t), kAlign);
   a->layout = o;
   o = align_up(o + (size_t)c->batch * sizeof(kvq::SeqLayout), kAlign);
   a->table = o;
@@ -294,6 +297,7 @@ void base_decode_params(const kvq_cache* c, kvq::DecodeParams* p) {
   p->G = c->cfg.group;
   p->Rcap = c->rcap;
   p->bits = c->bits;
+  p->qmax = c->cfg.qmax;
   p->eps = c->cfg.eps;
   p->qk_scale = (float)(1.4426950408889634 / std::sqrt((double)c->cfg.head_dim));
   p->geom = c->geom;
@@ -305,6 +309,7 @@ void base_decode_params(const kvq_cache* c, kvq::DecodeParams* p) {
   p->partials = c->partials;
   p->max_splits = c->max_splits;
   p->status = c->status;
+  p->range = c->range;
 }
 
 }  // namespace
@@ -390,6 +395,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   c->base = static_cast<uint8_t*>(device_mem);
   c->arena_bytes = device_bytes;
   c->status = reinterpret_cast<int32_t*>(c->base + a.status);
+  c->range = reinterpret_cast<uint32_t*>(c->base + a.range);
   c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + a.layout);
   c->table = c->paged ? reinterpret_cast<int32_t*>(c->base + a.table) : nullptr;
   c->pages = c->base + a.pages;
@@ -413,6 +419,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
     c->seg.row_bytes = cfg->head_dim * c->bits / 8;
     c->kmax = reinterpret_cast<uint32_t*>(c->base + sp.kmax);
     c->status = reinterpret_cast<int32_t*>(c->base + sp.status);
+    c->range = nullptr;
     c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + sp.layout);
     c->pages = nullptr;
     c->ring_k = c->base + sp.ring_k;
@@ -428,6 +435,8 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   }
   e = cudaMemcpy(c->layout, table.data(), table.size() * sizeof(kvq::SeqLayout), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(int32_t));
+  if (e == cudaSuccess && c->range)
+    e = cudaMemset(c->range, 0, (size_t)cfg->batch * cfg->n_kv_heads * 2 * sizeof(uint32_t));
   if (e == cudaSuccess) {
     const size_t smem = kvq::flush_launch_smem(cfg->group, cfg->head_dim, esize_of(cfg));
     e = kvq::configure_append(cfg->dtype, c->bits, smem);
@@ -554,6 +563,20 @@ static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (c->segmented) return append_segmented(c, new_k, new_v, n_tokens, seq_begin, n_seqs, s);
+  // a sequence that starts from empty (new, or released) starts its range
+  // maxima afresh: one memset per run of such sequences, before any launch
+  for (int b = seq_begin; b < seq_begin + n_seqs;) {
+    if (c->total[b] != 0) {
+      ++b;
+      continue;
+    }
+    int e = b;
+    while (e < seq_begin + n_seqs && c->total[e] == 0) ++e;
+    const size_t per = (size_t)c->cfg.n_kv_heads * 2;
+    const cudaError_t err = cudaMemsetAsync(c->range + b * per, 0, (size_t)(e - b) * per * sizeof(uint32_t), s);
+    if (err != cudaSuccess) return cuda_fail(err, "range reset");
+    b = e;
+  }
   const int64_t R = c->cfg.residual_len, G = c->cfg.group;
   const int64_t per_seq_elems = (int64_t)c->cfg.n_kv_heads * n_tokens * c->cfg.head_dim;
   // groups each sequence flushes in this call
@@ -606,6 +629,7 @@ static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v
     p.bits = c->bits;
     p.eps = c->cfg.eps;
     p.v_prefetch = kvq::flush_v_prefetch((int)G, p.D, (int)c->esize);
+    p.range = c->range;
     p.geom = c->geom;
     p.pages = c->pages;
     p.map = page_map(c);

@@ -147,6 +147,9 @@ struct AppendParams {
   int32_t flush_blocks;        // grid.x slots for flush groups (0 if none in this launch)
   int32_t window_blocks;       // grid.x slots for window writes (0 or 1)
   int32_t v_prefetch;          // flush_v_prefetch(G, D, esize)
+  // [batch][Hkv][2]: bits of the largest Key and Value absmax each unit has
+  // flushed (atomicMax; non-negative floats order as their bits)
+  uint32_t* range;
   SeqCounters old[kMaxSeqsPerLaunch];
   // paged caches: the blocks of sequence i's new groups are
   // blk_ids[blk_first[i] ..]; the flush writes them into the block table
@@ -155,7 +158,7 @@ struct AppendParams {
 };
 
 struct DecodeParams {
-  int32_t D, Hkv, Hq, g, G, Rcap, bits;
+  int32_t D, Hkv, Hq, g, G, Rcap, bits, qmax;
   float eps;
   float qk_scale;              // log2(e) / sqrt(D): scores are kept in base 2
   PageGeom geom;
@@ -164,6 +167,7 @@ struct DecodeParams {
   const void* ring_k;
   const void* ring_v;
   const void* q;               // [batch][Hq][D]
+  const uint32_t* range;       // the flushed absmax maxima per unit (AppendParams::range)
   float* partials;             // [batch*Hkv][max_splits][g][part_row(D)]
   int32_t max_splits;          // slots per unit; the window uses slot max_splits - 1
   int32_t chunk_pages;         // pages per quantized split
