@@ -145,28 +145,31 @@ class InputSpec:
         return round_to_bf16(x) if self.bf16 else x
 
     # ---- host blocks --------------------------------------------------------
-    def kv_block(self, layer: int, seqs, t0: int, n: int):
+    def kv_block(self, layer: int, seqs, t0: int, n: int, heads=None):
         """K, V for tokens [t0, t0 + n) of the given sequences:
-        fp32 arrays [len(seqs), n_kv_heads, n, head_dim]."""
+        fp32 arrays [len(seqs), n_kv_heads, n, head_dim], or
+        [len(seqs), len(heads), n, head_dim] for a subset ``heads`` of the KV
+        heads (each head's values do not depend on the others)."""
         seqs = list(seqs)
         H, D = self.n_kv_heads, self.head_dim
+        heads = list(range(H)) if heads is None else list(heads)
         sig = self.sigma(layer)
         t = np.arange(t0, t0 + n, dtype=np.uint64)
         idx = (t[:, None] * U64(D) + np.arange(D, dtype=np.uint64)[None, :])
-        K = np.empty((len(seqs), H, n, D), dtype=np.float32)
+        K = np.empty((len(seqs), len(heads), n, D), dtype=np.float32)
         V = np.empty_like(K)
         for i, b in enumerate(seqs):
-            for h in range(H):
+            for hi, h in enumerate(heads):
                 hk = hash_at(self.key("K", layer, b, h), idx)
                 k = np.multiply(NORMAL_TABLE[(hk >> U64(48)).astype(np.int64)], sig[h][None, :], dtype=np.float32)
                 if self.spikes:
                     spike = (hk & U64(0xFFFFFFFF)) < U64(SPIKE_THRESHOLD)
                     k = np.where(spike, np.multiply(k, np.float32(SPIKE_FACTOR), dtype=np.float32), k)
-                K[i, h] = self._finish(k)
+                K[i, hi] = self._finish(k)
                 hv = hash_at(self.key("V", layer, b, h), idx)
                 tau = TAU_TABLE[(hash_at(self.key("tau", layer, b, h), t) >> U64(52)).astype(np.int64)]
                 v = np.multiply(NORMAL_TABLE[(hv >> U64(48)).astype(np.int64)], tau[:, None], dtype=np.float32)
-                V[i, h] = self._finish(v)
+                V[i, hi] = self._finish(v)
         return K, V
 
     def q_block(self, layer: int, seqs, step: int) -> np.ndarray:

@@ -299,101 +299,3 @@ def test_edge_cases(kvq, torch):
     with pytest.raises(kvq.KVQError):
         kvq.kvq_append(pair.cache.handle, 16, 16, 1, 2, 2, 0)
     pair.status_ok()
-
-
-# --------------------------------------------------------------------------
-# full-size workloads, launched as the benchmark launches them; sampled outputs
-# --------------------------------------------------------------------------
-
-def _device_prefill(kvq, torch, spec, cache, layer, lengths, chunk=None):
-    from kvq_inputs.device import DeviceInputs
-    dev = DeviceInputs(spec)
-    uniform = len(set(lengths)) == 1 and chunk is None
-    if uniform:
-        K, V = dev.kv_block(layer, 0, len(lengths), 0, lengths[0])
-        cache.append(K, V, 0)
-        del K, V
-    else:
-        for b, n in enumerate(lengths):
-            step = chunk or n
-            for t0 in range(0, n, step):
-                K, V = dev.kv_block(layer, b, 1, t0, min(step, n - t0))
-                cache.append(K, V, b)
-    torch.cuda.synchronize()
-    return dev
-
-
-def _oracle_seq(spec, layer, b, T, R, G, qmax):
-    seq = O.GroupedSequence(spec.n_kv_heads, spec.head_dim, R, G, qmax)
-    k, v = spec.kv_block(layer, [b], 0, T)
-    seq.append(k[0], v[0])
-    return seq
-
-
-def _check_unit_vs_oracle(cache, seq, b, h):
-    got = cache.export_unit(b, h)
-    np.testing.assert_array_equal(got["k_codes"], seq.key_codes()[h])
-    np.testing.assert_array_equal(got["v_codes"], seq.value_codes()[h])
-    np.testing.assert_array_equal(got["k_scales"], seq.key_scales()[h])
-    np.testing.assert_array_equal(got["v_scales"], seq.value_scales()[h])
-    np.testing.assert_array_equal(got["window_k"], seq.window_kv()[0][h])
-
-
-def test_full_size_llama_batch32_layer(kvq, torch):
-    """One layer of the 32-layer, batch-32, 8192-token decode cache (4-bit,
-    R=128, G=32); every layer is launched the same way.  Sampled sequences are
-    checked code for code and attention against the oracle after 3 steps."""
-    spec = gen.InputSpec(seed=2, n_kv_heads=8, n_q_heads=32, head_dim=128)
-    B, T, steps = 32, 8192, 3
-    cache = kvq.KVQCache(B, 8, 32, 128, 128, 32, 7, T + 64)
-    dev = _device_prefill(kvq, torch, spec, cache, 5, [T] * B)
-    for s in range(steps):
-        K, V = dev.kv_block(5, 0, B, T + s, 1)
-        cache.append(K, V, 0)
-    q = dev.q_block(5, 0, B, steps - 1)
-    out = cache.decode_attention(q).cpu().numpy()
-    for b in (0, 17, 31):
-        seq = _oracle_seq(spec, 5, b, T + steps, 128, 32, 7)
-        for h in (0, 5):
-            _check_unit_vs_oracle(cache, seq, b, h)
-        ref = seq.attend(spec.q_block(5, [b], steps - 1)[0])
-        assert_attention_close(out[b], ref, f"seq {b}")
-    assert cache.device_status() == 0
-
-
-def test_full_size_ragged_8bit(kvq, torch):
-    """8-bit, 4 sequences with seeded lengths in [1024, 131072], G=64."""
-    spec = gen.InputSpec(seed=3, n_kv_heads=8, n_q_heads=32, head_dim=128, spikes=True)
-    lens = spec.lengths(4, 1024, 131072)
-    cache = kvq.KVQCache(4, 8, 32, 128, 128, 64, 127, [n + 8 for n in lens])
-    dev = _device_prefill(kvq, torch, spec, cache, 0, lens)
-    q = dev.q_block(0, 0, 4, 0)
-    out = cache.decode_attention(q).cpu().numpy()
-    for b in range(4):
-        seq = _oracle_seq(spec, 0, b, lens[b], 128, 64, 127)
-        _check_unit_vs_oracle(cache, seq, b, b % 8)
-        ref = seq.attend(spec.q_block(0, [b], 0)[0])
-        assert_attention_close(out[b], ref, f"seq {b} (T={lens[b]})")
-    assert cache.device_status() == 0
-
-
-def test_full_size_long_video(kvq, torch):
-    """432000-token cache built by 30 appends of 14400 tokens (4-bit, R=256,
-    G=128), then decode steps; two KV heads compared code for code and
-    attention compared at the first and last step."""
-    spec = gen.InputSpec(seed=4, n_kv_heads=8, n_q_heads=32, head_dim=128)
-    T, steps = 432000, 64
-    cache = kvq.KVQCache(1, 8, 32, 128, 256, 128, 7, T + steps)
-    dev = _device_prefill(kvq, torch, spec, cache, 0, [T], chunk=14400)
-    outs = {}
-    for s in range(steps):
-        K, V = dev.kv_block(0, 0, 1, T + s, 1)
-        cache.append(K, V, 0)
-        if s in (0, steps - 1):
-            outs[s] = cache.decode_attention(dev.q_block(0, 0, 1, s)).cpu().numpy()
-    seq = _oracle_seq(spec, 0, 0, T + steps, 256, 128, 7)
-    for h in (0, 6):
-        _check_unit_vs_oracle(cache, seq, 0, h)
-    ref = seq.attend(spec.q_block(0, [0], steps - 1)[0])
-    assert_attention_close(outs[steps - 1][0], ref, "last step")
-    assert cache.device_status() == 0
