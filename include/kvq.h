@@ -38,6 +38,9 @@
  *    stream).  kvq_append and kvq_decode_attention* only enqueue work and never
  *    synchronize; the caller orders calls on one cache (one stream, or events).
  *  - Device pointers must be 16-byte aligned and the tensors contiguous.
+ *  - Device: kernels launch on the current CUDA device; every entry point
+ *    that launches work returns KVQ_EINVAL, before any launch, when that is
+ *    not the device that holds the cache's arena.
  *  - One cache holds one layer.  A multi-layer model creates one cache per layer.
  */
 #ifndef KVQ_H
@@ -292,10 +295,12 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* new_k, const void* new_
 /* No counterpart in the source pages: an addition for callers that cannot
  * allocate device memory when they decode (a plugin whose host framework owns
  * every device allocation, a deployment that reserves all memory once at
- * start-up).  Computes exactly what kvq_decode_attention computes, but keeps the
- * split partials -- the decode's only scratch -- in a fixed array inside the
- * library instead of the arena's scratch region, and allocates nothing: no
- * cudaMalloc, cudaFree or allocating library call.
+ * start-up).  Computes the same attention as kvq_decode_attention, within the
+ * decode tolerance (its split boundaries may differ, so the fp32 rounding of
+ * the partials may), but keeps the split partials -- the decode's only
+ * scratch -- in a fixed array inside the library instead of the arena's
+ * scratch region, and allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library call.
  *  - The array holds 2^21 floats (8 MiB); every GPU that loads the library
  *    holds it until the process exits.  A cache whose batch * n_kv_heads *
  *    (n_q_heads / n_kv_heads) * (head_dim + 4) floats times 2 split columns
@@ -308,7 +313,8 @@ kvq_status kvq_decode_step(kvq_cache* cache, const void* new_k, const void* new_
  *    contents; nothing in it needs to start at zero, since every partial a
  *    call reads is written earlier in the same call.  Calls that overlap on the
  *    GPU (other streams, other caches) race on it: serialize them.
- * Arguments, layout, ownership and errors are those of kvq_decode_attention. */
+ * Arguments, layout, ownership and errors are those of kvq_decode_attention
+ * (KVQ_EINVAL as well when the current device is not the cache's). */
 kvq_status kvq_decode_attention_noalloc(kvq_cache* cache, const void* q, float* out, void* stream);
 
 /* Held-bytes ledger of a live cache (host counters, no device access). */

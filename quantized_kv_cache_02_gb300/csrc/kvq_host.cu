@@ -288,6 +288,18 @@ void plan_splits(const kvq_cache* c, int s0, int n, int requested, int slots, in
   *grid_splits = (int)((pmax + ch - 1) / ch);
 }
 
+// Kernels launch on the current device, and the cache's arena lives on
+// c->device: a launch on another device would read or write the wrong GPU's
+// memory, so every launching entry point refuses it first.
+kvq_status check_device(const kvq_cache* c) {
+  int cur = -1;
+  const cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != c->device)
+    return fail(KVQ_EINVAL, "the current device is %d but the cache lives on device %d", cur, c->device);
+  return KVQ_OK;
+}
+
 void base_decode_params(const kvq_cache* c, kvq::DecodeParams* p) {
   memset(p, 0, sizeof *p);
   p->D = c->cfg.head_dim;
@@ -550,6 +562,7 @@ void kvq_destroy(kvq_cache* cache) { delete cache; }
 static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v, int64_t n_tokens,
                               int32_t seq_begin, int32_t n_seqs, void* stream, bool window_copy) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (kvq_status st = check_device(c)) return st;
   if (n_tokens <= 0) return fail(KVQ_EINVAL, "n_tokens must be positive (got %lld)", (long long)n_tokens);
   if (n_seqs <= 0 || seq_begin < 0 || seq_begin + (int64_t)n_seqs > c->cfg.batch)
     return fail(KVQ_EINVAL, "sequence range [%d, %d) is outside [0, %d)", seq_begin, seq_begin + n_seqs,
@@ -710,6 +723,7 @@ kvq_status kvq_append(kvq_cache* c, const void* new_k, const void* new_v, int64_
 static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* stream, const kvq_decode_opts* opts,
                               const void* step_k, const void* step_v) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (kvq_status st = check_device(c)) return st;
   if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
   const int kernel = opts ? opts->kernel : 0;
   if (kernel < 0 || kernel > 3) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
@@ -880,6 +894,7 @@ extern "C" {
 
 kvq_status kvq_decode_attention_noalloc(kvq_cache* c, const void* q, float* out, void* stream) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (kvq_status st = check_device(c)) return st;
   if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
   const int B = c->cfg.batch, H = c->cfg.n_kv_heads, D = c->cfg.head_dim;
   // one split plan for every sequence, then as many split slots as the array holds
@@ -1186,6 +1201,7 @@ kvq_status kvq_device_status(const kvq_cache* c, int32_t* out_word, void* stream
 kvq_status kvq_restore(const kvq_cache* c, int32_t seq_begin, int32_t n_seqs, void* k_out, void* v_out,
                        int64_t t_stride, kvq_dtype out_dtype, void* stream) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (kvq_status st = check_device(c)) return st;
   if (n_seqs <= 0 || seq_begin < 0 || seq_begin + (int64_t)n_seqs > c->cfg.batch)
     return fail(KVQ_EINVAL, "sequence range [%d, %d) is outside [0, %d)", seq_begin, seq_begin + n_seqs,
                 c->cfg.batch);
@@ -1267,6 +1283,7 @@ kvq_status kvq_restore(const kvq_cache* c, int32_t seq_begin, int32_t n_seqs, vo
 kvq_status kvq_dense_decode_attention(kvq_cache* c, const void* k, const void* v, int64_t t_stride, const void* q,
                                       float* out, void* stream) {
   if (!c) return fail(KVQ_EINVAL, "cache is NULL");
+  if (kvq_status st = check_device(c)) return st;
   if (!aligned16(k) || !aligned16(v) || !aligned16(q) || !aligned16(out))
     return fail(KVQ_EINVAL, "k / v / q / out must be non-NULL 16-byte aligned device pointers");
   if (c->cfg.dtype != KVQ_BF16 || (c->cfg.head_dim != 64 && c->cfg.head_dim != 128))

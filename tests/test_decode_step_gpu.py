@@ -65,3 +65,46 @@ def test_decode_step_equals_append_then_decode(kvq, torch, D, G, qmax, dtype, po
         np.testing.assert_array_equal(ua["window_k"], ub["window_k"])
         np.testing.assert_array_equal(ua["window_v"], ub["window_v"])
     assert a.device_status() == 0
+
+
+@pytest.mark.parametrize("kernel", [0, 3])
+def test_decode_step_against_the_oracle(kvq, torch, kernel):
+    """kvq_decode_step compared with the oracle directly: the oracle appends
+    the step's token ("KV Cache Quantization Strategies", append_and_partition,
+    grouped) and attends over the held tokens, the new one included ("KV
+    Cache 与自回归视频生成" 3.1); attention within |d| <= 1e-3 + 1e-2 |ref|,
+    codes, scales and window bit for bit, over steps with and without a
+    flush."""
+    from oracle import kvq_oracle as O
+    B, H, Hq, D, R, G, qmax = 3, 4, 16, 128, 64, 32, 7
+    spec = gen.InputSpec(seed=52, n_kv_heads=H, n_q_heads=Hq, head_dim=D)
+    lens = [R + G - 2, 300, 70]
+    cache = kvq.KVQCache(B, H, Hq, D, R, G, qmax, max(lens) + G + 8)
+    seqs = [O.GroupedSequence(H, D, R, G, qmax) for _ in range(B)]
+    dev = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to("cuda").bfloat16().contiguous()
+    for s, n in enumerate(lens):
+        k, v = spec.kv_block(0, [s], 0, n)
+        cache.append(dev(k), dev(v), s)
+        seqs[s].append(k[0], v[0])
+    for step in range(G + 3):
+        k = np.concatenate([spec.kv_block(0, [s], lens[s] + step, 1)[0] for s in range(B)])
+        v = np.concatenate([spec.kv_block(0, [s], lens[s] + step, 1)[1] for s in range(B)])
+        q = spec.q_block(0, range(B), step)
+        got = cache.decode_step(dev(k), dev(v), dev(q), kernel=kernel).cpu().numpy()
+        for s in range(B):
+            seqs[s].append(k[s], v[s])
+        if step % 4 == 0 or step in (1, 2, G + 2):
+            ref = np.stack([seqs[s].attend(q[s]) for s in range(B)])
+            excess = np.abs(got - ref) - (1e-3 + 1e-2 * np.abs(ref))
+            assert excess.max() <= 0, f"step {step}: max excess {excess.max():.3e}"
+    for s in range(B):
+        st = cache.seq_state(s)
+        assert (st["total"], st["quantized"], st["window"]) == (seqs[s].total, seqs[s].quantized, seqs[s].window)
+        for h in (0, 3):
+            u = cache.export_unit(s, h)
+            np.testing.assert_array_equal(u["k_codes"], seqs[s].key_codes()[h])
+            np.testing.assert_array_equal(u["v_codes"], seqs[s].value_codes()[h])
+            np.testing.assert_array_equal(u["k_scales"].view(np.uint32), seqs[s].key_scales()[h].view(np.uint32))
+            np.testing.assert_array_equal(u["v_scales"].view(np.uint32), seqs[s].value_scales()[h].view(np.uint32))
+            np.testing.assert_array_equal(u["window_k"], seqs[s].window_kv()[0][h])
+    assert cache.device_status() == 0
