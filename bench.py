@@ -37,7 +37,8 @@ SPLIT_KERNEL_SOURCE = os.path.join(ROOT, "quantized_kv_cache_02_gb300", "csrc", 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "decode_split_traffic.json")
 SPLIT_KERNEL_NAMES = {0: "decode_mma_kernel<128,4> (split, one layer per launch)",
                       2: "decode_mma_kernel<128,4> (split, one layer per launch)",
-                      3: "decode_tc_kernel<4> (tcgen05 split, one layer per launch)"}
+                      3: "decode_tc_kernel<4> (tcgen05 split, one layer per launch)",
+                      4: "decode_line_kernel<128,4> (persistent-warp split, one layer per launch)"}
 
 
 # ---------------------------------------------------------------------------
@@ -302,7 +303,7 @@ def kernel_source_hash():
 def load_traffic(kernel=0):
     """ncu DRAM bytes per split launch, if the capture matches the current
     kernel source (else None).  The capture is of the mma.sync split kernel."""
-    if kernel == 3:
+    if kernel in (3, 4):
         return None
     try:
         with open(TRAFFIC_FILE) as f:
@@ -365,24 +366,38 @@ def variants_layer(torch, kvq, w, dev, peak, steps=20):
     return out
 
 
-def _timed_splits(torch, calls):
+def _timed_splits(torch, calls, batch=32):
     """Run ``calls`` (functions taking split_start, split_stop events) once
-    untimed, then timed; the mean split time in ms and the mean time of a
-    whole call (split + combine) between events around the loop."""
+    untimed, then timed.  Returns the mean split time in ms, the mean time of a
+    whole call (split + combine) on the device, and the host's median time to
+    issue one call in us.  A short decode takes less time on the GPU than its
+    call takes on the host, so each batch of calls is queued behind a bounded
+    spin kernel (torch.cuda._sleep) that lasts longer than the host needs to
+    queue the batch: the events then time the device, not the host."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in calls]
     for a, b in evs:  # torch creates the CUDA event on first record
         a.record()
         b.record()
+    torch.cuda.synchronize()
+    issue = []
     for f in calls:
+        t = time.perf_counter()
         f(None, None)
+        issue.append(time.perf_counter() - t)
+    host_s = statistics.median(issue)  # the first call of a kernel also loads its module
     torch.cuda.synchronize()
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record()
-    for f, (a, b) in zip(calls, evs):
-        f(a.cuda_event, b.cuda_event)
-    t1.record()
-    torch.cuda.synchronize()
-    return sum(a.elapsed_time(b) for a, b in evs) / len(evs), t0.elapsed_time(t1) / len(calls)
+    spin = int(3 * host_s * batch * 2.1e9) + 200000  # cycles at up to 2.1 GHz
+    whole = []
+    for i in range(0, len(calls), batch):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(spin)
+        t0.record()
+        for f, (a, b) in zip(calls[i:i + batch], evs[i:i + batch]):
+            f(a.cuda_event, b.cuda_event)
+        t1.record()
+        torch.cuda.synchronize()
+        whole.append(t0.elapsed_time(t1) / len(calls[i:i + batch]))
+    return sum(a.elapsed_time(b) for a, b in evs) / len(evs), sum(whole) / len(whole), host_s * 1e6
 
 
 def single_layer_b1(torch, kvq, peak, replicas=64, rounds=8):
@@ -403,7 +418,7 @@ def single_layer_b1(torch, kvq, peak, replicas=64, rounds=8):
     o = torch.empty(1, Hq, D, dtype=torch.float32, device="cuda")
     calls = [(lambda a, b, c=c, q=q: c.decode_attention(q, out=o, split_start=a, split_stop=b))
              for _ in range(rounds) for c, q in zip(caches, qs)]
-    split_ms, call_ms = _timed_splits(torch, calls)
+    split_ms, call_ms, host_us = _timed_splits(torch, calls)
     st = caches[0].seq_state(0)
     nbytes = split_bytes([st["quantized"]], [st["window"]], dict(head_dim=D, group=G, n_kv_heads=H, n_q_heads=Hq))
     gbs = nbytes / (split_ms / 1e3) / 1e9
@@ -411,6 +426,8 @@ def single_layer_b1(torch, kvq, peak, replicas=64, rounds=8):
             "l2": f"{replicas} replica caches decoded in rotation ({replicas * nbytes / 1e6:.0f} MB > 129 MB L2)",
             "split_ms": round(split_ms, 5), "decode_ms": round(call_ms, 5), "achieved_gbs": round(gbs, 1),
             "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": int(nbytes),
+            "host_us_per_call": round(host_us, 2),
+            "timing": "each batch of 32 calls queued behind a spin kernel, so the events time the device",
             "status": max(c.device_status() for c in caches)}
 
 
@@ -431,7 +448,7 @@ def ragged_8bit_layer(torch, kvq, peak, steps=20):
     q = dev.q_block(0, 0, 4, 0)
     o = torch.empty(4, Hq, D, dtype=torch.float32, device="cuda")
     calls = [(lambda a, b: cache.decode_attention(q, out=o, split_start=a, split_stop=b)) for _ in range(steps)]
-    split_ms, call_ms = _timed_splits(torch, calls)
+    split_ms, call_ms, host_us = _timed_splits(torch, calls)
     st = [cache.seq_state(b) for b in range(4)]
     nbytes = split_bytes([x["quantized"] for x in st], [x["window"] for x in st],
                          dict(head_dim=D, group=G, n_kv_heads=H, n_q_heads=Hq), bits=8)
@@ -439,7 +456,7 @@ def ragged_8bit_layer(torch, kvq, peak, steps=20):
     return {"workload": f"8-bit ragged batch, lengths {lens}, R 128, G 64, Key spikes",
             "split_ms": round(split_ms, 5), "decode_ms": round(call_ms, 5), "achieved_gbs": round(gbs, 1),
             "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": int(nbytes),
-            "status": cache.device_status()}
+            "host_us_per_call": round(host_us, 2), "status": cache.device_status()}
 
 
 def segmented_layer(torch, kvq, w, dev, peak, batch=8, steps=10):
@@ -881,8 +898,9 @@ def main():
     ap.add_argument("--no-foil", action="store_true", help="skip the dequantize-to-HBM foil measurement")
     ap.add_argument("--no-variants", action="store_true", help="skip the 2-bit and paged one-layer measurements")
     ap.add_argument("--layers", type=int, default=0, help="fewer layers (profiling runs only; 0 = all 32)")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 2, 3],
-                    help="split kernel: 0 = automatic (mma.sync at this shape), 2 = mma.sync, 3 = tcgen05")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 2, 3, 4],
+                    help="split kernel: 0 = automatic (mma.sync at this shape), 2 = mma.sync, 3 = tcgen05, "
+                         "4 = persistent-warp mma.sync")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")

@@ -130,7 +130,17 @@ typedef struct kvq_decode_opts {
                           the bound of kvq_decode_attention enter with signed
                           codes and q / sK scaled by a power of two, blocks
                           with a Value absmax above 16 are summed in fp32);
-                          KVQ_EUNSUPPORTED if not applicable */
+                          4 = persistent-warp mma.sync kernel (same
+                          operands and range handling as 2): every warp
+                          of one resident wave takes an equal share of a
+                          line of work items (32-token quantized pages
+                          weigh 1, 16-token window steps 2), so split
+                          boundaries need not fall on whole groups of
+                          pages; chunk_pages is ignored.  On a segmented
+                          cache, in kvq_decode_step, and where a unit
+                          would need more partials than the cache's split
+                          slots, it runs as 2.  KVQ_EUNSUPPORTED if not
+                          applicable */
   int32_t chunk_pages; /* 0 = automatic: about 6 split items per SM (8 on a
                           segmented cache), rounded to whole 8-page groups at
                           G = 32; with few (sequence, KV head) units on the

@@ -31,6 +31,16 @@ int decode_mma_resident_per_sm(const DecodeParams& p) {
   return p.bits == 2 ? resident_mma_bits2(p) : p.bits == 4 ? resident_mma_bits4(p) : resident_mma_bits8(p);
 }
 
+cudaError_t decode_line(const DecodeParams& p, bool launch, cudaStream_t s, int* per_sm) {
+  if (!decode_mma_supported(p) || p.seg.kcodes || p.step_k) {
+    *per_sm = 0;
+    return cudaSuccess;
+  }
+  return p.bits == 2 ? line_bits2(p, launch, s, per_sm)
+         : p.bits == 4 ? line_bits4(p, launch, s, per_sm)
+                       : line_bits8(p, launch, s, per_sm);
+}
+
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported) {
   *supported = decode_mma_supported(p);
   if (!*supported) return cudaSuccess;

@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "kvq_simt.cuh"
@@ -183,6 +184,20 @@ __device__ __forceinline__ void unbias_nibbles(uint32_t (&r)[4]) {
 __device__ __forceinline__ void byte_regs(uint32_t w, uint32_t (&r)[2]) {
   r[0] = w & 0x00FF00FFu;
   r[1] = (w >> 8) & 0x00FF00FFu;
+}
+
+// f16 hi of (x0, x1), and the f16 of hi - x = -(lo) from the mixed-precision
+// add (f16 + f32 -> f32, exact here: hi and x agree to within an f16 ulp), so
+// that hi + lo carries x to about 22 bits.
+__device__ __forceinline__ void split_hi_neglo(float x0, float x1, uint32_t& hi, uint32_t& nlo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  float d0, d1;
+  asm("{\n .reg .b16 a, b;\n mov.b32 {a, b}, %2;\n add.rn.f32.f16 %0, a, %3;\n add.rn.f32.f16 %1, b, %4;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "r"(hi), "f"(-x0), "f"(-x1));
+  const __half2 l = __floats2half2_rn(d0, d1);
+  nlo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 __device__ __forceinline__ float fast_rcp(float x) {
@@ -388,11 +403,11 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const float x0 = qk[kslot_channel<BITS>(kk, 2 * r)], x1 = qk[kslot_channel<BITS>(kk, 2 * r + 1)];
-        const __half2 hi = __floats2half2_rn(x0, x1);
-        const float2 back = __half22float2(hi);
-        const __half2 lo = __floats2half2_rn(x0 - back.x, x1 - back.y);
-        bh[kk][r] = *reinterpret_cast<const uint32_t*>(&hi);
-        bl[kk][r] = *reinterpret_cast<const uint32_t*>(&lo);
+        // bl holds the lo parts negated (hi - x, exact in fp32), taken off the
+        // hi products where the scores are summed; 8-bit codes share one
+        // accumulator for both, so their lo parts get the sign back here
+        split_hi_neglo(x0, x1, bh[kk][r], bl[kk][r]);
+        if (BITS == 8) bl[kk][r] ^= 0x80008000u;
       }
     }
   }
@@ -418,8 +433,8 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       if (!FULL && j >= npages) break;
       const uint8_t* kc = pg[j] + sub * 32 * S::kRowBytes;
       uint32_t wa[2][S::kWords], wb[2][S::kWords];
-      // hi and lo halves of q accumulate separately: two dependent MMA chains
-      // of half the length, summed once per sub-tile
+      // hi and (negated) lo halves of q accumulate separately: two dependent
+      // MMA chains of half the length, combined once per sub-tile
       float s[2][4], s2[2][4];
 #pragma unroll
       for (int mb = 0; mb < 2; ++mb) {
@@ -450,7 +465,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[mb][e] += s2[mb][e];
+          for (int e = 0; e < 4; ++e) s[mb][e] -= s2[mb][e];
       } else if (BITS == 4) {
 #pragma unroll
         for (int i = 0; i < S::kWords; ++i) {
@@ -468,7 +483,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
 #pragma unroll
         for (int mb = 0; mb < 2; ++mb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[mb][e] += s2[mb][e];
+          for (int e = 0; e < 4; ++e) s[mb][e] -= s2[mb][e];
       } else {
 #pragma unroll
         for (int kk = 0; kk < S::kWords; ++kk) {
@@ -1192,15 +1207,26 @@ cudaError_t configure_t(size_t smem) {
   return cudaSuccess;
 }
 
-// CTAs of the split kernel one SM holds at once for these parameters (0 on error).
+// CTAs of the split kernel one SM holds at once for these parameters (0 on
+// error).  The answer depends only on the device and the shared memory size,
+// so the last one is kept per device: the query costs more host time than a
+// batch-1 decode takes on the GPU.
 template <int D, int BITS, int GP, int MODE>
 int resident_t(const DecodeParams& p) {
   const size_t smem = smem_for<D>(p);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  // (shared memory bytes << 8 | CTAs per SM), one word so that concurrent
+  // callers never see one query's size with another's answer
+  static std::atomic<uint64_t> known[64];
+  const uint64_t k = known[dev].load(std::memory_order_relaxed);
+  if ((k & 0xFFu) != 0 && (k >> 8) == (uint64_t)smem) return (int)(k & 0xFFu);
   int per_sm = 0;
   if (configure_t<D, BITS, GP, MODE>(smem) != cudaSuccess) return 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_mma_kernel<D, BITS, GP, MODE>, kMmaThreads,
                                                     smem) != cudaSuccess)
     return 0;
+  if (per_sm > 0 && per_sm < 256) known[dev].store((uint64_t)smem << 8 | (uint64_t)per_sm, std::memory_order_relaxed);
   return per_sm;
 }
 

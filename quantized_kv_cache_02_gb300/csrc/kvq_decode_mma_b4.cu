@@ -1,7 +1,7 @@
 // Instantiations of the tensor-core split kernel for 4-bit codes (head_dim
 // 64 and 128, every GQA padding and page mode); see kvq_decode_mma.cuh.
 
-#include "kvq_decode_mma.cuh"
+#include "kvq_decode_line.cuh"
 
 namespace kvq {
 
@@ -11,6 +11,10 @@ int resident_mma_bits4(const DecodeParams& p) {
 
 cudaError_t launch_mma_bits4(const DecodeParams& p, cudaStream_t s) {
   return p.D == 64 ? launch_g<64, 4>(p, s) : launch_g<128, 4>(p, s);
+}
+
+cudaError_t line_bits4(const DecodeParams& p, bool launch, cudaStream_t s, int* per_sm) {
+  return p.D == 64 ? line_g<64, 4>(p, launch, s, per_sm) : line_g<128, 4>(p, launch, s, per_sm);
 }
 
 }  // namespace kvq

@@ -64,9 +64,19 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
   const int b = p.seq_begin + i;
   const int h = hq / p.g, j = hq - h * p.g;
   const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
-  const int nsplit = p.dense_chunk > 0 ? (T0 + p.dense_chunk - 1) / p.dense_chunk
-                                      : (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
-  const int nslots = nsplit + (p.dense_chunk == 0 && T0 > Q0 ? 1 : 0);
+  int nsplit = p.dense_chunk > 0 ? (T0 + p.dense_chunk - 1) / p.dense_chunk
+                                 : (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
+  int nslots = nsplit + (p.dense_chunk == 0 && T0 > Q0 ? 1 : 0);
+  if (p.line_warps > 0) {
+    // slots of the warps from the one holding the unit's first line position
+    // to the one holding its last
+    const int64_t C = p.line_start[p.n_seqs];
+    const int64_t cost = Q0 / 32 + 2 * ((T0 - Q0 + 15) / 16);
+    const int64_t s0 = p.line_start[i] + (int64_t)h * cost;
+    const int N = p.line_warps;
+    nslots = cost > 0 ? (int)(((s0 + cost) * N - 1) / C - ((s0 + 1) * N - 1) / C) + 1 : 0;
+    nsplit = nslots;
+  }
   const int D = p.D, nvec = D >> 2;
   const int64_t unit = (int64_t)b * p.Hkv + h;
   const int64_t stride = (int64_t)p.g * part_row(D);

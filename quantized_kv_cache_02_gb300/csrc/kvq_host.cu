@@ -726,7 +726,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
   if (kvq_status st = check_device(c)) return st;
   if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
   const int kernel = opts ? opts->kernel : 0;
-  if (kernel < 0 || kernel > 3) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
+  if (kernel < 0 || kernel > 4) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
   const bool mma_ok = c->cfg.dtype == KVQ_BF16 && (c->cfg.head_dim == 64 || c->cfg.head_dim == 128) &&
                       c->cfg.group % 32 == 0 && c->g >= 2;
   if (kernel == 2 && !mma_ok)
@@ -736,8 +736,12 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
   if (kernel == 3 && !tc_ok)
     return fail(KVQ_EUNSUPPORTED,
                 "tcgen05 kernel needs bf16, head_dim 128, 4-bit codes, group %% 32 == 0 and >= 2 query heads per KV head");
+  if (kernel == 4 && !mma_ok)
+    return fail(KVQ_EUNSUPPORTED,
+                "persistent-warp kernel needs bf16, head_dim 64/128, group %% 32 == 0 and >= 2 query heads per KV head");
   const bool use_tc = kernel == 3;
-  const bool use_mma = kernel == 2 || (kernel == 0 && mma_ok);
+  const bool use_line = kernel == 4 && !step_k && !c->segmented;
+  const bool use_mma = kernel == 2 || kernel == 4 || (kernel == 0 && mma_ok);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (opts && opts->split_start) {
     const cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(opts->split_start), s);
@@ -751,7 +755,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     mma_slots = kvq::decode_mma_resident_per_sm(qp) * c->n_sm;
   }
   struct Batch {
-    int s0, n, chunk, grid;
+    int s0, n, chunk, grid, line_warps;
+    std::vector<int64_t> line_start;
   };
   std::vector<Batch> batches;
   for (int s0 = 0; s0 < c->cfg.batch; s0 += kvq::kMaxSeqsPerLaunch) {
@@ -774,7 +779,40 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     fill_counters(c, bt.s0, bt.n, p.ctr);
     cudaError_t e = cudaSuccess;
     int supported = 0;
-    if (use_tc) {
+    bt.line_warps = 0;
+    if (use_line) {
+      // the line: each sequence's units in order, Q/32 + 2 ceil(W/16)
+      // positions a unit; warps = the resident CTAs x 4
+      int per_sm = 0;
+      e = kvq::decode_line(p, false, s, &per_sm);
+      if (e != cudaSuccess) return cuda_fail(e, "persistent-warp kernel set-up");
+      const int64_t N = (int64_t)per_sm * c->n_sm * 4;
+      bt.line_start.assign(bt.n + 1, 0);
+      for (int k = 0; k < bt.n; ++k) {
+        const int64_t Q = c->quantized[bt.s0 + k], T = c->total[bt.s0 + k];
+        bt.line_start[k + 1] = bt.line_start[k] + (int64_t)c->cfg.n_kv_heads * (Q / 32 + 2 * ((T - Q + 15) / 16));
+      }
+      const int64_t C = bt.line_start[bt.n];
+      // a unit's partials: one per warp that meets it, within the arena's slots
+      int64_t most = 0;
+      for (int k = 0; k < bt.n && N > 0 && C > 0; ++k) {
+        const int64_t cost = (bt.line_start[k + 1] - bt.line_start[k]) / c->cfg.n_kv_heads;
+        if (cost == 0) continue;
+        for (int h = 0; h < c->cfg.n_kv_heads; ++h) {
+          const int64_t s0 = bt.line_start[k] + h * cost;
+          most = std::max(most, ((s0 + cost) * N - 1) / C - ((s0 + 1) * N - 1) / C + 1);
+        }
+      }
+      if (per_sm > 0 && C > 0 && C < (int64_t(1) << 31) && most <= c->max_splits) {
+        bt.line_warps = (int)N;
+        p.line_warps = (int)N;
+        for (int k = 0; k <= bt.n; ++k) p.line_start[k] = bt.line_start[k];
+        e = kvq::decode_line(p, true, s, &per_sm);
+        supported = 1;
+      }
+    }
+    if (supported) {
+    } else if (use_tc) {
       e = kvq::launch_decode_tc(p, s, &supported);
       if (e == cudaSuccess && !supported) return fail(KVQ_EUNSUPPORTED, "tcgen05 kernel does not fit this configuration");
     } else if (use_mma) {
@@ -805,6 +843,8 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     cp.out = out;
     cp.seq_begin = bt.s0;
     cp.n_seqs = bt.n;
+    cp.line_warps = bt.line_warps;
+    for (int k = 0; k < (int)bt.line_start.size(); ++k) cp.line_start[k] = bt.line_start[k];
     fill_counters(c, bt.s0, bt.n, cp.ctr);
     const cudaError_t e = kvq::launch_combine(cp, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");

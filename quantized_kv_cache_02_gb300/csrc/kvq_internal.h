@@ -184,12 +184,22 @@ struct DecodeParams {
   const void* dense_v;
   int64_t t_stride;
   int32_t dense_chunk;         // tokens per dense split
+  // persistent-warp kernel: its warps (grid x 4) and the line position of
+  // each sequence's first unit (line_start[n_seqs] = the line's length); a
+  // sequence's units each take Q/32 + 2 ceil((T - Q) / 16) positions
+  int32_t line_warps;
+  int64_t line_start[kMaxSeqsPerLaunch + 1];
   SeqCounters ctr[kMaxSeqsPerLaunch];
 };
 
 struct CombineParams {
   int32_t D, Hkv, Hq, g, G, max_splits, chunk_pages;
   int32_t dense_chunk;         // > 0: slots are dense token chunks, no window slot
+  // > 0: the partials of the persistent-warp kernel, which takes line_warps
+  // warps over the line (as DecodeParams): a unit's slots are 0 .. n - 1 for
+  // the n warps from the one holding its first position to its last
+  int32_t line_warps;
+  int64_t line_start[kMaxSeqsPerLaunch + 1];
   const float* partials;
   float* out;                  // [batch][Hq][D]
   int32_t seq_begin, n_seqs;
@@ -258,6 +268,13 @@ cudaError_t launch_append(const AppendParams& p, int dtype, cudaStream_t s);
 cudaError_t configure_append(int dtype, int bits, size_t smem_bytes);
 cudaError_t launch_decode_simt(const DecodeParams& p, int dtype, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s, int* supported);
+// the persistent-warp split kernel: launch = false returns its resident CTAs
+// per SM in *per_sm (0: not supported); launch = true launches it with
+// p.line_warps warps
+cudaError_t decode_line(const DecodeParams& p, bool launch, cudaStream_t s, int* per_sm);
+cudaError_t line_bits2(const DecodeParams& p, bool launch, cudaStream_t s, int* per_sm);
+cudaError_t line_bits4(const DecodeParams& p, bool launch, cudaStream_t s, int* per_sm);
+cudaError_t line_bits8(const DecodeParams& p, bool launch, cudaStream_t s, int* per_sm);
 // the split kernel for one code width (one translation unit each)
 // CTAs of the tensor-core split kernel one SM holds at once for p (0: not
 // supported or unknown).

@@ -1,13 +1,13 @@
 """Full-size GPU parity on the benchmark's workloads, launched as the benchmark
-launches them, against the oracle at the density the survey plans: every
-(sequence, KV head) unit's codes, scales and window compared bit for bit
-(as digests of their bytes), and attention compared within
-|d| <= 1e-3 + 1e-2 |ref| on many units and steps.
+launches them, against the oracle: every (sequence, KV head) unit's codes,
+scales and window compared bit for bit (as digests of their bytes), and
+attention compared within |d| <= 1e-3 + 1e-2 |ref| on many units and steps.
 
 - Llama-3-8B decode cache (batch 32, ~8192 tokens, 4-bit, R 128, G 32):
   4 of the 32 layers (each layer is one cache launched the same way); all
   32 x 8 units of each; attention on 16 (layer, sequence) pairs over 3
-  consecutive steps, the second of which flushes a group in every unit.
+  consecutive steps, the second of which flushes a group in every unit, and
+  the persistent-warp kernel (kernel choice 4) on the last of them.
 - Long video (432000 tokens as 30 appends of 14400, R 256, G 128, 4-bit):
   all 8 units; attention after every 8th of the 64 decode steps.
 - 8-bit ragged batch (lengths drawn in [1024, 131072], G 64, Key spikes):
@@ -92,7 +92,7 @@ def test_full_size_llama_batch32_four_layers(kvq, torch, workers):
                                   attend_steps=range(steps) if att else ()))
                 keys.append((layer, b, h))
     pending = workers.map_async(unit_task, tasks, chunksize=8)
-    got_digest, got_out = {}, {}
+    got_digest, got_out, got_line = {}, {}, {}
     for layer in layers:
         cache = kvq.KVQCache(B, H, Hq, D, R, G, qmax, T0 + 8)
         K, V = dev.kv_block(layer, 0, B, 0, T0)
@@ -102,7 +102,11 @@ def test_full_size_llama_batch32_four_layers(kvq, torch, workers):
         for s in range(steps):
             K, V = dev.kv_block(layer, 0, B, T0 + s, 1)
             cache.append(K, V, 0)
-            outs.append(cache.decode_attention(dev.q_block(layer, 0, B, s)).cpu().numpy())
+            q = dev.q_block(layer, 0, B, s)
+            outs.append(cache.decode_attention(q).cpu().numpy())
+            # the persistent-warp kernel on the same cache, last step
+            if s == steps - 1:
+                got_line[layer] = cache.decode_attention(q, kernel=4).cpu().numpy()
             if s == 1:
                 assert all(cache.seq_state(b)["window"] == R for b in range(B)), "step 1 flushes a group"
         for b in range(B):
@@ -119,6 +123,7 @@ def test_full_size_llama_batch32_four_layers(kvq, torch, workers):
         for b in att_seqs:
             ref = np.stack([np.concatenate([results[(layer, b, h)][1][s] for h in range(H)]) for s in range(steps)])
             close(got_out[layer][:, b], ref, f"layer {layer} seq {b}")
+            close(got_line[layer][b], ref[-1], f"layer {layer} seq {b}, persistent-warp kernel")
     assert g == 4
 
 

@@ -87,7 +87,7 @@ class Trio:
         B = len(self.seqs)
         q = self.spec.q_block(0, range(B), step)
         qd = self.dev(q)
-        for kernel in (1, 2):
+        for kernel in (1, 2, 4):
             got = self.paged.decode_attention(qd, kernel=kernel).cpu().numpy()
             flat = self.flat.decode_attention(qd, kernel=kernel).cpu().numpy()
             np.testing.assert_array_equal(got, flat)

@@ -149,7 +149,7 @@ def test_llama_single_layer(kvq, torch):
         pair.append(k, v)
         if step % 8 == 0 or step in (31, 32, 39):
             q = spec.q_block(0, [0], step)
-            for kernel in (1, 2):
+            for kernel in (1, 2, 4):
                 got, ref = pair.attend(q, kernel=kernel)
                 assert_attention_close(got, ref, f"step {step} kernel {kernel}")
     for h in range(8):
@@ -175,7 +175,7 @@ def test_ragged_8bit(kvq, torch):
         v = np.stack([spec.kv_block(0, [b], lens[b] + step, 1)[1][0] for b in range(4)])
         pair.append(k, v)
         q = spec.q_block(0, range(4), step)
-        for kernel in (1, 2):
+        for kernel in (1, 2, 4):
             got, ref = pair.attend(q, kernel=kernel)
             assert_attention_close(got, ref, f"step {step} kernel {kernel}")
     for b in range(4):
@@ -219,7 +219,7 @@ def test_two_bit_ragged_both_kernels(kvq, torch, D, G, qmax):
         v = np.stack([spec.kv_block(0, [b], lens[b] + step, 1)[1][0] for b in range(4)])
         pair.append(k, v)
         q = spec.q_block(0, range(4), step)
-        for kernel in (1, 2):
+        for kernel in (1, 2, 4):
             got, ref = pair.attend(q, kernel=kernel)
             assert_attention_close(got, ref, f"qmax {qmax} D {D} G {G} step {step} kernel {kernel}")
     for b in range(4):
@@ -255,7 +255,7 @@ def test_chunked_prefill_and_invariance(kvq, torch):
             a, b = other.cache.export_unit(0, h), first.cache.export_unit(0, h)
             np.testing.assert_array_equal(a["window_k"], b["window_k"])
     q = spec.q_block(0, [0], 0)
-    for kernel in (1, 2):
+    for kernel in (1, 2, 4):
         got, ref = first.attend(q, kernel=kernel)
         assert_attention_close(got, ref, f"kernel {kernel}")
     first.status_ok()
@@ -282,7 +282,7 @@ def test_edge_cases(kvq, torch):
         pair.check_unit(1, h)
         pair.check_unit(2, h)
     q = spec.q_block(0, range(3), 0)
-    for kernel in (1, 2):
+    for kernel in (1, 2, 4):
         got, ref = pair.attend(q, kernel=kernel, seqs=[0, 1, 2])
         assert not got[0].any()
         assert_attention_close(got[1:], ref[1:], f"kernel {kernel}")

@@ -83,8 +83,9 @@ def run_case(kvq, torch, qmax, kmul, vmul, qmul, seed, kernels, what):
 
 
 def kernels_for(qmax):
-    # 0 automatic, 1 CUDA cores, 2 mma.sync tensor cores, 3 tcgen05 (4-bit only)
-    return (0, 1, 2, 3) if qmax == 7 else (0, 1, 2)
+    # 0 automatic, 1 CUDA cores, 2 mma.sync tensor cores, 3 tcgen05 (4-bit
+    # only), 4 persistent-warp mma.sync
+    return (0, 1, 2, 3, 4) if qmax == 7 else (0, 1, 2, 4)
 
 
 def ones(b, t):

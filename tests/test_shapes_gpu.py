@@ -87,23 +87,23 @@ def test_head_dim_256_bf16_two_bit(kvq, torch):
 def test_batch_above_one_launch(kvq, torch):
     """300 sequences: the decode runs as two launches of 256 and 44."""
     lens = [(37 * b) % 150 + (b % 3) * 64 for b in range(300)]
-    run_case(kvq, torch, lens, 2, 4, 64, 32, 32, 7, "bf16", kernels=(0, 1, 2), seed=63, steps=1)
+    run_case(kvq, torch, lens, 2, 4, 64, 32, 32, 7, "bf16", kernels=(0, 1, 2, 4), seed=63, steps=1)
 
 
 @pytest.mark.parametrize("Hq", [16, 24, 64])
 def test_gqa_on_tensor_cores(kvq, torch, Hq):
     """g = 2, 3 (padded to 4) and 8 query heads per KV head on the mma.sync kernel."""
-    run_case(kvq, torch, [700, 1234], 8, Hq, 128, 128, 32, 7, "bf16", kernels=(2,), seed=64, check_heads=(0, 7))
+    run_case(kvq, torch, [700, 1234], 8, Hq, 128, 128, 32, 7, "bf16", kernels=(2, 4), seed=64, check_heads=(0, 7))
 
 
 @pytest.mark.parametrize("G", [64, 256])
 def test_large_groups_staged(kvq, torch, G):
-    run_case(kvq, torch, [G * 5 + 129, G + 128, 100], 4, 16, 64, 128, G, 7, "bf16", kernels=(1, 2), seed=65)
+    run_case(kvq, torch, [G * 5 + 129, G + 128, 100], 4, 16, 64, 128, G, 7, "bf16", kernels=(1, 2, 4), seed=65)
 
 
 @pytest.mark.parametrize("G", [32, 128])
 def test_odd_chunks_tensor_cores(kvq, torch, G):
     """Split items of odd page counts on the mma.sync kernel (as the whole-wave
     plan picks for long staged units): each warp's run ends on a one-page group."""
-    run_case(kvq, torch, [G * 9 + 50, G * 4 + 3, 130], 4, 16, 128, 128, G, 7, "bf16", kernels=(2,), seed=66,
+    run_case(kvq, torch, [G * 9 + 50, G * 4 + 3, 130], 4, 16, 128, 128, G, 7, "bf16", kernels=(2, 4), seed=66,
              chunks=(0, 1, 3, 5, 7))
