@@ -62,6 +62,12 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// Fire-and-forget copy of [src, src + bytes) from HBM into L2 (16-byte
+// aligned address and size).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
@@ -273,6 +279,8 @@ __device__ __forceinline__ void lds_words(const uint8_t* p, uint32_t (&w)[N]) {
 // kVWideAbs.  Other items take the CUDA-core path (fp32, IEEE division with
 // the eps clamp) inside the same kernel.
 constexpr float kVWideAbs = 16.f;
+// split items of at most this many pages prefetch their first pages to L2
+constexpr int kShortItemPages = 16;
 constexpr int kMaxRangeShift = 100;
 
 // Binary exponent of a positive finite float (floor(log2 x)); 0 gives -127.
@@ -843,6 +851,58 @@ constexpr int kRowsBuf = NBUF * 32 * D * 2;
 // G = 32, and any larger G (either map) staged in 32-token units.
 constexpr int kFlat32 = 0, kPaged32 = 1, kStaged = 2;
 
+// A short split item (a few pages a warp, as at batch 1) spends most of its
+// time waiting: its first copies are issued only after the query set-up,
+// which itself waits on global loads.  Lane 0 of each warp therefore asks L2
+// for the warp's first pages before that set-up (whole pages of a contiguous
+// G = 32 cache), so the copies then hit L2.
+template <int D>
+__device__ __forceinline__ void prefetch_first_pages(const DecodeParams& p, int b, int h, int pg0, int pg1, int warp,
+                                                  int n) {
+  const int64_t stored = p.geom.page_bytes;
+  for (int k = 0; k < n; ++k) {
+    const int pg = pg0 + warp + k * kMmaWarps;
+    if (pg >= pg1) break;
+    prefetch_l2(p.pages + page_offset(p.map, stored, b, h, pg), (uint32_t)stored);
+  }
+}
+
+// The combine inside the split launch (DecodeParams::done): after its partial
+// is written, a CTA counts itself finished for its unit, and the CTA that
+// finishes the unit's last item merges the unit's g query heads (one warp
+// each, merge_head) into the output and sets the count back to 0 for the
+// next launch.  The count is one device-scope acquire-release atomic: the
+// barrier before it orders every thread's partial writes ahead of its
+// release, and for the last CTA its acquire (passed on by the barrier after
+// it) orders the others' partials ahead of the merge's loads, which read L2.
+// No CTA waits for another.
+__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* counter) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
+
+template <int D>
+__device__ __noinline__ void finish_unit(const DecodeParams& p, int i, int h) {
+  __shared__ uint32_t last;
+  const int b = p.seq_begin + i;
+  const int64_t unit = (int64_t)b * p.Hkv + h;
+  const int T0 = p.ctr[i].total, Q0 = p.ctr[i].quantized;
+  const int nsplit = (Q0 / p.G + p.chunk_pages - 1) / p.chunk_pages;
+  const int nslots = nsplit + (T0 > Q0 ? 1 : 0);
+  __syncthreads();
+  if (threadIdx.x == 0) last = arrive_acq_rel(p.done + unit) + 1u == (uint32_t)nslots;
+  __syncthreads();
+  if (!last) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t stride = (int64_t)p.g * part_row(D);
+  const float* base = p.partials + unit * p.max_splits * stride;
+  for (int j = warp; j < p.g; j += kMmaWarps)
+    merge_head<D <= 128 ? 1 : 2, true>(base + (int64_t)j * part_row(D), nsplit, nslots, p.max_splits, stride, D,
+                                       p.out + ((int64_t)b * p.Hq + (int64_t)h * p.g + j) * D, lane);
+  if (threadIdx.x == 0) p.done[unit] = 0u;
+}
+
 // The residual-window item of unit (sequence i of the launch, KV head h): its
 // ring rows on the tensor cores (plus, for kvq_decode_step, this step's token,
 // which it also stores into its ring row).  ``buf`` holds kRowsBuf<D, 2> bytes
@@ -889,6 +949,12 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   const int i = u / p.Hkv, h = u - i * p.Hkv;
   bool win;
   int pg0, pg1, slot;
+  if (p.done && col == 0 && p.ctr[i].total == 0) {
+    // a unit without tokens: zeros (no item of it runs)
+    float* o = p.out + ((int64_t)(p.seq_begin + i) * p.Hq + (int64_t)h * p.g) * D;
+    for (int idx = threadIdx.x; idx < p.g * D; idx += blockDim.x) o[idx] = 0.f;
+    return;
+  }
   if (!split_item(p, col, i, &win, &pg0, &pg1, &slot)) return;
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -922,19 +988,43 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   if (win) {
     window_rows<D, GP>(p, i, h, lane, warp, gid, tig, buf, st);
   } else {
+  if (MODE == kFlat32 && lane == 0 && pg1 - pg0 <= kShortItemPages)
+    prefetch_first_pages<D>(p, b, h, pg0, pg1, warp, slots);
+  // the unit's flushed maxima for the range test below, loaded with the queries
+  float kabs = 0.f, vabs = 0.f;
+  if (p.range) {
+    const uint2 r = *reinterpret_cast<const uint2*>(p.range + 2 * ((int64_t)b * p.Hkv + h));
+    kabs = __uint_as_float(r.x);
+    vabs = __uint_as_float(r.y);
+  }
   // queries of the GP column heads (head n % g for the padding columns, so every
   // value stays finite), pre-scaled, in shared memory: channel c of head n goes
   // to float4 ((i * GP + n) * 4 + tig) with tig = c / (D/4), i = (c % (D/4)) / 4,
   // so the lanes that read together hit distinct banks
+  // (8 channels a thread from one 16-byte load, every load of the CTA in
+  // flight at once)
   float qa = 0.f;
-  for (int idx = threadIdx.x; idx < GP * D; idx += blockDim.x) {
-    const int n = idx / D, c = idx - n * D;
-    const __nv_bfloat16* qrow =
-        reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D;
-    const int tg = c / S::kChan, i4 = (c - tg * S::kChan) >> 2;
-    const float qv = __bfloat162float(qrow[c]) * p.qk_scale;
-    qa = fmaxf(qa, fabsf(qv));
-    reinterpret_cast<float*>(q4)[((i4 * GP + n) * 4 + tg) * 4 + (c & 3)] = qv;
+#pragma unroll
+  for (int x0 = 0; x0 < GP * D / 8; x0 += kMmaThreads) {
+    const int x = x0 + threadIdx.x;
+    if (GP * D / 8 % kMmaThreads == 0 || x < GP * D / 8) {
+      const int n = x / (D / 8), c0 = (x - n * (D / 8)) * 8;
+      const uint4 raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                                        ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D + c0);
+      const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      float qv[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(q2[e]);
+        qv[2 * e] = f.x * p.qk_scale;
+        qv[2 * e + 1] = f.y * p.qk_scale;
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qa = fmaxf(qa, fabsf(qv[e]));
+      const int tg = c0 / S::kChan, i4 = (c0 - tg * S::kChan) >> 2;  // channels c0 .. c0 + 3, then i4 + 1
+      q4[(i4 * GP + n) * 4 + tg] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+      q4[((i4 + 1) * GP + n) * 4 + tg] = make_float4(qv[4], qv[5], qv[6], qv[7]);
+    }
   }
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) qa = fmaxf(qa, __shfl_xor_sync(0xffffffffu, qa, off));
@@ -949,11 +1039,9 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     for (int w = 0; w < kMmaWarps; ++w) qa = fmaxf(qa, qred[w]);
     const int qexp = float_exp2i(qa);
     const float kthr = fmaxf(pow2i(BITS == 2 ? qexp + 1 + 4 - 14 : qexp + 1 - 9), p.eps);
-    const int64_t unit = (int64_t)b * p.Hkv + h;
-    const float kabs = p.range ? __uint_as_float(p.range[2 * unit]) : 0.f;
-    const float vabs = p.range ? __uint_as_float(p.range[2 * unit + 1]) : 0.f;
     if (!(fmaxf(kabs, p.eps) * kthr <= (float)p.qmax * 0.9999f && vabs <= kVWideAbs * 0.999f)) {
       simt_item<__nv_bfloat16, BITS, D / 32, false>(p, i, h, false, pg0, pg1, slot, reinterpret_cast<float*>(buf));
+      if (p.done) finish_unit<D>(p, i, h);
       return;
     }
   }
@@ -991,7 +1079,6 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     for (int s = 0; s < slots && s < my_n; ++s) issue(s, s);
   }
   __syncwarp();
-
   // Pages are consumed in issue order; page k sits in slot k mod slots, and
   // bit t of ``phases`` is the parity slot t's barrier completes next.  Every
   // lane keeps the same counters; lane 0 issues the copies.
@@ -1087,6 +1174,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   }  // page path
   __syncthreads();  // every warp is done with its slots: reuse them for the merge
   write_partial<D, GP>(p, (int64_t)b * p.Hkv + h, slot, warp, gid, tig, st, buf);
+  if (p.done) finish_unit<D>(p, i, h);
 }
 
 // Decode attention over a dense bf16 Key/Value cache ([batch][Hkv][t_stride][D],

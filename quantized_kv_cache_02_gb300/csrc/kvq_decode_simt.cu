@@ -41,17 +41,11 @@ cudaError_t launch_bits(const DecodeParams& p, cudaStream_t s) {
 }
 
 constexpr int kCombineWarps = 4;
-constexpr int kCombineChunk = 8;  // slots whose loads are in flight together
 
-// Merge of the split partials (o[D], m, l) of one (sequence, query head):
-// M = max m_s, L = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M) / L
-// ("KV Cache 与自回归视频生成" section 05, FlashDecoding).  One warp per
-// (sequence, query head).  The slots are taken eight at a time: lane s reads
-// slot s's (m, l) while every lane reads its 16-byte pieces of the eight o
-// rows, so one round trip serves the whole chunk; the chunk is then folded
-// into the running (M, L, o) with the usual rescale.  VPL = 16-byte pieces of
-// o per lane (1 for head_dim <= 128, 2 up to 256).  A sequence without tokens
-// gets zeros.
+// Merge of the split partials (o[D], m, l) of one (sequence, query head) by
+// one warp each (merge_head), after a split launch that does not merge
+// inside itself (DecodeParams::done null).  A sequence without tokens gets
+// zeros.
 template <int VPL>
 __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const CombineParams p) {
   pdl_wait();
@@ -77,70 +71,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) combine_kernel(const Combi
     nslots = cost > 0 ? (int)(((s0 + cost) * N - 1) / C - ((s0 + 1) * N - 1) / C) + 1 : 0;
     nsplit = nslots;
   }
-  const int D = p.D, nvec = D >> 2;
   const int64_t unit = (int64_t)b * p.Hkv + h;
-  const int64_t stride = (int64_t)p.g * part_row(D);
-  const float* base = p.partials + unit * p.max_splits * stride + (int64_t)j * part_row(D);
-  // slot k < nsplit is split column k; the window's partial sits in the last column
-  auto row = [&](int k) { return base + (k < nsplit ? k : p.max_splits - 1) * stride; };
-
-  float M = -INFINITY, L = 0.f;
-  float4 o[VPL];
-#pragma unroll
-  for (int e = 0; e < VPL; ++e) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k0 = 0; k0 < nslots; k0 += kCombineChunk) {
-    const int n = min(kCombineChunk, nslots - k0);
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (lane < n) ml = __ldg(reinterpret_cast<const float2*>(row(k0 + lane) + D));
-    float4 v[kCombineChunk][VPL];
-#pragma unroll
-    for (int s = 0; s < kCombineChunk; ++s)
-#pragma unroll
-      for (int e = 0; e < VPL; ++e) {
-        const int c4 = lane + 32 * e;
-        v[s][e] = (s < n && c4 < nvec) ? __ldg(reinterpret_cast<const float4*>(row(k0 + s)) + c4)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    float cm = ml.x;
-#pragma unroll
-    for (int off = 4; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
-    cm = __shfl_sync(0xffffffffu, cm, 0);
-    const float Mn = fmaxf(M, cm);
-    const float Ms = Mn == -INFINITY ? 0.f : Mn;
-    const float corr = exp2f(M - Ms);
-    const float f = exp2f(ml.x - Ms);  // lanes >= n: 0
-    float ls = ml.y * f;
-#pragma unroll
-    for (int off = 4; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
-    L = fmaf(L, corr, __shfl_sync(0xffffffffu, ls, 0));
-#pragma unroll
-    for (int e = 0; e < VPL; ++e) {
-      o[e].x *= corr;
-      o[e].y *= corr;
-      o[e].z *= corr;
-      o[e].w *= corr;
-    }
-#pragma unroll
-    for (int s = 0; s < kCombineChunk; ++s) {
-      const float fs = __shfl_sync(0xffffffffu, f, s);
-#pragma unroll
-      for (int e = 0; e < VPL; ++e) {
-        o[e].x = fmaf(v[s][e].x, fs, o[e].x);
-        o[e].y = fmaf(v[s][e].y, fs, o[e].y);
-        o[e].z = fmaf(v[s][e].z, fs, o[e].z);
-        o[e].w = fmaf(v[s][e].w, fs, o[e].w);
-      }
-    }
-    M = Mn;
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  // the entry points accept only 16-byte aligned outputs
-  float4* out = reinterpret_cast<float4*>(p.out + ((int64_t)b * p.Hq + hq) * D);
-#pragma unroll
-  for (int e = 0; e < VPL; ++e) {
-    const int c4 = lane + 32 * e;
-    if (c4 < nvec) out[c4] = make_float4(o[e].x * inv, o[e].y * inv, o[e].z * inv, o[e].w * inv);
-  }
+  const int64_t stride = (int64_t)p.g * part_row(p.D);
+  const float* base = p.partials + unit * p.max_splits * stride + (int64_t)j * part_row(p.D);
+  merge_head<VPL, false>(base, nsplit, nslots, p.max_splits, stride, p.D, p.out + ((int64_t)b * p.Hq + hq) * p.D,
+                         lane);
 }
 
 }  // namespace

@@ -57,6 +57,7 @@ struct kvq_cache {
   size_t arena_bytes;
   int32_t* status;
   uint32_t* range;  // [batch][Hkv][2]: largest flushed Key / Value absmax (null: segmented)
+  uint32_t* done;   // [batch][Hkv]: finished split items of the running decode (null: segmented)
   kvq::SeqLayout* layout;
   uint8_t* pages;
   void* ring_k;
@@ -119,7 +120,7 @@ int rcap_of(const kvq_config* c) {
 }
 
 struct ArenaPlan {
-  size_t status, range, layout, table, pages, ring_k, ring_v, partials, total;
+  size_t status, range, done, layout, table, pages, ring_k, ring_v, partials, total;
   std::vector<int64_t> pages_cap, page_base;
   int max_splits, min_chunk_pages;
   int32_t table_stride;
@@ -154,6 +155,8 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int
   o = align_up(o + sizeof(int32_t), kAlign);
   a->range = o;
   o = align_up(o + units * 2 * sizeof(uint32_t), kAlign);
+  a->done = o;
+  o = align_up(o + units * sizeof(uint32_t), kAlign);
   a->layout = o;
   o = align_up(o + (size_t)c->batch * sizeof(kvq::SeqLayout), kAlign);
   a->table = o;
@@ -408,6 +411,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   c->arena_bytes = device_bytes;
   c->status = reinterpret_cast<int32_t*>(c->base + a.status);
   c->range = reinterpret_cast<uint32_t*>(c->base + a.range);
+  c->done = reinterpret_cast<uint32_t*>(c->base + a.done);
   c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + a.layout);
   c->table = c->paged ? reinterpret_cast<int32_t*>(c->base + a.table) : nullptr;
   c->pages = c->base + a.pages;
@@ -432,6 +436,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
     c->kmax = reinterpret_cast<uint32_t*>(c->base + sp.kmax);
     c->status = reinterpret_cast<int32_t*>(c->base + sp.status);
     c->range = nullptr;
+    c->done = nullptr;
     c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + sp.layout);
     c->pages = nullptr;
     c->ring_k = c->base + sp.ring_k;
@@ -449,6 +454,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, sizeof(int32_t));
   if (e == cudaSuccess && c->range)
     e = cudaMemset(c->range, 0, (size_t)cfg->batch * cfg->n_kv_heads * 2 * sizeof(uint32_t));
+  if (e == cudaSuccess && c->done) e = cudaMemset(c->done, 0, (size_t)cfg->batch * cfg->n_kv_heads * sizeof(uint32_t));
   if (e == cudaSuccess) {
     const size_t smem = kvq::flush_launch_smem(cfg->group, cfg->head_dim, esize_of(cfg));
     e = kvq::configure_append(cfg->dtype, c->bits, smem);
@@ -756,6 +762,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
   }
   struct Batch {
     int s0, n, chunk, grid, line_warps;
+    bool merged;  // the split launch merged its partials itself
     std::vector<int64_t> line_start;
   };
   std::vector<Batch> batches;
@@ -811,11 +818,27 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
         supported = 1;
       }
     }
+    bt.merged = false;
     if (supported) {
     } else if (use_tc) {
       e = kvq::launch_decode_tc(p, s, &supported);
       if (e == cudaSuccess && !supported) return fail(KVQ_EUNSUPPORTED, "tcgen05 kernel does not fit this configuration");
     } else if (use_mma) {
+      // A short decode (one wave of resident CTAs, items of at most 16
+      // 32-token units, as at batch 1) merges each unit's partials itself
+      // (its last finishing CTA), so no combine launch follows it: 10.7 us
+      // against 11.5 us a decode of a batch-1 4096-token layer.  Longer
+      // launches keep the combine kernel: there the arrival count holds every
+      // CTA's slot a little longer and the merges of many slots end the
+      // launch (measured slower on the 32 x 8 x 8192 layer and on the
+      // 432000-token layer).
+      const int64_t ctas = (int64_t)(bt.grid + 1) * bt.n * c->cfg.n_kv_heads;
+      const int64_t item_units = (int64_t)bt.chunk * (c->cfg.group / 32);
+      if (kvq::decode_mma_supported(p) && mma_slots > 0 && ctas <= mma_slots && item_units <= 16) {
+        p.done = c->done;
+        p.out = out;
+        bt.merged = c->done != nullptr;
+      }
       e = kvq::launch_decode_mma(p, s, &supported);
       if (e == cudaSuccess && !supported && kernel == 2)
         return fail(KVQ_EUNSUPPORTED, "tensor-core kernel does not fit this configuration (shared memory)");
@@ -830,6 +853,7 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
     if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   }
   for (const Batch& bt : batches) {
+    if (bt.merged) continue;
     kvq::CombineParams cp;
     memset(&cp, 0, sizeof cp);
     cp.D = c->cfg.head_dim;

@@ -169,6 +169,12 @@ struct DecodeParams {
   const void* q;               // [batch][Hq][D]
   const uint32_t* range;       // the flushed absmax maxima per unit (AppendParams::range)
   float* partials;             // [batch*Hkv][max_splits][g][part_row(D)]
+  // non-null (tensor-core split kernel only): the combine runs inside the
+  // split launch.  done[unit] counts the unit's finished items (0 between
+  // launches); the CTA that finishes last merges the unit's partials into
+  // out [batch][Hq][D] and sets the count back to 0
+  uint32_t* done;
+  float* out;
   int32_t max_splits;          // slots per unit; the window uses slot max_splits - 1
   int32_t chunk_pages;         // pages per quantized split
   int32_t grid_splits;         // quantized split columns in this launch (window column after)

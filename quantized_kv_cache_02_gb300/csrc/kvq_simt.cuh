@@ -377,6 +377,92 @@ __device__ inline void simt_item(const DecodeParams& p, int i, int h, bool win, 
   }
 }
 
+// Merge of one (sequence, query head)'s split partials by one warp:
+// M = max m_s, L = sum l_s 2^(m_s - M), o = sum o_s 2^(m_s - M) / L
+// ("KV Cache 与自回归视频生成" section 05, FlashDecoding).  base points at
+// the head's row in slot 0; slot k < nsplit is split column k, a later one
+// the window's (column max_splits - 1); rows are ``stride`` floats apart.
+// The slots are taken eight at a time: lane s reads slot s's (m, l) while
+// every lane reads its 16-byte pieces of the eight o rows, so one round trip
+// serves the whole chunk; the chunk is then folded into the running
+// (M, L, o) with the usual rescale.  VPL = 16-byte pieces of o per lane (1
+// for head_dim <= 128, 2 up to 256).  FRESH: the partials were written by
+// other CTAs of the running launch, so they are read from L2 (ld.global.cg),
+// never through a possibly stale L1 line.  No slots: zeros.
+template <int VPL, bool FRESH>
+__device__ __forceinline__ void merge_head(const float* base, int nsplit, int nslots, int max_splits, int64_t stride,
+                                           int D, float* out_row, int lane) {
+  // slots whose loads are in flight together: a whole warp's worth of (m, l)
+  // and as many o rows as registers allow, so a short decode's 17 or so
+  // slots take one round trip
+  constexpr int kCombineChunk = VPL == 1 ? (FRESH ? 24 : 32) : 16;
+  constexpr int kReduce = kCombineChunk > 16 ? 16 : kCombineChunk > 8 ? 8 : 4;  // first butterfly offset
+  const int nvec = D >> 2;
+  auto row = [&](int k) { return base + (k < nsplit ? k : max_splits - 1) * stride; };
+  auto ld2 = [](const float* q) {
+    return FRESH ? __ldcg(reinterpret_cast<const float2*>(q)) : __ldg(reinterpret_cast<const float2*>(q));
+  };
+  auto ld4 = [](const float* q, int c4) {
+    return FRESH ? __ldcg(reinterpret_cast<const float4*>(q) + c4) : __ldg(reinterpret_cast<const float4*>(q) + c4);
+  };
+  float M = -INFINITY, L = 0.f;
+  float4 o[VPL];
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) o[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k0 = 0; k0 < nslots; k0 += kCombineChunk) {
+    const int n = min(kCombineChunk, nslots - k0);
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < n) ml = ld2(row(k0 + lane) + D);
+    float4 v[kCombineChunk][VPL];
+#pragma unroll
+    for (int s = 0; s < kCombineChunk; ++s)
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) {
+        const int c4 = lane + 32 * e;
+        v[s][e] = (s < n && c4 < nvec) ? ld4(row(k0 + s), c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    float cm = ml.x;
+#pragma unroll
+    for (int off = kReduce; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, off));
+    cm = __shfl_sync(0xffffffffu, cm, 0);
+    const float Mn = fmaxf(M, cm);
+    const float Ms = Mn == -INFINITY ? 0.f : Mn;
+    const float corr = exp2f(M - Ms);
+    const float f = exp2f(ml.x - Ms);  // lanes >= n: 0
+    float ls = ml.y * f;
+#pragma unroll
+    for (int off = kReduce; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    L = fmaf(L, corr, __shfl_sync(0xffffffffu, ls, 0));
+#pragma unroll
+    for (int e = 0; e < VPL; ++e) {
+      o[e].x *= corr;
+      o[e].y *= corr;
+      o[e].z *= corr;
+      o[e].w *= corr;
+    }
+#pragma unroll
+    for (int s = 0; s < kCombineChunk; ++s) {
+      const float fs = __shfl_sync(0xffffffffu, f, s);
+#pragma unroll
+      for (int e = 0; e < VPL; ++e) {
+        o[e].x = fmaf(v[s][e].x, fs, o[e].x);
+        o[e].y = fmaf(v[s][e].y, fs, o[e].y);
+        o[e].z = fmaf(v[s][e].z, fs, o[e].z);
+        o[e].w = fmaf(v[s][e].w, fs, o[e].w);
+      }
+    }
+    M = Mn;
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  // the entry points accept only 16-byte aligned outputs
+  float4* out = reinterpret_cast<float4*>(out_row);
+#pragma unroll
+  for (int e = 0; e < VPL; ++e) {
+    const int c4 = lane + 32 * e;
+    if (c4 < nvec) out[c4] = make_float4(o[e].x * inv, o[e].y * inv, o[e].z * inv, o[e].w * inv);
+  }
+}
+
 // Which split item CTA (x, unit) of a decode launch handles.  Returns false if
 // the CTA has nothing to do.
 __device__ __forceinline__ bool split_item(const DecodeParams& p, int x, int i, bool* win, int* pg0,

@@ -107,3 +107,31 @@ def test_odd_chunks_tensor_cores(kvq, torch, G):
     plan picks for long staged units): each warp's run ends on a one-page group."""
     run_case(kvq, torch, [G * 9 + 50, G * 4 + 3, 130], 4, 16, 128, 128, G, 7, "bf16", kernels=(2, 4), seed=66,
              chunks=(0, 1, 3, 5, 7))
+
+
+@pytest.mark.parametrize("chunk", [0, 2, 8, 40])
+def test_in_launch_merge_and_combine_kernel(kvq, torch, chunk):
+    """A short decode (one wave, items of at most 16 pages: automatic, 2 and
+    8 pages an item) merges each unit's partials in its last finishing CTA; a
+    decode of 40-page items merges in the combine kernel.  Batch 3 with an
+    empty sequence, a window-only sequence and a 4096-token one, decoded
+    three times in a row (the arrival counts must come back to zero), each
+    against the oracle."""
+    H, Hq, D, R, G = 8, 32, 128, 128, 32
+    lens = [4096, 0, 77]
+    spec = gen.InputSpec(seed=67, n_kv_heads=H, n_q_heads=Hq, head_dim=D)
+    cache = kvq.KVQCache(len(lens), H, Hq, D, R, G, 7, [n + 8 for n in lens])
+    seqs = [O.GroupedSequence(H, D, R, G, 7) for _ in lens]
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().bfloat16()
+    for b, n in enumerate(lens):
+        if n:
+            k, v = spec.kv_block(0, [b], 0, n)
+            cache.append(dev(k), dev(v), b)
+            seqs[b].append(k[0], v[0])
+    for rep in range(3):
+        q = spec.q_block(0, range(len(lens)), rep)
+        out = cache.decode_attention(dev(q), kernel=2, chunk_pages=chunk).cpu().numpy()
+        assert not out[1].any(), "a sequence without tokens attends to zeros"
+        for b in (0, 2):
+            close(out[b], seqs[b].attend(q[b]), f"chunk {chunk} decode {rep} seq {b}")
+    assert cache.device_status() == 0
