@@ -471,9 +471,10 @@ def ragged_8bit_layer(torch, kvq, peak, steps=20):
 def segmented_layer(torch, kvq, w, dev, peak, batch=8, steps=10):
     """The segmented cache (the page's flush rule: each append's overflow is
     one segment) at the benchmark's head shape, 8 sequences of 8192 tokens:
-    one prefill segment, then one-token segments.  Its decode runs on the
-    CUDA-core kernel; a segment's Key scale row is stored once and each token
-    records the first token of its segment."""
+    one prefill segment, then one-token segments.  A segment's Key scale row
+    is stored once and each token records the first token of its segment; the
+    decode runs on the tensor-core kernel in 32-token tiles (the tile of the
+    one-token segments on the CUDA cores inside the same launch)."""
     H, Hq, D, R = w["n_kv_heads"], w["n_q_heads"], w["head_dim"], w["residual_len"]
     T0 = w["context"]
     cache = kvq.KVQCache(batch, H, Hq, D, R, w["group"], w["qmax"], T0 + 3 + steps + 8, segmented=True)

@@ -123,7 +123,8 @@ typedef struct kvq_unit_view {
 typedef struct kvq_decode_opts {
   int32_t kernel;      /* 0 = automatic; 1 = CUDA-core kernel (any supported
                           shape); 2 = tensor-core kernel on mma.sync (bf16,
-                          head_dim 64/128, G a multiple of 32); 3 = tcgen05
+                          head_dim 64/128, G a multiple of 32, or a
+                          segmented cache with 4-bit codes); 3 = tcgen05
                           tensor-core kernel (bf16, head_dim 128, 4-bit codes,
                           G a multiple of 32; it handles the input range per
                           block of 128 tokens: groups with a Key scale below
@@ -148,7 +149,8 @@ typedef struct kvq_decode_opts {
                           waves of its resident CTAs.  Else quantized groups
                           per split item.  Results agree for any choice within
                           the attention tolerance (the summation order of the
-                          splits differs). */
+                          splits differs).  A segmented cache counts tokens
+                          and rounds the chunk up to a multiple of 128. */
   void* split_start;   /* optional cudaEvent_t recorded just before the split kernel */
   void* split_stop;    /* optional cudaEvent_t recorded just after it */
 } kvq_decode_opts;
@@ -237,7 +239,12 @@ kvq_status kvq_create_paged(const kvq_config* cfg, const int64_t* capacity_per_s
  * Keys and Values alike), each segment's Key scales (head_dim fp32) in the
  * row of its first token, each token's Value scale, per sequence the first
  * token of each token's segment (int32), and a window ring of R rows.  Decode
- * attention runs on the CUDA-core kernel; kvq_export_unit returns one Key
+ * attention (bf16, head_dim 64/128, 4-bit codes, >= 2 query heads per KV
+ * head; else the CUDA-core kernel) runs on the tensor-core kernel in 32-token
+ * tiles: a tile inside one segment shares one Key scale row, as a group page
+ * does; a tile that holds a segment boundary (as every tile of one-token
+ * segments does) or the unit's last, partial tile is scored on the CUDA cores
+ * inside the same launch.  kvq_export_unit returns one Key
  * scale row per segment; kvq_export_pages returns KVQ_EUNSUPPORTED; the other
  * calls work as on a grouped cache.  Arguments as kvq_required_bytes /
  * kvq_create. */

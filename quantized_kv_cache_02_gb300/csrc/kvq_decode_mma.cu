@@ -22,8 +22,9 @@ cudaError_t launch_decode_dense(const DecodeParams& p, cudaStream_t s, int* supp
 }
 
 bool decode_mma_supported(const DecodeParams& p) {
-  return (p.D == 64 || p.D == 128) && (p.G % 32 == 0) && p.g >= 2 && p.g <= kMaxGqa &&
-         decode_mma_smem_bytes(p) <= kMaxSmem;
+  // a segmented cache: 4-bit codes, split items of whole 32-token tiles
+  const bool tiles = p.seg.kcodes ? p.bits == 4 && p.chunk_pages % 32 == 0 : p.G % 32 == 0;
+  return (p.D == 64 || p.D == 128) && tiles && p.g >= 2 && p.g <= kMaxGqa && decode_mma_smem_bytes(p) <= kMaxSmem;
 }
 
 int decode_mma_resident_per_sm(const DecodeParams& p) {

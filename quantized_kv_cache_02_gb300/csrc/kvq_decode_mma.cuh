@@ -344,8 +344,14 @@ struct WarpState {
 };
 
 // A group of PB pages (FULL) or of npages < PB pages (the tail of a warp's
-// run), already in shared memory.
-template <int D, int BITS, int GP, bool FULL>
+// run), already in shared memory.  TOKV (4-bit only): the pages are 32-token
+// tiles of a segmented cache, whose Value codes are token-major rows like the
+// Key rows.  Their Value A operand pairs two tokens of one channel from two
+// rows with a byte permute; lane (gid, tig) takes the channels
+// [gid D/8, (gid + 1) D/8) (O'^T row gid of m-tile mt is channel
+// gid D/8 + 2 mt, row gid + 8 the next one, whose odd nibble comes x16) and
+// the tokens 8 tig .. 8 tig + 7 that its P columns hold.
+template <int D, int BITS, int GP, bool FULL, bool TOKV = false>
 __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BITS, GP>::PB], int npages_rt,
                                           const PageGeom& geom, int G, const float4* q4, float* rsc, int lane,
                                           int gid, int tig, WarpState<D>& st) {
@@ -429,7 +435,8 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
   // A operand of the p/sV counter: the value 1 (or 16 on the x16 k-slots) in
   // every element, as 2^-24-scaled subnormals like the codes
   constexpr uint32_t kOneLo = 0x00010001u;
-  constexpr uint32_t kOneHi = BITS == 4 ? 0x00100010u : 0x00010001u;
+  constexpr uint32_t kOneHi = BITS == 4 && !TOKV ? 0x00100010u : 0x00010001u;
+  static_assert(!TOKV || BITS == 4, "token-major Value codes: 4-bit only");
 
   for (int sub = 0; sub < G / 32; ++sub) {
     // ---- scores of every page; keep each column's own page ------------------
@@ -569,7 +576,7 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
       // undo the code's position factor: 4-bit x16 on the second row of each
       // pair; 2-bit x1, x4 (m-block 0) and x16, x64 (m-block 1)
       const float f0 = BITS == 2 ? (mb == 0 ? 1.f : 0.0625f) : 1.f;
-      const float f1 = BITS == 2 ? (mb == 0 ? 0.25f : 0.015625f) : BITS == 4 ? 0.0625f : 1.f;
+      const float f1 = BITS == 2 ? (mb == 0 ? 0.25f : 0.015625f) : BITS == 4 && !TOKV ? 0.0625f : 1.f;
       const float i0 = fast_rcp(vscale[r0]) * f0;
       const float i1 = fast_rcp(vscale[r0 + kGap]) * f1;
       pk[mb][0] = pack_f16x2(pr[mb][0] * i0, pr[mb][1] * i0);
@@ -589,6 +596,44 @@ __device__ __forceinline__ void mma_group(const uint8_t* const (&pg)[Shape<D, BI
         if (BITS != 2) mma16816(st.C, kOneLo, kOneLo, kOneHi, kOneHi, bp[mb][0], bp[mb][1]);
       }
       const uint8_t* vc = pg[j] + geom.code_bytes + sub * S::kSubBytes;
+      if constexpr (TOKV) {
+        // this lane's D/16 bytes (channels gid D/8 ..) of token rows 8 tig + r,
+        // one 32-bit word of each row at a time (four m-tiles).  Lanes of odd
+        // tig load each pair of rows the other way round (w[2i] = row 2i + 1),
+        // so the four tig lanes of a gid fall on two banks, not one; their P
+        // halves are swapped to match (same dot products).
+        constexpr int kLaneBytes = D / 16;
+        const uint8_t* vrow = vc + 8 * tig * S::kRowBytes + gid * kLaneBytes;
+        const int rflip = tig & 1;
+        uint32_t bq[2][2];
+#pragma unroll
+        for (int mb = 0; mb < 2; ++mb) {
+          bq[mb][0] = __byte_perm(bp[mb][0], 0u, rflip ? 0x1032u : 0x3210u);
+          bq[mb][1] = __byte_perm(bp[mb][1], 0u, rflip ? 0x1032u : 0x3210u);
+        }
+#pragma unroll
+        for (int wd = 0; wd < kLaneBytes / 4; ++wd) {
+          uint32_t w[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r)
+            w[r] = *reinterpret_cast<const uint32_t*>(vrow + (r ^ rflip) * S::kRowBytes + 4 * wd);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const int mt = 4 * wd + m;
+            // bytes (m of row a, m of row a, m of row b, m of row b): the low
+            // nibbles are channel 2 mt of tokens a, b, the high ones channel 2 mt + 1
+            constexpr uint32_t kSel[4] = {0x4400u, 0x5511u, 0x6622u, 0x7733u};
+#pragma unroll
+            for (int mb = 0; mb < 2; ++mb) {
+              const uint32_t x01 = __byte_perm(w[4 * mb], w[4 * mb + 1], kSel[m]);
+              const uint32_t x23 = __byte_perm(w[4 * mb + 2], w[4 * mb + 3], kSel[m]);
+              mma16816(st.O[mt], x01 & 0x000F000Fu, x01 & 0x00F000F0u, x23 & 0x000F000Fu, x23 & 0x00F000F0u,
+                       bq[mb][0], bq[mb][1]);
+            }
+          }
+        }
+        continue;
+      }
 #pragma unroll
       for (int mt = 0; mt < S::kSteps; ++mt) {
         const int c_lo = 16 * mt + gid, c_hi = c_lo + 8;
@@ -786,9 +831,11 @@ __device__ __forceinline__ void merge_streams(WarpState<D>& st, int off) {
 // Fold the four warps' (m, l, O) of the stream-0 columns into one partial
 // (o = sum O, m, l per query head) of slot ``slot`` of ``unit``.  ``buf`` is
 // shared memory no warp still reads (kMmaWarps * kMaxGqa * (D + 2) floats).
+// tokv: O'^T rows hold the channels of mma_group's token-major Value path.
 template <int D, int GP>
 __device__ __forceinline__ void write_partial(const DecodeParams& p, int64_t unit, int slot, int warp,
-                                              int gid, int tig, const WarpState<D>& st, uint8_t* buf) {
+                                              int gid, int tig, const WarpState<D>& st, uint8_t* buf,
+                                              bool tokv = false) {
   const int g = p.g;
 
   float* mrg = reinterpret_cast<float*>(buf);  // [kMmaWarps][kMaxGqa][D + 2]
@@ -797,14 +844,15 @@ __device__ __forceinline__ void write_partial(const DecodeParams& p, int64_t uni
   const bool stream0 = 2 * tig < GP && warp < kMmaWarps;  // a fifth (control) warp holds no rows
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
-    const int c_lo = 16 * mt + gid;
+    const int c_lo = tokv ? gid * (D / 8) + 2 * mt : 16 * mt + gid;
+    const int c_hi = tokv ? c_lo + 1 : c_lo + 8;
     if (stream0 && hd0 < g) {
       mw[hd0 * (D + 2) + c_lo] = st.O[mt][0];
-      mw[hd0 * (D + 2) + c_lo + 8] = st.O[mt][2];
+      mw[hd0 * (D + 2) + c_hi] = st.O[mt][2];
     }
     if (stream0 && hd1 < g) {
       mw[hd1 * (D + 2) + c_lo] = st.O[mt][1];
-      mw[hd1 * (D + 2) + c_lo + 8] = st.O[mt][3];
+      mw[hd1 * (D + 2) + c_hi] = st.O[mt][3];
     }
   }
   if (gid == 0 && stream0) {
@@ -848,8 +896,131 @@ template <int D, int NBUF>
 constexpr int kRowsBuf = NBUF * 32 * D * 2;
 
 // Page modes of the split kernel: contiguous pages of G = 32, paged pages of
-// G = 32, and any larger G (either map) staged in 32-token units.
-constexpr int kFlat32 = 0, kPaged32 = 1, kStaged = 2;
+// G = 32, any larger G (either map) staged in 32-token units, and the
+// 32-token tiles of a segmented cache (4-bit; token-major Value rows).
+constexpr int kFlat32 = 0, kPaged32 = 1, kStaged = 2, kSeg32 = 3;
+
+// A tile of a segmented cache that the tensor cores cannot take: its tokens
+// span more than one segment (so more than one Key scale row), or it is the
+// unit's last, partial tile (nvalid < 32 tokens).  Its tokens go through the
+// CUDA cores in fp32: lane r scores token t0 + r against every head with its
+// own segment's Key scale row; the warp then folds the tile into stream 0 of
+// the tensor-core state (mma_group, token-major Value path): the same lazy
+// running max (moved only past 2^8), l, and O' -- unbiased codes x 2^-24, x16
+// on the odd-channel rows, so the bias counter C takes nothing.  pw: 32 x GP
+// floats of this warp's shared memory.
+template <int D, int GP>
+__device__ __noinline__ void seg_tile_cuda_cores(const DecodeParams& p, const uint8_t* tile, int64_t unit_row,
+                                                 const int32_t* first, int t0, int nvalid, const float4* q4,
+                                                 float* pw, WarpState<D>& st, int lane) {
+  using S = Shape<D, 4, GP>;
+  constexpr float kTwo24i = 1.f / 16777216.f;
+  constexpr float kSlack = 8.f;  // as mma_group's lazy rescaling
+  const PageGeom ug = make_geom(32, D, 4);
+  const int gid = lane >> 2, tig = lane & 3;
+  const float* qf = reinterpret_cast<const float*>(q4);
+  // ---- scores of token t0 + lane, every head (base 2, q pre-scaled)
+  float sc[GP];
+#pragma unroll
+  for (int n = 0; n < GP; ++n) sc[n] = -INFINITY;
+  if (lane < nvalid) {
+    const float4* ks = reinterpret_cast<const float4*>(p.seg.kscales + (unit_row + first[t0 + lane]) * D);
+    const uint32_t* kr = reinterpret_cast<const uint32_t*>(tile + lane * S::kRowBytes);
+#pragma unroll
+    for (int n = 0; n < GP; ++n) sc[n] = 0.f;
+    for (int w8 = 0; w8 < D / 8; ++w8) {
+      const uint32_t w = kr[w8];
+      const float4 sa = __ldg(ks + 2 * w8), sb = __ldg(ks + 2 * w8 + 1);
+      const float sk[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int c = 8 * w8 + e;
+        const float kv = (float)((int)((w >> (4 * e)) & 0xFu) - 8) * fast_rcp(fmaxf(sk[e], p.eps));
+        const int tg = c / S::kChan, i4 = (c - tg * S::kChan) >> 2;
+#pragma unroll
+        for (int n = 0; n < GP; ++n) sc[n] = fmaf(qf[((i4 * GP + n) * 4 + tg) * 4 + (c & 3)], kv, sc[n]);
+      }
+    }
+  }
+  // ---- per-head maxima; the lazy max of this thread's stream-0 columns
+  float mx[GP];
+#pragma unroll
+  for (int n = 0; n < GP; ++n) {
+    mx[n] = sc[n];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx[n] = fmaxf(mx[n], __shfl_xor_sync(0xffffffffu, mx[n], off));
+  }
+  const bool own = 2 * tig < GP;  // this thread's columns are stream 0's heads 2 tig, 2 tig + 1
+  float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+  for (int n = 0; n < GP; n += 2)
+    if (2 * tig == n) {
+      mxa = mx[n];
+      mxb = mx[n + 1];
+    }
+  if (own && mxa > st.m0 + kSlack) {
+    const float mn = fmaxf(st.m0, mxa), a = st.m0 == -INFINITY ? 0.f : fast_exp2(st.m0 - mn);
+    st.m0 = mn;
+    st.l0 *= a;
+    st.C[0] *= a;
+    st.C[2] *= a;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.O[mt][0] *= a;
+      st.O[mt][2] *= a;
+    }
+  }
+  if (own && mxb > st.m1 + kSlack) {
+    const float mn = fmaxf(st.m1, mxb), a = st.m1 == -INFINITY ? 0.f : fast_exp2(st.m1 - mn);
+    st.m1 = mn;
+    st.l1 *= a;
+    st.C[1] *= a;
+    st.C[3] *= a;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      st.O[mt][1] *= a;
+      st.O[mt][3] *= a;
+    }
+  }
+  // ---- weights p = 2^(s - m) of token lane, head n (column n's m sits in lane n / 2)
+#pragma unroll
+  for (int n = 0; n < GP; ++n) {
+    const float m = __shfl_sync(0xffffffffu, (n & 1) ? st.m1 : st.m0, n >> 1);
+    const float pv = lane < nvalid ? fast_exp2(sc[n] - m) : 0.f;
+    pw[lane * GP + n] = pv;
+    float ls = pv;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ls += __shfl_xor_sync(0xffffffffu, ls, off);
+    // l is summed over a column's rows (gid) at the end: count it once
+    if (gid == 0 && 2 * tig == n) st.l0 += ls;
+    if (gid == 0 && 2 * tig + 1 == n) st.l1 += ls;
+  }
+  __syncwarp();
+  // ---- O'^T += V^T p / sV on this thread's channels and columns
+  if (own) {
+    const float* vscale = reinterpret_cast<const float*>(tile + ug.vscale_off);
+    const uint8_t* vrows = tile + ug.code_bytes + gid * (D / 16);
+    for (int r = 0; r < nvalid; ++r) {
+      const float iv = fast_rcp(vscale[r]) * kTwo24i;
+      const float w0 = pw[r * GP + 2 * tig] * iv, w1 = pw[r * GP + 2 * tig + 1] * iv;
+#pragma unroll
+      for (int wd = 0; wd < D / 64; ++wd) {
+        const uint32_t word = *reinterpret_cast<const uint32_t*>(vrows + r * S::kRowBytes + 4 * wd);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int mt = 4 * wd + m;
+          const float vlo = (float)((int)((word >> (8 * m)) & 0xFu) - 8);
+          const float vhi = 16.f * (float)((int)((word >> (8 * m + 4)) & 0xFu) - 8);
+          st.O[mt][0] = fmaf(vlo, w0, st.O[mt][0]);
+          st.O[mt][1] = fmaf(vlo, w1, st.O[mt][1]);
+          st.O[mt][2] = fmaf(vhi, w0, st.O[mt][2]);
+          st.O[mt][3] = fmaf(vhi, w1, st.O[mt][3]);
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
 
 // A short split item (a few pages a warp, as at batch 1) spends most of its
 // time waiting: its first copies are issued only after the query set-up,
@@ -967,7 +1138,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   // as a G = 32 page, so shared memory and the math do not depend on G.
   const PageGeom geom = p.geom;                                      // a stored page
   const int upp = MODE == kStaged ? p.G / 32 : 1;                    // units per page
-  const PageGeom ug = MODE == kStaged ? make_geom(32, D, BITS) : geom;  // a staged unit
+  const PageGeom ug = MODE == kStaged || MODE == kSeg32 ? make_geom(32, D, BITS) : geom;  // a staged unit
   const uint32_t page_bytes = (uint32_t)ug.page_bytes;              // bytes of a slot
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
   float* scratch = reinterpret_cast<float*>(smem + 128 * ((kMmaWarps * slots * 8 + 127) / 128));
@@ -1040,7 +1211,8 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     const int qexp = float_exp2i(qa);
     const float kthr = fmaxf(pow2i(BITS == 2 ? qexp + 1 + 4 - 14 : qexp + 1 - 9), p.eps);
     if (!(fmaxf(kabs, p.eps) * kthr <= (float)p.qmax * 0.9999f && vabs <= kVWideAbs * 0.999f)) {
-      simt_item<__nv_bfloat16, BITS, D / 32, false>(p, i, h, false, pg0, pg1, slot, reinterpret_cast<float*>(buf));
+      simt_item<__nv_bfloat16, BITS, D / 32, MODE == kSeg32>(p, i, h, false, pg0, pg1, slot,
+                                                            reinterpret_cast<float*>(buf));
       if (p.done) finish_unit<D>(p, i, h);
       return;
     }
@@ -1054,11 +1226,45 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     return MODE == kFlat32 ? unit_pages + (int64_t)pg * stored : p.pages + page_offset(p.map, stored, b, h, pg);
   };
   auto src_of = [&](int pos) { return page_src(pg0 + warp + pos * kMmaWarps); };  // G = 32
-  // the copies of unit pos into slot s (lane 0)
-  auto issue = [&](int pos, int s) {
+  const int npg = MODE == kSeg32 ? (pg1 - pg0 + 31) / 32 : (pg1 - pg0) * upp;  // units of this CTA
+  const int my_n = warp < npg ? (npg - warp + kMmaWarps - 1) / kMmaWarps : 0;
+  // segmented cache: the warp's tiles pg0 / 32 + warp + 4 pos; per tile the
+  // first token of its first token's segment (whose row holds the segment's
+  // Key scales) and whether every token is in that segment and below Q,
+  // loaded by the lanes for 32 positions at a time (lane k: position
+  // seg_base + k); lane 0 marks each slot's tile (seg_flag) as it issues it
+  const int64_t unit_row = ((int64_t)b * p.Hkv + h) * p.seg.cap;
+  const int32_t* seg_first = MODE == kSeg32 ? p.seg.first + (int64_t)b * p.seg.cap : nullptr;
+  const int Qseg = p.ctr[i].quantized;
+  int seg_base = -64, seg_f = 0;
+  bool seg_u = false;
+  uint8_t* seg_flag = my_buf + (size_t)(kMmaWarps - warp) * slots * page_bytes + (size_t)warp * 8;
+  float* seg_pw = reinterpret_cast<float*>(my_buf + (size_t)(kMmaWarps - warp) * slots * page_bytes + 32) +
+                  warp * 32 * GP;
+  auto seg_tile = [&](int pos) { return pg0 / 32 + warp + pos * kMmaWarps; };
+  auto seg_load = [&](int pos) {  // all lanes: the 32 positions from pos's block
+    seg_base = pos & ~31;
+    const int t = seg_tile(seg_base + lane);
+    seg_f = 0;
+    seg_u = false;
+    if (seg_base + lane < my_n) {
+      seg_f = seg_first[32 * t];
+      seg_u = 32 * t + 31 < Qseg && seg_first[32 * t + 31] == seg_f;
+    }
+  };
+  // the copies of unit pos into slot s (lane 0); f, u: its tile's scale row and mark (segmented)
+  auto issue = [&](int pos, int s, int f, bool u) {
     const uint32_t bar = my_bar + 8 * s, dst = smem_addr(my_buf + (size_t)s * page_bytes);
+    if constexpr (MODE == kSeg32) seg_flag[s] = u ? 1 : 0;
     mbar_expect_tx(bar, page_bytes);
-    if constexpr (MODE != kStaged) {
+    if constexpr (MODE == kSeg32) {
+      const int64_t row = unit_row + 32 * (int64_t)seg_tile(pos);
+      const int rb = S::kRowBytes;
+      bulk_load(dst, p.seg.kcodes + row * rb, 32 * rb, bar);
+      bulk_load(dst + (uint32_t)ug.code_bytes, p.seg.vcodes + row * rb, 32 * rb, bar);
+      bulk_load(dst + (uint32_t)ug.kscale_off, p.seg.kscales + (unit_row + f) * D, 4 * D, bar);
+      bulk_load(dst + (uint32_t)ug.vscale_off, p.seg.vscales + row, 128, bar);
+    } else if constexpr (MODE != kStaged) {
       bulk_load(dst, src_of(pos), page_bytes, bar);
     } else {
       const int u = pg0 * upp + warp + pos * kMmaWarps;
@@ -1070,13 +1276,20 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
       bulk_load(dst + (uint32_t)ug.vscale_off, src + geom.vscale_off + 128 * sub, 128, bar);
     }
   };
-  const int npg = (pg1 - pg0) * upp;  // units of this CTA
-  const int my_n = warp < npg ? (npg - warp + kMmaWarps - 1) / kMmaWarps : 0;
+  if (MODE == kSeg32) seg_load(0);
   if (lane == 0) {
     for (int s = 0; s < slots; ++s) mbar_init(my_bar + 8 * s, 1);
     fence_mbar_init();
     fence_proxy_async();
-    for (int s = 0; s < slots && s < my_n; ++s) issue(s, s);
+  }
+  for (int s = 0; s < slots && s < my_n; ++s) {
+    int f = 0;
+    bool u = false;
+    if (MODE == kSeg32) {
+      f = __shfl_sync(0xffffffffu, seg_f, s);
+      u = __shfl_sync(0xffffffffu, seg_u, s);
+    }
+    if (lane == 0) issue(s, s, f, u);
   }
   __syncwarp();
   // Pages are consumed in issue order; page k sits in slot k mod slots, and
@@ -1108,20 +1321,59 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
       }
     }
     if (!ok) break;
-    if (np == S::PB)
+    if constexpr (MODE == kSeg32) {
+      if constexpr (BITS == 4) {
+        bool all = true;
+#pragma unroll
+        for (int j = 0; j < S::PB; ++j)
+          if (j < np) all = all && seg_flag[sl[j]] != 0;
+        if (all && np == S::PB) {
+          mma_group<D, BITS, GP, true, true>(pgs, np, ug, 32, q4, my_rsc, lane, gid, tig, st);
+        } else if (all) {
+          mma_group<D, BITS, GP, false, true>(pgs, np, ug, 32, q4, my_rsc, lane, gid, tig, st);
+        } else {
+#pragma unroll
+          for (int j = 0; j < S::PB; ++j) {
+            if (j >= np) break;
+            if (seg_flag[sl[j]]) {
+              const uint8_t* one[S::PB];
+#pragma unroll
+              for (int jj = 0; jj < S::PB; ++jj) one[jj] = pgs[j];
+              mma_group<D, BITS, GP, false, true>(one, 1, ug, 32, q4, my_rsc, lane, gid, tig, st);
+            } else {
+              const int t0 = 32 * seg_tile(k + j);
+              seg_tile_cuda_cores<D, GP>(p, pgs[j], unit_row, seg_first, t0, min(32, Qseg - t0), q4, seg_pw, st,
+                                         lane);
+            }
+            __syncwarp();
+          }
+        }
+      }
+    } else if (np == S::PB) {
       mma_group<D, BITS, GP, true>(pgs, np, ug, MODE == kStaged ? p.G / upp : p.G, q4, my_rsc, lane, gid, tig, st);
-    else
+    } else {
       mma_group<D, BITS, GP, false>(pgs, np, ug, MODE == kStaged ? p.G / upp : p.G, q4, my_rsc, lane, gid, tig, st);
+    }
     __syncwarp();
     // refill the freed slots with the next pages of this warp's run
     const int refill = min(np, my_n - issued);
+    int seg_fs[S::PB];
+    bool seg_us[S::PB];
+    if (MODE == kSeg32) {
+#pragma unroll
+      for (int j = 0; j < S::PB; ++j) {
+        if (j < refill && issued + j >= seg_base + 32) seg_load(issued + j);
+        seg_fs[j] = __shfl_sync(0xffffffffu, seg_f, (issued + j) & 31);
+        seg_us[j] = __shfl_sync(0xffffffffu, seg_u, (issued + j) & 31);
+      }
+    }
     if (lane == 0 && refill > 0) {
       fence_proxy_async();
 #pragma unroll
       for (int j = 0; j < S::PB; ++j) {
         if (j < refill) {
           if (MODE != kFlat32) {
-            issue(issued + j, sl[j]);
+            issue(issued + j, sl[j], MODE == kSeg32 ? seg_fs[j] : 0, MODE == kSeg32 ? seg_us[j] : false);
           } else {
             mbar_expect_tx(my_bar + 8 * sl[j], page_bytes);
             bulk_load(smem_addr(my_buf + (size_t)sl[j] * page_bytes), next_src + (int64_t)j * kMmaWarps * page_bytes,
@@ -1160,12 +1412,14 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     // carries the full sum), so the bias term is bias * 2^24 * C
     constexpr float kTwo24 = 16777216.f;
     const float c0 = S::kBias * kTwo24 * st.C[0], c1 = S::kBias * kTwo24 * st.C[1];
+    // (segmented tiles: the second row of each m-tile, an odd channel, came x16)
+    constexpr float kTwo24hi = MODE == kSeg32 ? kTwo24 / 16.f : kTwo24;
 #pragma unroll
     for (int mt = 0; mt < D / 16; ++mt) {
       st.O[mt][0] = fmaf(st.O[mt][0], kTwo24, -c0);
       st.O[mt][1] = fmaf(st.O[mt][1], kTwo24, -c1);
-      st.O[mt][2] = fmaf(st.O[mt][2], kTwo24, -c0);
-      st.O[mt][3] = fmaf(st.O[mt][3], kTwo24, -c1);
+      st.O[mt][2] = fmaf(st.O[mt][2], kTwo24hi, -c0);
+      st.O[mt][3] = fmaf(st.O[mt][3], kTwo24hi, -c1);
     }
   }
   // fold the page streams onto stream 0 (columns 0 .. GP-1)
@@ -1173,7 +1427,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   for (int off = GP / 2; off < 4; off <<= 1) merge_streams<D>(st, off);
   }  // page path
   __syncthreads();  // every warp is done with its slots: reuse them for the merge
-  write_partial<D, GP>(p, (int64_t)b * p.Hkv + h, slot, warp, gid, tig, st, buf);
+  write_partial<D, GP>(p, (int64_t)b * p.Hkv + h, slot, warp, gid, tig, st, buf, MODE == kSeg32 && !win);
   if (p.done) finish_unit<D>(p, i, h);
 }
 
@@ -1270,6 +1524,8 @@ template <int D>
 size_t smem_for(const DecodeParams& p) {
   const int slots = mma_slots(unit_bytes(p), p.g);
   size_t pages = (size_t)kMmaWarps * slots * unit_bytes(p);
+  // segmented tiles: each warp's slot marks (8 bytes) and CUDA-core weights
+  if (p.seg.kcodes) pages += 32 + (size_t)kMmaWarps * 32 * gqa_pad(p.g) * sizeof(float);
   const size_t merge = (size_t)kMmaWarps * kMaxGqa * (D + 2) * sizeof(float);
   const size_t window = (size_t)kMmaWarps * kRowsBuf<D, 2>;
   if (pages < merge) pages = merge;
@@ -1322,6 +1578,8 @@ template <int D, int BITS>
 int resident_g(const DecodeParams& p) {
   auto pick = [&](auto gp) {
     constexpr int GP = decltype(gp)::value;
+    if constexpr (BITS == 4)
+      if (p.seg.kcodes) return resident_t<D, BITS, GP, kSeg32>(p);
     if (p.G != 32) return resident_t<D, BITS, GP, kStaged>(p);
     return p.map.table ? resident_t<D, BITS, GP, kPaged32>(p) : resident_t<D, BITS, GP, kFlat32>(p);
   };
@@ -1344,6 +1602,8 @@ cudaError_t launch_t(const DecodeParams& p, cudaStream_t s) {
 
 template <int D, int BITS, int GP>
 cudaError_t launch_m(const DecodeParams& p, cudaStream_t s) {
+  if constexpr (BITS == 4)
+    if (p.seg.kcodes) return launch_t<D, BITS, GP, kSeg32>(p, s);
   if (p.G != 32) return launch_t<D, BITS, GP, kStaged>(p, s);
   return p.map.table ? launch_t<D, BITS, GP, kPaged32>(p, s) : launch_t<D, BITS, GP, kFlat32>(p, s);
 }

@@ -178,7 +178,7 @@ kvq_status plan_arena(const kvq_config* c, const int64_t* cap, ArenaPlan* a, int
 // for capacity_max tokens per unit, the segment maxima, rings of R rows and
 // the split partials.
 struct SegPlan {
-  size_t status, layout, kcodes, vcodes, kscales, vscales, first, kmax, ring_k, ring_v, partials, total;
+  size_t status, range, layout, kcodes, vcodes, kscales, vscales, first, kmax, ring_k, ring_v, partials, total;
   int64_t cap;
   int max_splits;
 };
@@ -191,14 +191,18 @@ kvq_status plan_arena_seg(const kvq_config* c, const int64_t* cap, SegPlan* a) {
       return fail(KVQ_EINVAL, "capacity of sequence %d must be in [1, 2^31) (got %lld)", b, (long long)cap[b]);
     cmax = std::max(cmax, cap[b]);
   }
-  a->cap = cmax;
+  // rows of 32 tokens start on 16-byte boundaries in every per-unit array
+  // (the tensor-core kernel copies them whole)
+  a->cap = (cmax + 31) / 32 * 32;
   a->max_splits = (int)((cmax + kMinChunkTokens - 1) / kMinChunkTokens) + 1;
   const size_t units = (size_t)c->batch * c->n_kv_heads, D = c->head_dim;
-  const size_t rows = units * (size_t)cmax;
+  const size_t rows = units * (size_t)a->cap;
   const int g = c->n_q_heads / c->n_kv_heads;
   size_t o = 0;
   a->status = o;
   o = align_up(o + sizeof(int32_t), kAlign);
+  a->range = o;
+  o = align_up(o + units * 2 * sizeof(uint32_t), kAlign);
   a->layout = o;
   o = align_up(o + (size_t)c->batch * sizeof(kvq::SeqLayout), kAlign);
   a->kcodes = o;
@@ -210,7 +214,7 @@ kvq_status plan_arena_seg(const kvq_config* c, const int64_t* cap, SegPlan* a) {
   a->vscales = o;
   o = align_up(o + rows * sizeof(float), kAlign);
   a->first = o;
-  o = align_up(o + (size_t)c->batch * (size_t)cmax * sizeof(int32_t), kAlign);
+  o = align_up(o + (size_t)c->batch * (size_t)a->cap * sizeof(int32_t), kAlign);
   a->kmax = o;
   o = align_up(o + units * D * sizeof(uint32_t), kAlign);
   const size_t ring = units * (size_t)c->residual_len * D * esize_of(c);
@@ -287,6 +291,9 @@ void plan_splits(const kvq_cache* c, int s0, int n, int requested, int slots, in
   // larger G is split into 32-token units, four warps' worth per page or more,
   // so any chunk keeps the warps even there.
   if (requested <= 0 && ch > 8 && c->cfg.group == 32) ch = (ch + 7) / 8 * 8;
+  // a segmented cache's tokens go to the tensor-core kernel in 32-token
+  // tiles, four warps' worth an item (the CUDA-core kernel takes any chunk)
+  if (c->segmented) ch = (ch + 127) / 128 * 128;
   *chunk = (int)ch;
   *grid_splits = (int)((pmax + ch - 1) / ch);
 }
@@ -435,7 +442,7 @@ kvq_status create(const kvq_config* cfg, const int64_t* capacity_per_seq, int64_
     c->seg.row_bytes = cfg->head_dim * c->bits / 8;
     c->kmax = reinterpret_cast<uint32_t*>(c->base + sp.kmax);
     c->status = reinterpret_cast<int32_t*>(c->base + sp.status);
-    c->range = nullptr;
+    c->range = reinterpret_cast<uint32_t*>(c->base + sp.range);
     c->done = nullptr;
     c->layout = reinterpret_cast<kvq::SeqLayout*>(c->base + sp.layout);
     c->pages = nullptr;
@@ -487,6 +494,7 @@ kvq_status append_segmented(kvq_cache* c, const void* new_k, const void* new_v, 
     p.eps = c->cfg.eps;
     p.seg = c->seg;
     p.kmax = c->kmax;
+    p.range = c->range;
     p.ring_k = p.ring_k_out = c->ring_k;
     p.ring_v = p.ring_v_out = c->ring_v;
     const int64_t in_off = (int64_t)(s0 - seq_begin) * per_seq_elems * c->esize;
@@ -581,7 +589,6 @@ static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v
                   (long long)c->total[b], (long long)n_tokens, (long long)c->cap[b]);
   }
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (c->segmented) return append_segmented(c, new_k, new_v, n_tokens, seq_begin, n_seqs, s);
   // a sequence that starts from empty (new, or released) starts its range
   // maxima afresh: one memset per run of such sequences, before any launch
   for (int b = seq_begin; b < seq_begin + n_seqs;) {
@@ -596,6 +603,7 @@ static kvq_status append_impl(kvq_cache* c, const void* new_k, const void* new_v
     if (err != cudaSuccess) return cuda_fail(err, "range reset");
     b = e;
   }
+  if (c->segmented) return append_segmented(c, new_k, new_v, n_tokens, seq_begin, n_seqs, s);
   const int64_t R = c->cfg.residual_len, G = c->cfg.group;
   const int64_t per_seq_elems = (int64_t)c->cfg.n_kv_heads * n_tokens * c->cfg.head_dim;
   // groups each sequence flushes in this call
@@ -733,11 +741,13 @@ static kvq_status decode_impl(kvq_cache* c, const void* q, float* out, void* str
   if (!aligned16(q) || !aligned16(out)) return fail(KVQ_EINVAL, "q / out must be 16-byte aligned device pointers");
   const int kernel = opts ? opts->kernel : 0;
   if (kernel < 0 || kernel > 4) return fail(KVQ_EINVAL, "unknown kernel choice %d", kernel);
+  // (a segmented cache: 4-bit codes, in 32-token tiles)
   const bool mma_ok = c->cfg.dtype == KVQ_BF16 && (c->cfg.head_dim == 64 || c->cfg.head_dim == 128) &&
-                      c->cfg.group % 32 == 0 && c->g >= 2;
+                      (c->segmented ? c->bits == 4 : c->cfg.group % 32 == 0) && c->g >= 2;
   if (kernel == 2 && !mma_ok)
     return fail(KVQ_EUNSUPPORTED,
-                "tensor-core kernel needs bf16, head_dim 64/128, group %% 32 == 0 and >= 2 query heads per KV head");
+                "tensor-core kernel needs bf16, head_dim 64/128, group %% 32 == 0 (segmented: 4-bit codes) and >= 2 "
+                "query heads per KV head");
   const bool tc_ok = mma_ok && c->cfg.head_dim == 128 && c->bits == 4 && !c->segmented;
   if (kernel == 3 && !tc_ok)
     return fail(KVQ_EUNSUPPORTED,

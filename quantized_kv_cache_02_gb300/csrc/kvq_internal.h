@@ -91,7 +91,7 @@ struct SegArrays {
   float* kscales;              // [batch][Hkv][cap][D]; a segment's row at its first token
   float* vscales;              // [batch][Hkv][cap]
   int32_t* first;              // [batch][cap]: first token of each token's segment
-  int64_t cap;                 // token rows per unit
+  int64_t cap;                 // token rows per unit (a multiple of 32)
   int32_t row_bytes;           // D * bits / 8
 };
 
@@ -100,6 +100,7 @@ struct SegFlushParams {
   float eps;
   SegArrays seg;
   uint32_t* kmax;              // [batch][Hkv][D] bits of the segment's Key absmax (zeroed first)
+  uint32_t* range;             // [batch][Hkv][2]: largest flushed Key / Value absmax (as AppendParams::range)
   const void* ring_k;          // [batch][Hkv][R][D] (the window before the append)
   const void* ring_v;
   void* ring_k_out;            // the same rings (written by the window pass only)

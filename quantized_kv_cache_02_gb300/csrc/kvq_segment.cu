@@ -106,11 +106,17 @@ __global__ void __launch_bounds__(kSegThreads) seg_pass1_kernel(const SegFlushPa
   // ---- Keys: this chunk's per-channel absmax into the segment's maxima ------
   load_rows<T>(tile, p, i, h, t_begin, cnt, T0);
   __syncthreads();
+  float amax = 0.f;
   for (int c = threadIdx.x; c < D; c += blockDim.x) {
     float a = 0.f;
     for (int r = 0; r < cnt; ++r) a = fmaxf(a, fabsf(tile[r * D + c]));
     atomicMax(p.kmax + unit * D + c, __float_as_uint(a));
+    amax = fmaxf(amax, a);
   }
+  // the unit's largest flushed Key absmax, for the decode's range test
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0 && amax > 0.f) atomicMax(p.range + 2 * unit, __float_as_uint(amax));
   __syncthreads();
   // ---- Values: per-token scale and codes --------------------------------
   SegFlushParams q = p;
@@ -127,6 +133,7 @@ __global__ void __launch_bounds__(kSegThreads) seg_pass1_kernel(const SegFlushPa
     if (lane == 0) {
       sV[r] = __fdiv_rn(qmax, fmaxf(a, p.eps));
       p.seg.vscales[unit * p.seg.cap + t_begin + r] = sV[r];
+      if (a > 0.f) atomicMax(p.range + 2 * unit + 1, __float_as_uint(a));
     }
   }
   __syncthreads();

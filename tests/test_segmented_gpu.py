@@ -72,12 +72,13 @@ class SegPair:
         np.testing.assert_array_equal(got["window_v"], self.state["value_residual"][0, h])
         return got
 
-    def attend(self, q):
+    def attend(self, q, kernels=(0,)):
         qd = self.torch.from_numpy(np.ascontiguousarray(q[None])).to("cuda").to(self.tdt).contiguous()
-        got = self.cache.decode_attention(qd).cpu().numpy()[0].astype(np.float64)
         ref = O.decode_attention(self.state, q[None])[0]
-        excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
-        assert excess.max() <= 0, f"|d| {np.abs(got - ref).max():.3e}"
+        for kernel in kernels:
+            got = self.cache.decode_attention(qd, kernel=kernel).cpu().numpy()[0].astype(np.float64)
+            excess = np.abs(got - ref) - (ATOL + RTOL * np.abs(ref))
+            assert excess.max() <= 0, f"kernel {kernel}: |d| {np.abs(got - ref).max():.3e}"
 
 
 # ---- the page's mechanism checks, on the GPU path --------------------------
@@ -207,3 +208,55 @@ def test_segment_head_groups(kvq, torch, dtype, D, Hkv, Hq):
     for h in range(Hkv):
         pair.check_unit(h)
     assert pair.cache.device_status() == 0
+
+
+@pytest.mark.parametrize("D,Hkv,Hq", [(128, 2, 8), (128, 2, 16), (64, 2, 4), (128, 1, 8)])
+def test_segment_tensor_cores(kvq, torch, D, Hkv, Hq):
+    """4-bit bf16 segmented caches on the tensor-core kernel (kernel 2; the
+    automatic choice, 0, takes it too) and on the CUDA-core kernel (1): a long
+    first segment (whole 32-token tiles on the tensor cores), its partial last
+    tile, one-token segments (tiles of many Key scale rows, on the CUDA cores
+    inside the same kernel), segments that begin and end inside a tile, and a
+    decode after each kind of append."""
+    R = 64
+    spec = gen.InputSpec(seed=47, n_kv_heads=Hkv, n_q_heads=Hq, head_dim=D, spikes=True)
+    pair = SegPair(kvq, torch, Hkv, Hq, D, R, qmax=7, capacity=2400, dtype="bf16")
+    t = 0
+    for n in [700] + [1] * 37 + [45, 1, 1, 1, 1, 333, 96, 1, 1, 640]:
+        k, v = spec.kv_block(0, [0], t, n)
+        t += n
+        pair.append(k[0], v[0])
+        if n != 1 or t % 9 == 0:
+            pair.attend(spec.q_block(0, [0], t)[0], kernels=(0, 1, 2))
+    for h in range(Hkv):
+        pair.check_unit(h)
+    assert pair.cache.device_status() == 0
+
+
+def test_segment_tensor_cores_batch(kvq, torch):
+    """A batch of segmented sequences of different lengths (one empty, one
+    with only a window) on the tensor-core kernel against the oracle."""
+    H, Hq, D, R = 4, 16, 128, 64
+    lens = [[1000, 1, 1, 70], [], [30], [64, 1, 1, 1, 2000]]
+    spec = gen.InputSpec(seed=48, n_kv_heads=H, n_q_heads=Hq, head_dim=D, spikes=True)
+    cache = kvq.KVQCache(len(lens), H, Hq, D, R, 8, 7, [sum(x) + 8 for x in lens], segmented=True)
+    states = [None] * len(lens)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda().bfloat16()
+    for b, chunks in enumerate(lens):
+        t = 0
+        for n in chunks:
+            k, v = spec.kv_block(0, [b], t, n)
+            t += n
+            cache.append(dev(k), dev(v), b)
+            states[b] = O.append_and_partition(states[b], k, v, R, 7, group=None)
+    q = spec.q_block(0, range(len(lens)), 0)
+    for kernel in (0, 2):
+        got = cache.decode_attention(dev(q), kernel=kernel).cpu().numpy().astype(np.float64)
+        for b in range(len(lens)):
+            if states[b] is None:
+                assert not got[b].any()
+                continue
+            ref = O.decode_attention(states[b], q[b][None])[0]
+            excess = np.abs(got[b] - ref) - (ATOL + RTOL * np.abs(ref))
+            assert excess.max() <= 0, f"kernel {kernel} seq {b}: |d| {np.abs(got[b] - ref).max():.3e}"
+    assert cache.device_status() == 0
