@@ -605,6 +605,32 @@ def foil_layer(torch, cache, q, w, B, H, D, stream, peak, iters=20):
                     "path would cost"}
 
 
+def run_variant(args):
+    """One of the one-layer measurements alone (for profiling it): prints one
+    JSON line with the variant's figures."""
+    import torch
+
+    import quantized_kv_cache_02_gb300 as kvq
+    from kvq_inputs.device import DeviceInputs
+    from kvq_inputs.gen import InputSpec
+    kvq.load_library()
+    w = dict(WORKLOAD)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    dev = DeviceInputs(InputSpec(seed=w["seed"], n_kv_heads=w["n_kv_heads"], n_q_heads=w["n_q_heads"],
+                                 head_dim=w["head_dim"]))
+    run = {"segmented": lambda: segmented_layer(torch, kvq, w, dev, peak),
+           "b1": lambda: single_layer_b1(torch, kvq, peak),
+           "long_video": lambda: long_video_layer(torch, kvq, peak),
+           "ragged": lambda: ragged_8bit_layer(torch, kvq, peak)}[args.variant]
+    print(json.dumps({"variant": args.variant, **run()}), flush=True)
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -911,11 +937,15 @@ def main():
     ap.add_argument("--kernel", type=int, default=0, choices=[0, 2, 3, 4],
                     help="split kernel: 0 = automatic (mma.sync at this shape), 2 = mma.sync, 3 = tcgen05, "
                          "4 = persistent-warp mma.sync")
+    ap.add_argument("--variant", choices=["segmented", "b1", "long_video", "ragged"], default=None,
+                    help="run only this one-layer measurement (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         raise SystemExit("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.variant:
+        run_variant(args)
     else:
         run_ours(args)
 

@@ -260,3 +260,27 @@ def test_segment_tensor_cores_batch(kvq, torch):
             excess = np.abs(got[b] - ref) - (ATOL + RTOL * np.abs(ref))
             assert excess.max() <= 0, f"kernel {kernel} seq {b}: |d| {np.abs(got[b] - ref).max():.3e}"
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("vmag,kmag", [(6e4, 1.0), (1.0, 1e6), (300.0, 1e4)])
+def test_segment_tensor_cores_input_range(kvq, torch, vmag, kmag):
+    """Inputs beyond the tensor-core operands' range on a segmented cache
+    (Value rows of absmax up to 6e4; Key spikes up to 1e6 against q x 24):
+    the segment flush records the unit's maxima and the decode takes the
+    CUDA-core path for such units inside the same launch; every kernel
+    against the oracle."""
+    Hkv, Hq, D, R = 2, 8, 128, 64
+    spec = gen.InputSpec(seed=49, n_kv_heads=Hkv, n_q_heads=Hq, head_dim=D)
+    pair = SegPair(kvq, torch, Hkv, Hq, D, R, qmax=7, capacity=1200, dtype="bf16")
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).bfloat16().float().numpy()
+    t = 0
+    for n in [600, 1, 1, 200]:
+        k, v = spec.kv_block(0, [0], t, n)
+        k, v = k[0].copy(), v[0].copy()
+        v[:, ::8] *= vmag                  # every 8th token
+        k[:, ::5, 3] *= kmag               # one channel of every 5th token
+        t += n
+        pair.append(bf(k), bf(v))
+        q = spec.q_block(0, [0], t)[0] * (24.0 if kmag > 1 else 1.0)
+        pair.attend(bf(q), kernels=(0, 1, 2))
+    assert pair.cache.device_status() == 0
