@@ -1027,14 +1027,12 @@ __device__ __noinline__ void seg_tile_cuda_cores(const DecodeParams& p, const ui
 // which itself waits on global loads.  Lane 0 of each warp therefore asks L2
 // for the warp's first pages before that set-up (whole pages of a contiguous
 // G = 32 cache), so the copies then hit L2.
-template <int D>
-__device__ __forceinline__ void prefetch_first_pages(const DecodeParams& p, int b, int h, int pg0, int pg1, int warp,
-                                                  int n) {
-  const int64_t stored = p.geom.page_bytes;
+__device__ __forceinline__ void prefetch_first_pages(const uint8_t* unit_pages, int64_t stored, int pg0, int pg1,
+                                                     int warp, int n) {
   for (int k = 0; k < n; ++k) {
     const int pg = pg0 + warp + k * kMmaWarps;
     if (pg >= pg1) break;
-    prefetch_l2(p.pages + page_offset(p.map, stored, b, h, pg), (uint32_t)stored);
+    prefetch_l2(unit_pages + (int64_t)pg * stored, (uint32_t)stored);
   }
 }
 
@@ -1118,6 +1116,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   const int col = blockIdx.x / n_units;
   const int u = blockIdx.x - col * n_units;
   const int i = u / p.Hkv, h = u - i * p.Hkv;
+  const int b = p.seq_begin + i;
   bool win;
   int pg0, pg1, slot;
   if (p.done && col == 0 && p.ctr[i].total == 0) {
@@ -1130,7 +1129,6 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
-  const int b = p.seq_begin + i;
   const int g = p.g;
   // Ring slots hold 32-token units.  With G = 32 a unit is a whole page (one
   // bulk copy); with a larger G it is the unit's Key rows, Value sub-tile,
@@ -1159,15 +1157,24 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   if (win) {
     window_rows<D, GP>(p, i, h, lane, warp, gid, tig, buf, st);
   } else {
-  if (MODE == kFlat32 && lane == 0 && pg1 - pg0 <= kShortItemPages)
-    prefetch_first_pages<D>(p, b, h, pg0, pg1, warp, slots);
-  // the unit's flushed maxima for the range test below, loaded with the queries
-  float kabs = 0.f, vabs = 0.f;
-  if (p.range) {
-    const uint2 r = *reinterpret_cast<const uint2*>(p.range + 2 * ((int64_t)b * p.Hkv + h));
-    kabs = __uint_as_float(r.x);
-    vabs = __uint_as_float(r.y);
+  // The loads that depend only on the unit go out first, all at once: the
+  // unit's flushed maxima, this thread's 8 query channels and (contiguous
+  // G = 32) its page base; a short decode would otherwise wait on each in turn.
+  uint2 rng = make_uint2(0u, 0u);
+  if (p.range) rng = __ldg(reinterpret_cast<const uint2*>(p.range + 2 * ((int64_t)b * p.Hkv + h)));
+  static_assert(GP * D / 8 <= kMmaThreads, "one 16-byte query load a thread");
+  uint4 qraw = make_uint4(0u, 0u, 0u, 0u);
+  if (threadIdx.x < GP * D / 8) {
+    const int n = threadIdx.x / (D / 8), c0 = (threadIdx.x - n * (D / 8)) * 8;
+    qraw = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                                ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D + c0));
   }
+  int64_t unit_base = 0;
+  if (MODE == kFlat32) unit_base = p.map.layout[b].page_base + h * p.map.layout[b].unit_stride;
+  if (MODE == kFlat32 && lane == 0 && pg1 - pg0 <= kShortItemPages)
+    prefetch_first_pages(p.pages + unit_base, (int64_t)p.geom.page_bytes, pg0, pg1, warp, slots);
+  // the unit's flushed maxima, for the range test below
+  const float kabs = __uint_as_float(rng.x), vabs = __uint_as_float(rng.y);
   // queries of the GP column heads (head n % g for the padding columns, so every
   // value stays finite), pre-scaled, in shared memory: channel c of head n goes
   // to float4 ((i * GP + n) * 4 + tig) with tig = c / (D/4), i = (c % (D/4)) / 4,
@@ -1175,14 +1182,11 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   // (8 channels a thread from one 16-byte load, every load of the CTA in
   // flight at once)
   float qa = 0.f;
-#pragma unroll
-  for (int x0 = 0; x0 < GP * D / 8; x0 += kMmaThreads) {
-    const int x = x0 + threadIdx.x;
-    if (GP * D / 8 % kMmaThreads == 0 || x < GP * D / 8) {
+  {
+    const int x = threadIdx.x;
+    if (x < GP * D / 8) {
       const int n = x / (D / 8), c0 = (x - n * (D / 8)) * 8;
-      const uint4 raw = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                                        ((int64_t)b * p.Hq + (int64_t)h * g + n % g) * D + c0);
-      const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+      const __nv_bfloat162* q2 = reinterpret_cast<const __nv_bfloat162*>(&qraw);
       float qv[8];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -1221,7 +1225,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
   // source of this warp's pos-th unit (units u0 + warp, + 4, ...), through
   // the block table for a paged cache
   const int64_t stored = geom.page_bytes;
-  const uint8_t* unit_pages = MODE == kFlat32 ? p.pages + page_offset(p.map, stored, b, h, 0) : p.pages;
+  const uint8_t* unit_pages = MODE == kFlat32 ? p.pages + unit_base : p.pages;
   auto page_src = [&](int pg) {
     return MODE == kFlat32 ? unit_pages + (int64_t)pg * stored : p.pages + page_offset(p.map, stored, b, h, pg);
   };
