@@ -276,6 +276,11 @@ kvq_status kvq_append(kvq_cache* cache, const void* new_k, const void* new_v, in
 /* Decode attention for every sequence: q device [batch][n_q_heads][head_dim] of
  * the cache dtype; out device float [batch][n_q_heads][head_dim].  A sequence
  * with no tokens yields zeros.  Uses the arena's split scratch region.
+ * Launches: a split kernel (one per 256 sequences) and a combine kernel after
+ * it, except for a short decode on the tensor-core kernel (one wave of the
+ * resident CTAs, split items of at most 16 32-token units, e.g. a single
+ * sequence), whose last CTA per (sequence, KV head) merges the partials
+ * itself (an arrival count in the arena, back to 0 when the launch ends).
  *
  * Input range.  Any finite Key, Value and query values are accepted; scales
  * below eps (absmax > qmax / eps) restore as code / eps, as the page's restore
