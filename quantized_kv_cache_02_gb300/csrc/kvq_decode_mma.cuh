@@ -1507,11 +1507,16 @@ cudaError_t launch_dense_g(const DecodeParams& p, int cols, cudaStream_t s) {
 }
 
 // Shared-memory page slots per warp: about 60 KB of pages per CTA, at least
-// one group (8 / padded g pages) and at most 8.
+// one group (8 / padded g pages) and at most 8.  Slots above 6 KB (8-bit
+// codes) get one page beyond a group even though the CTA then needs more
+// shared memory (2 CTAs per SM instead of 3): with one group's slots only,
+// no copy is in flight while a group is computed (the 8-bit ragged decode:
+// 171.5 -> 155.1 us).
 int mma_slots(int64_t page_bytes, int g) {
   const int pb = 8 / gqa_pad(g);
   int slots = (int)(60 * 1024 / (kMmaWarps * page_bytes));
   if (slots < pb) slots = pb;
+  if (page_bytes > 6144 && slots < pb + 1) slots = pb + 1;
   if (slots > 8) slots = 8;
   return slots;
 }
