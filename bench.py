@@ -526,6 +526,18 @@ def long_video_layer(torch, kvq, peak):
     H, Hq, D, R, G = v["n_kv_heads"], v["n_q_heads"], v["head_dim"], v["residual_len"], v["group"]
     T = v["chunk"] * v["chunks"]
     dev = DeviceInputs(InputSpec(seed=v["seed"], n_kv_heads=H, n_q_heads=Hq, head_dim=D))
+    # warm-up on a small cache of the same configuration: the first launch of
+    # each kernel instance loads it, which must not land in the timed region
+    warm = kvq.KVQCache(1, H, Hq, D, R, G, v["qmax"], 4 * v["chunk"])
+    wo = torch.empty(1, Hq, D, dtype=torch.float32, device="cuda")
+    for c in range(3):
+        K, V = dev.kv_block(1, 0, 1, c * v["chunk"], v["chunk"])
+        warm.append(K, V, 0)
+        K1, V1 = dev.kv_block(1, 0, 1, 3 * v["chunk"] + c, 1)
+        warm.append(K1, V1, 0)
+        warm.decode_attention(dev.q_block(1, 0, 1, c), out=wo)
+    torch.cuda.synchronize()
+    del warm
     cache = kvq.KVQCache(1, H, Hq, D, R, G, v["qmax"], T + v["decode_steps"] + 8)
     chunks = [dev.kv_block(0, 0, 1, c * v["chunk"], v["chunk"]) for c in range(v["chunks"])]
     torch.cuda.synchronize()

@@ -109,6 +109,20 @@ __device__ __forceinline__ void unpack16(const uint4& raw, float (&x)[8]) {
   }
 }
 
+// Absolute values of two bf16 packed in a word, as 16-bit unsigned integers:
+// for values >= 0 the bit patterns order like the values, so a per-halfword
+// unsigned max is the max of |x|, and the fp32 absmax of a half h is the float
+// with bits h << 16.  Two channels (or tokens) a pair of instructions, with no
+// conversion to fp32 until the final maximum.
+__device__ __forceinline__ uint32_t abs_bf16x2(uint32_t w) { return w & 0x7FFF7FFFu; }
+__device__ __forceinline__ uint32_t umax_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float bf16_lo_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f32(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
 // N consecutive elements of shared memory as fp32 (vector loads)
 template <typename T, int N>
 __device__ __forceinline__ void load_elems(const T* src, float (&x)[N]) {
@@ -282,11 +296,27 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
     if (p.v_prefetch) {
       asm volatile("cp.async.wait_group 1;\n" ::: "memory");  // this thread's Key rows
       if (act) {
-        for (int r = r0; r < G; r += rows_per_pass) {
-          float x[kVec];
-          unpack16(*reinterpret_cast<const uint4*>(tileT + (size_t)r * D + col), x);
+        if constexpr (sizeof(T) == 2) {
+          uint32_t am[4] = {0u, 0u, 0u, 0u};  // |x| of channels col + 2k (low half), + 2k + 1 (high)
+          for (int r = r0; r < G; r += rows_per_pass) {
+            const uint4 v = *reinterpret_cast<const uint4*>(tileT + (size_t)r * D + col);
+            am[0] = umax_u16x2(am[0], abs_bf16x2(v.x));
+            am[1] = umax_u16x2(am[1], abs_bf16x2(v.y));
+            am[2] = umax_u16x2(am[2], abs_bf16x2(v.z));
+            am[3] = umax_u16x2(am[3], abs_bf16x2(v.w));
+          }
 #pragma unroll
-          for (int e = 0; e < kVec; ++e) amax[e] = fmaxf(amax[e], fabsf(x[e]));
+          for (int k = 0; k < 4; ++k) {
+            amax[2 * k] = bf16_lo_f32(am[k]);
+            amax[2 * k + 1] = bf16_hi_f32(am[k]);
+          }
+        } else {
+          for (int r = r0; r < G; r += rows_per_pass) {
+            float x[kVec];
+            unpack16(*reinterpret_cast<const uint4*>(tileT + (size_t)r * D + col), x);
+#pragma unroll
+            for (int e = 0; e < kVec; ++e) amax[e] = fmaxf(amax[e], fabsf(x[e]));
+          }
         }
       }
     } else {
@@ -376,9 +406,21 @@ __global__ void __launch_bounds__(kAppendThreads, 4) append_kernel(const AppendP
           const int r = base + r0 + k * rows_per_pass;
           const uint4 v = act && r < G ? *reinterpret_cast<const uint4*>(tileV + (size_t)r * D + col)
                                        : make_uint4(0u, 0u, 0u, 0u);
-          float x[kVec];
-          unpack16(v, x);
-          row_max(r, x);
+          if constexpr (sizeof(T) == 2) {
+            // the row's |x| maximum over this thread's 8 channels, packed, then
+            // as the same one-element row_max input
+            const uint32_t m2 = umax_u16x2(umax_u16x2(abs_bf16x2(v.x), abs_bf16x2(v.y)),
+                                           umax_u16x2(abs_bf16x2(v.z), abs_bf16x2(v.w)));
+            float x[kVec];
+            x[0] = fmaxf(bf16_lo_f32(m2), bf16_hi_f32(m2));
+#pragma unroll
+            for (int e = 1; e < kVec; ++e) x[e] = 0.f;
+            row_max(r, x);
+          } else {
+            float x[kVec];
+            unpack16(v, x);
+            row_max(r, x);
+          }
         }
       }
     } else {
