@@ -1036,6 +1036,15 @@ __device__ __forceinline__ void prefetch_first_pages(const uint8_t* unit_pages, 
   }
 }
 
+// The CUDA-core path of an item the range test sends there, kept out of line
+// so that the page loop's code stays compact (the layer's split 76.2 -> 75.8
+// us, measured).
+template <int BITS, int D, bool SEG>
+__device__ __noinline__ void range_fallback(const DecodeParams& p, int i, int h, int pg0, int pg1, int slot,
+                                            float* scratch) {
+  simt_item<__nv_bfloat16, BITS, D / 32, SEG>(p, i, h, false, pg0, pg1, slot, scratch);
+}
+
 // The combine inside the split launch (DecodeParams::done): after its partial
 // is written, a CTA counts itself finished for its unit, and the CTA that
 // finishes the unit's last item merges the unit's g query heads (one warp
@@ -1215,8 +1224,7 @@ __global__ void __launch_bounds__(kMmaThreads, 3) decode_mma_kernel(const Decode
     const int qexp = float_exp2i(qa);
     const float kthr = fmaxf(pow2i(BITS == 2 ? qexp + 1 + 4 - 14 : qexp + 1 - 9), p.eps);
     if (!(fmaxf(kabs, p.eps) * kthr <= (float)p.qmax * 0.9999f && vabs <= kVWideAbs * 0.999f)) {
-      simt_item<__nv_bfloat16, BITS, D / 32, MODE == kSeg32>(p, i, h, false, pg0, pg1, slot,
-                                                            reinterpret_cast<float*>(buf));
+      range_fallback<BITS, D, MODE == kSeg32>(p, i, h, pg0, pg1, slot, reinterpret_cast<float*>(buf));
       if (p.done) finish_unit<D>(p, i, h);
       return;
     }
